@@ -1,0 +1,163 @@
+"""Reference oracle for RoPE + causal softmax attention (CPU, IEEE double).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU-baseline leg may use
+this package; the library's product path never imports it.  It shares no code with the CUDA path.
+
+The arithmetic lives in ``rope_causal_oracle.c`` (plain C loops, fp64, threaded over rows).  This
+module compiles it with the host C compiler into ``oracle/_build/`` and marshals arrays through
+ctypes.  What it computes, and the passages it follows, are stated in that file's header:
+
+* RoPE as a pre-multiplication transform on Q and K ("AttnFuse Makes RoPE a First-Class Attention
+  Compilation Operation", 2026-09-13 AI papers report, paragraph 1; AttnFuse abstract), half-split
+  pairs (k, k+d/2), theta_k = base^(-2k/d), position = token index;
+* causal softmax attention (same report, paragraph 2: causality and softmax building blocks),
+  scale 1/sqrt(d), natural-log log-sum-exp per row, GQA head h -> kv head floor(h*Hkv/Hq).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rope_causal_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+ORC_F64, ORC_BF16, ORC_F16 = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain IEEE: no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.orc_rope_rotate.restype = ctypes.c_int
+            lib.orc_rope_rotate.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p, ctypes.c_int]
+            lib.orc_rope_causal.restype = ctypes.c_int
+            lib.orc_rope_causal.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _as_raw(x):
+    """Return (contiguous numpy buffer, dtype code).  Accepts torch CPU tensors (bf16/fp16/fp64) or numpy."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(x, torch.Tensor):
+        x = x.detach().cpu().contiguous()
+        if x.dtype == torch.bfloat16:
+            return x.view(torch.int16).numpy().view(np.uint16), ORC_BF16
+        if x.dtype == torch.float16:
+            return x.view(torch.int16).numpy().view(np.uint16), ORC_F16
+        if x.dtype == torch.float64:
+            return x.numpy(), ORC_F64
+        raise TypeError(f"oracle accepts bf16, fp16 or fp64 tensors, got {x.dtype}")
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float64:
+        return x, ORC_F64
+    if x.dtype == np.float16:
+        return x.view(np.uint16), ORC_F16
+    raise TypeError(f"oracle accepts float64/float16 arrays or torch bf16/fp16/fp64 tensors, got {x.dtype}")
+
+
+def rope_rotate(x, base: float, positions=None, threads: int | None = None) -> np.ndarray:
+    """Rotate x of shape [..., R, H, d] (R rows of H heads); row r sits at positions[r] (default: r).
+
+    Leading dimensions are flattened into rows, so for [B, N, H, d] the default position of (b, n) is
+    n only when B == 1; pass ``positions`` explicitly (or use :func:`rope_rotate_bnhd`) otherwise.
+    """
+    raw, dt = _as_raw(x)
+    shape = raw.shape
+    if len(shape) < 2:
+        raise ValueError("x must have at least 2 dims [..., H, d]")
+    H, d = shape[-2], shape[-1]
+    rows = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+    if positions is None:
+        pos = np.arange(rows, dtype=np.float64)
+    else:
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.float64).reshape(-1))
+        if pos.size != rows:
+            raise ValueError(f"positions has {pos.size} entries for {rows} rows")
+    out = np.empty(shape, dtype=np.float64)
+    rc = _load().orc_rope_rotate(raw.ctypes.data, dt, rows, H, d, pos.ctypes.data, float(base), out.ctypes.data,
+                                 int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("orc_rope_rotate failed")
+    return out
+
+
+def rope_rotate_bnhd(x, base: float, threads: int | None = None) -> np.ndarray:
+    """Rotate x of shape [B, N, H, d] with position = token index n (the library's convention)."""
+    B, N = x.shape[0], x.shape[1]
+    pos = np.tile(np.arange(N, dtype=np.float64), B)
+    return rope_rotate(x, base, positions=pos, threads=threads)
+
+
+def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None):
+    """Causal softmax attention with RoPE on q and k.
+
+    q: [B, N, Hq, d]; k, v: [B, N, Hkv, d] (same dtype: bf16/fp16 torch tensors, fp16 or fp64 arrays).
+    rows: optional 1-D sequence of query positions to evaluate (default: all N in order).
+    Returns (out [B, R, Hq, d] float64, lse [B, Hq, R] float64) with R = len(rows) or N.
+    """
+    qr, dq = _as_raw(q)
+    kr, dk = _as_raw(k)
+    vr, dv = _as_raw(v)
+    if not (dq == dk == dv):
+        raise TypeError("q, k, v must share one dtype")
+    if qr.ndim != 4 or kr.ndim != 4 or vr.ndim != 4:
+        raise ValueError("q, k, v must be 4-D [B, N, H, d]")
+    B, N, Hq, d = qr.shape
+    Hkv = kr.shape[2]
+    if kr.shape != (B, N, Hkv, d) or vr.shape != (B, N, Hkv, d):
+        raise ValueError("k and v must be [B, N, Hkv, d] matching q")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if rows is None:
+        sel_ptr, n_sel, sel = None, N, None
+    else:
+        sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        if sel.size and (sel.min() < 0 or sel.max() >= N):
+            raise ValueError("rows out of range")
+        sel_ptr, n_sel = sel.ctypes.data, int(sel.size)
+    out = np.zeros((B, n_sel, Hq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq, n_sel), dtype=np.float64)
+    if n_sel == 0:
+        return out, lse
+    rc = _load().orc_rope_causal(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, dq, B, Hq, Hkv, N, d, float(base),
+                                 sel_ptr, n_sel, out.ctypes.data, lse.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("orc_rope_causal failed")
+    return out, lse

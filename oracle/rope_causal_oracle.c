@@ -1,0 +1,269 @@
+/*
+ * Reference oracle for causal softmax attention with Rotary Position Embedding (RoPE).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously-correct definition that the
+ * CUDA path is checked against.  Only the test suite, the smoke check and the CPU-baseline leg of
+ * the benchmark may build, load or call it; the library's product path never does.  It shares no
+ * code, header, table or constant with the CUDA sources.
+ *
+ * What it computes (all arithmetic in IEEE double, no blocking, no fusion, no reordering):
+ *
+ *   RoPE, half-split pairing.  "AttnFuse Makes RoPE a First-Class Attention Compilation Operation"
+ *   (2026-09-13 AI papers report), paragraph 1, and the AttnFuse abstract (arxivdaily 2609.13612):
+ *   RoPE is a transformation applied to Q and K *before* the QK^T product.  The pages name RoPE
+ *   but print no formula; this library fixes the common half-split convention:
+ *       theta_k = base^(-2k/d),                 k = 0 .. d/2-1
+ *       x'[k]       = x[k]       cos(p theta_k) - x[k+d/2] sin(p theta_k)
+ *       x'[k+d/2]   = x[k+d/2]   cos(p theta_k) + x[k]     sin(p theta_k)
+ *   with p the token index.  V is not rotated.
+ *
+ *   Causal softmax attention.  Same report, paragraph 2 (causality and softmax building blocks):
+ *       s_ij = (q'_i . k'_j) / sqrt(d)      for j <= i   (keys j > i are excluded)
+ *       o_i  = sum_j softmax_j(s_ij) v_j
+ *       lse_i = max_j s_ij + ln sum_j exp(s_ij - max_j s_ij)     (natural log)
+ *   GQA: query head h reads key/value head floor(h / (Hq/Hkv)).
+ *
+ * Layouts (row-major, contiguous): q, out [B, N, Hq, d]; k, v [B, N, Hkv, d]; lse [B, Hq, N].
+ * Inputs may be raw bf16 or fp16 bit patterns (decoded exactly to double here) or doubles.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F64 = 0, ORC_BF16 = 1, ORC_F16 = 2 };
+
+/* bf16 is the upper half of an IEEE binary32: widen and reinterpret (exact). */
+static double decode_bf16(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits (exact). */
+static double decode_f16(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int m = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24); /* subnormal: m * 2^-14 / 2^10 */
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(m | 0x400), e - 25); /* (1024 + m) * 2^(e - 15 - 10) */
+  return sign ? -v : v;
+}
+
+static double load_elem(const void *p, int dtype, size_t idx) {
+  if (dtype == ORC_F64) return ((const double *)p)[idx];
+  uint16_t h = ((const uint16_t *)p)[idx];
+  return dtype == ORC_BF16 ? decode_bf16(h) : decode_f16(h);
+}
+
+/* theta_k = base^(-2k/d) for k in [0, d/2). */
+static void rope_frequencies(int d, double base, double *theta) {
+  for (int k = 0; k < d / 2; ++k) theta[k] = pow(base, -2.0 * (double)k / (double)d);
+}
+
+/* Rotate one head vector x[0..d) that sits at position pos (half-split pairs). */
+static void rope_rotate_vec(const double *x, double *y, int d, double pos, const double *theta) {
+  int half = d / 2;
+  for (int k = 0; k < half; ++k) {
+    double angle = pos * theta[k];
+    double c = cos(angle), s = sin(angle);
+    double a = x[k], b = x[k + half];
+    y[k] = a * c - b * s;
+    y[k + half] = b * c + a * s;
+  }
+}
+
+/* ------------------------------------------------------------------------------------------- */
+/* A tiny work queue over pthreads: items [0, n_items) are claimed one at a time.               */
+
+typedef struct {
+  void (*fn)(void *ctx, int64_t item, double *scratch);
+  void *ctx;
+  int64_t n_items;
+  int64_t next; /* claimed with an atomic fetch-add */
+  size_t scratch_doubles;
+  int failed;
+} orc_pool_t;
+
+static void *orc_worker(void *arg) {
+  orc_pool_t *pool = (orc_pool_t *)arg;
+  double *scratch = (double *)malloc(sizeof(double) * (pool->scratch_doubles ? pool->scratch_doubles : 1));
+  if (!scratch) {
+    __atomic_store_n(&pool->failed, 1, __ATOMIC_SEQ_CST);
+    return NULL;
+  }
+  for (;;) {
+    int64_t item = __atomic_fetch_add(&pool->next, 1, __ATOMIC_SEQ_CST);
+    if (item >= pool->n_items) break;
+    pool->fn(pool->ctx, item, scratch);
+  }
+  free(scratch);
+  return NULL;
+}
+
+static int orc_run(orc_pool_t *pool, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 1024) nthreads = 1024;
+  pool->next = 0;
+  pool->failed = 0;
+  pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!tids) return -1;
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&tids[t], NULL, orc_worker, pool) != 0) break;
+    ++started;
+  }
+  if (started == 0) orc_worker(pool); /* no thread could start: do the work here */
+  for (int t = 0; t < started; ++t) pthread_join(tids[t], NULL);
+  free(tids);
+  return pool->failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------------- */
+/* Public entry 1: rotate x[rows, H, d] where row r sits at position positions[r].              */
+
+typedef struct {
+  const void *x;
+  int dtype;
+  int H, d;
+  const double *positions;
+  const double *theta;
+  double *out;
+} rot_ctx_t;
+
+static void rot_item(void *vctx, int64_t r, double *scratch) {
+  rot_ctx_t *c = (rot_ctx_t *)vctx;
+  for (int h = 0; h < c->H; ++h) {
+    size_t base = ((size_t)r * c->H + h) * c->d;
+    for (int e = 0; e < c->d; ++e) scratch[e] = load_elem(c->x, c->dtype, base + e);
+    rope_rotate_vec(scratch, c->out + base, c->d, c->positions[r], c->theta);
+  }
+}
+
+int orc_rope_rotate(const void *x, int dtype, int64_t rows, int H, int d, const double *positions, double base,
+                    double *out, int nthreads) {
+  if (!x || !positions || !out || rows < 0 || H < 1 || d < 2 || (d % 2) != 0) return -1;
+  double *theta = (double *)malloc(sizeof(double) * (size_t)(d / 2));
+  if (!theta) return -1;
+  rope_frequencies(d, base, theta);
+  rot_ctx_t ctx = {x, dtype, H, d, positions, theta, out};
+  orc_pool_t pool = {rot_item, &ctx, rows, 0, (size_t)d, 0};
+  int rc = orc_run(&pool, nthreads);
+  free(theta);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------------------------- */
+/* Public entry 2: causal attention with RoPE on Q and K.                                        */
+/*   sel_rows: the query positions to evaluate (NULL = all N, in order), n_sel of them.          */
+/*   out: [B, n_sel, Hq, d] doubles;  lse: [B, Hq, n_sel] doubles (may be NULL).                 */
+
+typedef struct {
+  const void *q, *v;
+  int dtype;
+  int B, Hq, Hkv, N, d;
+  const double *theta;
+  const double *krot; /* [B, N, Hkv, d] rotated keys */
+  const int64_t *sel;
+  int64_t n_sel;
+  double *out, *lse;
+} attn_ctx_t;
+
+typedef struct {
+  const void *k;
+  int dtype;
+  int Hkv, d;
+  int N;
+  const double *theta;
+  double *krot;
+} krot_ctx_t;
+
+static void krot_item(void *vctx, int64_t bn, double *scratch) {
+  krot_ctx_t *c = (krot_ctx_t *)vctx;
+  int n = (int)(bn % c->N);
+  for (int h = 0; h < c->Hkv; ++h) {
+    size_t base = ((size_t)bn * c->Hkv + h) * c->d;
+    for (int e = 0; e < c->d; ++e) scratch[e] = load_elem(c->k, c->dtype, base + e);
+    rope_rotate_vec(scratch, c->krot + base, c->d, (double)n, c->theta);
+  }
+}
+
+/* One item = one (b, h, selected row). scratch holds: raw q (d), rotated q (d), scores (N). */
+static void attn_item(void *vctx, int64_t item, double *scratch) {
+  attn_ctx_t *c = (attn_ctx_t *)vctx;
+  int64_t s = item % c->n_sel;
+  int h = (int)((item / c->n_sel) % c->Hq);
+  int b = (int)(item / (c->n_sel * c->Hq));
+  int64_t i = c->sel ? c->sel[s] : s;
+  int g = c->Hq / c->Hkv;
+  int hk = h / g; /* GQA: consecutive query heads share one key/value head */
+  int d = c->d;
+  double *qraw = scratch, *qrot = scratch + d, *score = scratch + 2 * d;
+
+  size_t qbase = (((size_t)b * c->N + (size_t)i) * c->Hq + h) * d;
+  for (int e = 0; e < d; ++e) qraw[e] = load_elem(c->q, c->dtype, qbase + e);
+  rope_rotate_vec(qraw, qrot, d, (double)i, c->theta);
+
+  double scale = 1.0 / sqrt((double)d);
+  double mx = -INFINITY;
+  for (int64_t j = 0; j <= i; ++j) { /* causal: keys j <= i only */
+    const double *kr = c->krot + (((size_t)b * c->N + (size_t)j) * c->Hkv + hk) * d;
+    double dot = 0.0;
+    for (int e = 0; e < d; ++e) dot += qrot[e] * kr[e];
+    score[j] = dot * scale;
+    if (score[j] > mx) mx = score[j];
+  }
+  double denom = 0.0;
+  for (int64_t j = 0; j <= i; ++j) {
+    score[j] = exp(score[j] - mx);
+    denom += score[j];
+  }
+  double *o = c->out + (((size_t)b * c->n_sel + (size_t)s) * c->Hq + h) * d;
+  for (int e = 0; e < d; ++e) o[e] = 0.0;
+  for (int64_t j = 0; j <= i; ++j) {
+    double p = score[j] / denom;
+    size_t vbase = (((size_t)b * c->N + (size_t)j) * c->Hkv + hk) * d;
+    for (int e = 0; e < d; ++e) o[e] += p * load_elem(c->v, c->dtype, vbase + e);
+  }
+  if (c->lse) c->lse[((size_t)b * c->Hq + h) * c->n_sel + (size_t)s] = mx + log(denom);
+}
+
+int orc_rope_causal(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
+                    double base, const int64_t *sel_rows, int64_t n_sel, double *out, double *lse, int nthreads) {
+  if (!q || !k || !v || !out || B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 2 || (d % 2) != 0 || (Hq % Hkv) != 0)
+    return -1;
+  if (!sel_rows) n_sel = N;
+  if (n_sel < 0) return -1;
+  if (sel_rows)
+    for (int64_t s = 0; s < n_sel; ++s)
+      if (sel_rows[s] < 0 || sel_rows[s] >= N) return -1;
+
+  double *theta = (double *)malloc(sizeof(double) * (size_t)(d / 2));
+  double *krot = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N * (size_t)Hkv * (size_t)d);
+  if (!theta || !krot) {
+    free(theta);
+    free(krot);
+    return -1;
+  }
+  rope_frequencies(d, base, theta);
+
+  krot_ctx_t kctx = {k, dtype, Hkv, d, N, theta, krot};
+  orc_pool_t kpool = {krot_item, &kctx, (int64_t)B * N, 0, (size_t)d, 0};
+  int rc = orc_run(&kpool, nthreads);
+
+  if (rc == 0) {
+    attn_ctx_t actx = {q, v, dtype, B, Hq, Hkv, N, d, theta, krot, sel_rows, n_sel, out, lse};
+    orc_pool_t apool = {attn_item, &actx, (int64_t)B * Hq * n_sel, 0, (size_t)(2 * d + N), 0};
+    rc = orc_run(&apool, nthreads);
+  }
+  free(theta);
+  free(krot);
+  return rc;
+}
