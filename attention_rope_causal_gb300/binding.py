@@ -1,0 +1,138 @@
+"""Thin ctypes binding over libattnfuse's C ABI (include/attnfuse.h).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current CUDA stream.  There is no CPU fallback: if the
+library is missing or the device is not sm_103a, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ATTNFUSE_FUSED, ATTNFUSE_PREROTATE = 0, 1
+ATTNFUSE_BF16, ATTNFUSE_FP16 = 0, 1
+STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_TIMEOUT", 5: "ERR_NO_MEMORY"}
+MODES = {"fused": ATTNFUSE_FUSED, "prerotate": ATTNFUSE_PREROTATE}
+DTYPES = {torch.bfloat16: ATTNFUSE_BF16, torch.float16: ATTNFUSE_FP16}
+
+# Every function the header declares, with its ctypes signature.
+_SIGNATURES = {
+    "attnfuse_rope_causal_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "attnfuse_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 7),
+    "attnfuse_rope_apply": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_void_p]),
+    "attnfuse_device_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "attnfuse_diag_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_void_p]),
+    "attnfuse_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attnfuse_last_error": (ctypes.c_char_p, []),
+    "attnfuse_version": (ctypes.c_char_p, []),
+}
+
+
+class AttnFuseError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libattnfuse.so (built by ``attention_rope_causal_gb300.build.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with attention_rope_causal_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load()
+        raise AttnFuseError(status, lib.attnfuse_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def workspace_bytes(B, Hq, Hkv, N, d, mode="fused", dtype=torch.bfloat16) -> int:
+    return int(load().attnfuse_workspace_bytes(B, Hq, Hkv, N, d, MODES[mode], DTYPES[dtype]))
+
+
+def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, lse=None, want_lse: bool = True,
+                    workspace=None, stream=None):
+    """Causal RoPE attention forward through ``attnfuse_rope_causal_fwd``.
+
+    q: [B, N, Hq, d], k/v: [B, N, Hkv, d] CUDA tensors (bf16 or fp16, contiguous).
+    Returns (out [B, N, Hq, d], lse [B, Hq, N] float32 or None).
+    """
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(load().attnfuse_rope_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
+                                           float(rope_base), MODES[mode], DTYPES[q.dtype], ws_ptr, ws_bytes,
+                                           _stream_ptr(stream)))
+    return out, lse
+
+
+def rope_apply(x, rope_base: float, out=None, stream=None):
+    """y = RoPE(x) for x [B, N, H, d] through ``attnfuse_rope_apply`` (out may be x: in place)."""
+    B, N, H, d = x.shape
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    _check(load().attnfuse_rope_apply(_ptr(x), _ptr(out), B, N, H, d, float(rope_base), DTYPES[x.dtype],
+                                      _stream_ptr(stream)))
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and read (and clear) the kernels' device status word; returns the status code."""
+    return int(load().attnfuse_device_status(_stream_ptr(stream)))
+
+
+def diag_wait_timeout(timeout_ns: int, stream=None):
+    _check(load().attnfuse_diag_wait_timeout(int(timeout_ns), _stream_ptr(stream)))
+
+
+def last_error() -> str:
+    return load().attnfuse_last_error().decode(errors="replace")

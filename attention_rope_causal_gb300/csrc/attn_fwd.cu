@@ -1,0 +1,609 @@
+// Causal softmax attention forward on sm_103a, with optional on-chip RoPE of the Q and K tiles.
+//
+// What it computes: for every batch b, query head h (KV head h / (Hq/Hkv)) and query row i,
+//   o_i = sum_{j <= i} softmax_j(q'_i . k'_j / sqrt(d)) v_j   and   lse_i = ln sum_{j<=i} exp(...),
+// where q', k' are RoPE-rotated (fused mode) or were rotated beforehand (pre-rotate mode: the
+// kernel then runs with ROTATE = false on already-rotated inputs).  RoPE is a pre-multiplication
+// transform and the causal mask and softmax are building blocks of one fused kernel ("AttnFuse Makes
+// RoPE a First-Class Attention Compilation Operation", 2026-09-13 AI papers report, paragraphs 1-2).
+// The online softmax keeps a running row max m_i and denominator l_i ("Fast and Exact
+// Relative-Position Attention via Structure-Aware Kernels", prerequisites: FlashAttention and
+// online softmax), in fp32 and with base-2 exponentials (same page, technical novelty (4)).
+//
+// Structure (one CTA = 256 query rows of one (b, h) = two 128-row tiles q0, q1; 512 threads):
+//   warp 0        TMA producer: Q once, then K and V tiles (128 keys) through 2-stage rings.
+//   warp 1        tcgen05.mma issuer; owns the tensor-memory allocation (512 columns:
+//                 S0 | S1 | O0 | O1, P_i written over the first half of S_i).
+//   warps 4-7     softmax for q0 (thread = query row = TMEM lane), epilogue for q0.
+//   warps 8-11    softmax for q1, epilogue for q1.
+//   warps 12-15   fused mode: rotate each K tile in shared memory before its QK^T MMA.
+//   (warps 4-15 also rotate the Q tiles once, at the start, in fused mode.)
+// MMA order per key tile i: S0_i, PV1_{i-1}, S1_i, PV0_i, so that each softmax warpgroup works on
+// one tile while the tensor cores run the other's products.  Fully masked key tiles are never
+// loaded (tile i runs for query tile qt only while i <= qt); the diagonal tile is masked per
+// element.  Softmax rescales O only when a row max grows by more than 2^8, which keeps the result
+// exact (the stale max is used consistently for P, l and lse).
+//
+// Every barrier wait gives up after AttnParams::timeout_ns: the CTA then records bit 0 in the
+// device status word, stops its loops, lets its copies and MMAs land, frees tensor memory and
+// returns.  Later CTAs see the status word and return at once.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <type_traits>
+
+#include "attnfuse_internal.h"
+#include "ptx.cuh"
+#include "rope.cuh"
+
+namespace attnfuse {
+
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;  // keys per tile
+constexpr int kThreads = 512;
+constexpr int KST = 2;   // K ring depth
+constexpr int VST = 2;   // V ring depth
+constexpr uint32_t kBoxBytes = 128 * 128;  // 128 rows x 64 16-bit columns, 128-byte swizzled
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// Register split after setmaxnreg: 128 x (56 + 88) + 256 x 184 = 65536 = 512 threads x 128.
+constexpr uint32_t kRegsCtrl = 56, kRegsSoftmax = 184, kRegsRotate = 88;
+static_assert(128 * (kRegsCtrl + kRegsRotate) + 256 * kRegsSoftmax == kThreads * 128, "register split");
+
+template <int D>
+struct Cfg {
+  static constexpr int NBOX = D / 64;
+  static constexpr uint32_t TILE = NBOX * kBoxBytes;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
+  static constexpr uint32_t OFF_CTL = OFF_V + VST * TILE;
+  static constexpr uint32_t SMEM = OFF_CTL + 256 + 1024;  // + control block + alignment slack
+  static constexpr uint32_t COL_O = 2 * BN;               // O0 at 256, O1 at 256 + D
+  static_assert(COL_O + 2 * D <= kTmemCols, "TMEM budget");
+};
+
+struct __align__(8) Ctrl {
+  uint64_t q_full, q_ready;
+  uint64_t k_full[KST], k_ready[KST], k_empty[KST];
+  uint64_t v_full[VST], v_empty[VST];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int skip;
+};
+static_assert(sizeof(Ctrl) <= 256, "control block");
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t& b) { return ptx::smem_u32(&b); }
+
+__device__ __forceinline__ void signal_abort(Ctrl& ctl) {
+  *reinterpret_cast<volatile int*>(&ctl.abort_flag) = 1;
+  atomicOr(&g_device_status, 1u);
+}
+
+// Bounded wait; false if it ran out (and raised the abort) or another thread aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctrl& ctl, unsigned long long timeout_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        signal_abort(ctl);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used only to let in-flight copies and MMAs land.
+__device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Whole-warp wait with a warp-uniform outcome.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, Ctrl& ctl,
+                                              unsigned long long timeout_ns) {
+  bool ok = wait_bar(bar, parity, ctl, timeout_ns);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Byte offsets, inside a 128-row tile of 128-byte swizzled boxes, of the two 16-byte chunks that
+// hold the rotation pairs (k, k + d/2) for k in [8 ck, 8 ck + 8) of row r.  TMA's 128-byte
+// swizzle stores logical chunk c of row r at physical chunk c ^ (r & 7).
+template <int D>
+__device__ __forceinline__ void pair_offsets(int r, int ck, uint32_t& xo, uint32_t& yo) {
+  if constexpr (D == 128) {
+    xo = (uint32_t)r * 128u + (uint32_t)((ck ^ (r & 7)) * 16);
+    yo = xo + kBoxBytes;  // columns 64..127 live in the second box at the same offset
+  } else {
+    xo = (uint32_t)r * 128u + (uint32_t)((ck ^ (r & 7)) * 16);
+    yo = (uint32_t)r * 128u + (uint32_t)(((ck + 4) ^ (r & 7)) * 16);
+  }
+}
+
+// Rotate rows [0, nrows) of the Q tiles (positions q_row0 + row) with exact per-element angles,
+// the same arithmetic as the pre-rotation kernel.  Threads tid = 0 .. nthr-1 share the items.
+template <int D, bool BF16>
+__device__ __forceinline__ void rotate_q_tiles(uint8_t* sq, int nrows, int q_row0, int tid, int nthr,
+                                               const AttnParams& p) {
+  constexpr int NCH = D / 16;
+  for (int item = tid; item < nrows * NCH; item += nthr) {
+    const int row = item / NCH;
+    const int ck = item - row * NCH;
+    const int tile = row / BM;
+    const int r = row - tile * BM;
+    float c[8], s[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      rope_cs((uint32_t)(q_row0 + row), p.freqs.lo[ck * 8 + t], p.freqs.hi[ck * 8 + t], c[t], s[t]);
+    uint32_t xo, yo;
+    pair_offsets<D>(r, ck, xo, yo);
+    uint8_t* base = sq + (size_t)tile * Cfg<D>::TILE;
+    uint4 xv = *reinterpret_cast<uint4*>(base + xo);
+    uint4 yv = *reinterpret_cast<uint4*>(base + yo);
+    rope_rotate_chunk<BF16>(xv, yv, c, s);
+    *reinterpret_cast<uint4*>(base + xo) = xv;
+    *reinterpret_cast<uint4*>(base + yo) = yv;
+  }
+}
+
+template <int D, bool ROTATE, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
+  using C = Cfg<D>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr uint32_t AB = BF16 ? 1u : 0u;
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, BN, 0, 0);   // S = Q K^T: A, B K-major
+  constexpr uint32_t IDESC_PV = ptx::idesc_f16(AB, BM, D, 0, 1);   // O += P V: B (V) MN-major
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(sgen + C::OFF_CTL);
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work unit: (b, h, 256-row query block t); blocks are numbered longest-first ----------
+  const int bh_count = p.B * p.Hq;
+  const int unit = blockIdx.x;
+  const int t = p.n_qblocks - 1 - unit / bh_count;
+  const int bh = unit - (unit / bh_count) * bh_count;
+  const int b = bh / p.Hq;
+  const int h = bh - b * p.Hq;
+  const int hk = h / (p.Hq / p.Hkv);
+  const int q_row0 = t * 2 * BM;
+  const bool active1 = q_row0 + BM < p.N;
+  const int n0 = 2 * t + 1;                // key tiles for q0 (tile 2t is its diagonal)
+  const int n1 = active1 ? 2 * t + 2 : 0;  // key tiles for q1
+  const int n_kt = active1 ? n1 : n0;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_addr(ctl.q_full), 1);
+    ptx::mbar_init(bar_addr(ctl.q_ready), 3 * 128);
+    for (int s = 0; s < KST; ++s) {
+      ptx::mbar_init(bar_addr(ctl.k_full[s]), 1);
+      ptx::mbar_init(bar_addr(ctl.k_ready[s]), 128);
+      ptx::mbar_init(bar_addr(ctl.k_empty[s]), 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      ptx::mbar_init(bar_addr(ctl.v_full[s]), 1);
+      ptx::mbar_init(bar_addr(ctl.v_empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar_addr(ctl.s_full[i]), 1);
+      ptx::mbar_init(bar_addr(ctl.p_full[i]), 128);
+      ptx::mbar_init(bar_addr(ctl.o_full[i]), 1);
+    }
+    ptx::mbar_init(bar_addr(ctl.mma_done), 1);
+    ctl.abort_flag = 0;
+    ctl.skip = (*reinterpret_cast<volatile unsigned int*>(&g_device_status)) != 0u;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const bool skip = ctl.skip != 0;
+  const unsigned long long tmo = p.timeout_ns;
+  __syncwarp();  // setmaxnreg and tcgen05 warp-collectives need converged warps
+
+  if (warp < 4) {
+    ptx::setmaxnreg_dec<kRegsCtrl>();
+    if (!skip && warp == 0 && lane == 0) {
+      // ================================ TMA producer ==========================================
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      const int nq = active1 ? 2 : 1;
+      ptx::mbar_arrive_expect_tx(bar_addr(ctl.q_full), (uint32_t)nq * C::TILE);
+      for (int i = 0; i < nq; ++i)
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          ptx::tma_load_4d(sQ + i * C::TILE + bx * kBoxBytes, &tmQ, bar_addr(ctl.q_full), bx * 64, h,
+                           q_row0 + i * BM, b);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n_kt && ok; ++i) {
+        const int ks = i % KST, kph = (i / KST) & 1;
+        if (!(ok = wait_bar(bar_addr(ctl.k_empty[ks]), kph ^ 1, ctl, tmo))) break;
+        ptx::mbar_arrive_expect_tx(bar_addr(ctl.k_full[ks]), C::TILE);
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          ptx::tma_load_4d(sK + ks * C::TILE + bx * kBoxBytes, &tmK, bar_addr(ctl.k_full[ks]), bx * 64, hk, i * BN,
+                           b);
+        ++k_issued;
+        const int vs = i % VST, vph = (i / VST) & 1;
+        if (!(ok = wait_bar(bar_addr(ctl.v_empty[vs]), vph ^ 1, ctl, tmo))) break;
+        ptx::mbar_arrive_expect_tx(bar_addr(ctl.v_full[vs]), C::TILE);
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          ptx::tma_load_4d(sV + vs * C::TILE + bx * kBoxBytes, &tmV, bar_addr(ctl.v_full[vs]), bx * 64, hk, i * BN,
+                           b);
+        ++v_issued;
+      }
+      if (!ok) {
+        // Let every copy already issued land before shared memory is released.
+        const unsigned long long drain = 100000000ull;
+        drain_bar(bar_addr(ctl.q_full), 0, drain);
+        for (int s = 0; s < KST; ++s)
+          if (k_issued > s) drain_bar(bar_addr(ctl.k_full[s]), ((k_issued - 1 - s) / KST) & 1, drain);
+        for (int s = 0; s < VST; ++s)
+          if (v_issued > s) drain_bar(bar_addr(ctl.v_full[s]), ((v_issued - 1 - s) / VST) & 1, drain);
+      }
+    } else if (!skip && warp == 1 && lane == 0) {
+      // ================================ MMA issuer ============================================
+      auto issue_S = [&](int iq, uint32_t kbase) {
+        const uint32_t qbase = sQ + iq * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+          ptx::mma_ss(tmem + iq * BN, ptx::sdesc_sw128(qbase + off, 16, 1024), ptx::sdesc_sw128(kbase + off, 16, 1024),
+                      IDESC_S, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_PV = [&](int iq, uint32_t vbase, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          ptx::mma_ts(tmem + C::COL_O + iq * D, tmem + iq * BN + kk * 8,
+                      ptx::sdesc_sw128(vbase + kk * 2048, kBoxBytes, 1024), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+      };
+      bool ok = wait_bar(bar_addr(ROTATE ? ctl.q_ready : ctl.q_full), 0, ctl, tmo);
+      ptx::tc_fence_after();
+      for (int i = 0; i < n_kt && ok; ++i) {
+        const int ks = i % KST, kph = (i / KST) & 1;
+        if (!(ok = wait_bar(bar_addr(ROTATE ? ctl.k_ready[ks] : ctl.k_full[ks]), kph, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        const uint32_t kbase = sK + ks * C::TILE;
+        if (i < n0) {
+          issue_S(0, kbase);
+          ptx::mma_commit(bar_addr(ctl.s_full[0]));
+        }
+        if (i >= 1 && i - 1 < n1) {  // P1 of the previous key tile
+          const int j = i - 1, vs = j % VST, vph = (j / VST) & 1;
+          if (!(ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo))) break;
+          if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
+          ptx::tc_fence_after();
+          issue_PV(1, sV + vs * C::TILE, j == 0);
+          ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
+          if (j == n1 - 1) ptx::mma_commit(bar_addr(ctl.o_full[1]));
+        }
+        if (i < n1) {
+          issue_S(1, kbase);
+          ptx::mma_commit(bar_addr(ctl.s_full[1]));
+        }
+        ptx::mma_commit(bar_addr(ctl.k_empty[ks]));
+        if (i < n0) {
+          const int vs = i % VST, vph = (i / VST) & 1;
+          if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
+          if (!(ok = wait_bar(bar_addr(ctl.p_full[0]), i & 1, ctl, tmo))) break;
+          ptx::tc_fence_after();
+          issue_PV(0, sV + vs * C::TILE, i == 0);
+          if (n1 == 0) ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
+          if (i == n0 - 1) ptx::mma_commit(bar_addr(ctl.o_full[0]));
+        }
+      }
+      if (ok && n1 > 0) {  // P1 of the last key tile
+        const int j = n1 - 1, vs = j % VST, vph = (j / VST) & 1;
+        ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo) && wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo);
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_PV(1, sV + vs * C::TILE, j == 0);
+          ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
+          ptx::mma_commit(bar_addr(ctl.o_full[1]));
+        }
+      }
+      // Every MMA issued must finish before tensor memory is freed.
+      ptx::mma_commit(bar_addr(ctl.mma_done));
+      drain_bar(bar_addr(ctl.mma_done), 0, 100000000ull);
+    }
+  } else if (warp < 12) {
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    if (!skip) {
+      bool ok = true;
+      if constexpr (ROTATE) {
+        ok = wait_bar_warp(bar_addr(ctl.q_full), 0, ctl, tmo);
+        if (ok) {
+          rotate_q_tiles<D, BF16>(sgen + C::OFF_Q, active1 ? 2 * BM : BM, q_row0, threadIdx.x - 128, 3 * 128, p);
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(bar_addr(ctl.q_ready));
+        }
+      }
+      // ================================ softmax + epilogue ====================================
+      const int wi = (warp - 4) / 4;  // which query tile
+      const int qt = 2 * t + wi;
+      const int n_steps = wi == 0 ? n0 : n1;
+      const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + lane_off + wi * BN;
+      const uint32_t tO = tmem + lane_off + C::COL_O + wi * D;
+      const float sl2 = p.scale_log2;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n_steps && ok; ++j) {
+        if (!(ok = wait_bar_warp(bar_addr(ctl.s_full[wi]), j & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sv[c]);
+        ptx::tmem_wait_ld();
+        if (j == n_steps - 1) {  // diagonal tile: key column c is visible to row r iff c <= r
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
+        const float m_new = fmaxf(m_run, mx * sl2);
+        // Rescale only when some row's max grew past the threshold (warp-uniform decision, since
+        // TMEM loads and stores are warp-collective); otherwise keep the stale max.
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_run = m_new;
+        } else {
+          const bool need = m_new > m_run + kRescaleThreshold;
+          rescale = __any_sync(0xFFFFFFFFu, need);
+          if (need) {
+            alpha = ptx::ex2_approx(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+          }
+        }
+        const float neg_m = -m_run;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16)
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[c][2 * e]), sl2, neg_m));
+            const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl2, neg_m));
+            sum += p0 + p1;
+            pk[e] = Pack<BF16>::pack(p0, p1);
+          }
+          ptx::tmem_st16(tS + 16 * c, pk);
+        }
+        l_run += sum;
+        if (rescale) {  // O += P V for this tile is issued only after p_full, so O is stable here
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + 32 * c, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st32(tO + 32 * c, o);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(ctl.p_full[wi]));
+      }
+      if (ok && n_steps > 0) ok = wait_bar_warp(bar_addr(ctl.o_full[wi]), 0, ctl, tmo);
+      if (ok && n_steps > 0) {
+        ptx::tc_fence_after();
+        const int row = qt * BM + r;
+        const float inv_l = 1.f / l_run;
+        T* orow = reinterpret_cast<T*>(p.out) + (((size_t)b * p.N + row) * p.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + 32 * c, o);
+          ptx::tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = Pack<BF16>::pack(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          if (row < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+        if (row < p.N && p.lse != nullptr)
+          p.lse[((size_t)b * p.Hq + h) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
+      }
+    }
+  } else {
+    ptx::setmaxnreg_dec<kRegsRotate>();
+    if constexpr (ROTATE) {
+      if (!skip) {
+        bool ok = wait_bar_warp(bar_addr(ctl.q_full), 0, ctl, tmo);
+        if (ok) {
+          rotate_q_tiles<D, BF16>(sgen + C::OFF_Q, active1 ? 2 * BM : BM, q_row0, threadIdx.x - 128, 3 * 128, p);
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(bar_addr(ctl.q_ready));
+        }
+        // ============================== K-tile rotation =========================================
+        // Thread mapping: fixed chunk ck (8 frequencies), rows r0 + RS * pass.  The cos/sin of the
+        // thread's rows are carried by angle addition: exact values at position r0 of key tile 0,
+        // advanced by the exact rotation of RS positions between passes and of 128 positions
+        // between tiles (error grows by ~1 fp32 rounding per step: < 3e-5 after 32768 positions).
+        const int rt = threadIdx.x - 384;
+        const int w = rt / 32;
+        int ck, r0, RS;
+        if constexpr (D == 128) {
+          ck = lane & 7;
+          r0 = w * 4 + (lane >> 3);
+          RS = 16;
+        } else {
+          // rows of one 8-lane phase differ by 4, so their chunks (ck ^ (r & 7)) never share banks
+          ck = lane & 3;
+          const int q = lane >> 2;
+          r0 = w * 8 + (((q & 1) << 2) | (q >> 1));
+          RS = 32;
+        }
+        constexpr int PASSES = D == 128 ? 8 : 4;
+        float c0[8], s0[8], cR[8], sR[8], cT[8], sT[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t lo = p.freqs.lo[ck * 8 + e], hi = p.freqs.hi[ck * 8 + e];
+          rope_cs((uint32_t)r0, lo, hi, c0[e], s0[e]);
+          rope_cs((uint32_t)RS, lo, hi, cR[e], sR[e]);
+          rope_cs((uint32_t)BN, lo, hi, cT[e], sT[e]);
+        }
+        for (int i = 0; i < n_kt && ok; ++i) {
+          const int ks = i % KST, kph = (i / KST) & 1;
+          if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
+          uint8_t* kt = sgen + C::OFF_K + ks * C::TILE;
+          float c[8], s[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            c[e] = c0[e];
+            s[e] = s0[e];
+          }
+#pragma unroll
+          for (int pass = 0; pass < PASSES; ++pass) {
+            uint32_t xo, yo;
+            pair_offsets<D>(r0 + pass * RS, ck, xo, yo);
+            uint4 xv = *reinterpret_cast<uint4*>(kt + xo);
+            uint4 yv = *reinterpret_cast<uint4*>(kt + yo);
+            rope_rotate_chunk<BF16>(xv, yv, c, s);
+            *reinterpret_cast<uint4*>(kt + xo) = xv;
+            *reinterpret_cast<uint4*>(kt + yo) = yv;
+            if (pass + 1 < PASSES) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) rope_advance(c[e], s[e], cR[e], sR[e]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) rope_advance(c0[e], s0[e], cT[e], sT[e]);
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every role reaches here; no tcgen05 work is in flight --------------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// One CTA of 32 threads that waits on a barrier no one arrives on, for at most timeout_ns.
+__global__ void diag_wait_timeout_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+      if (ptx::mbar_try_wait(ptx::smem_u32(&bar), 0)) break;  // never true: nothing arrives
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        atomicOr(&g_device_status, 1u);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <int D, bool ROTATE, bool BF16>
+cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t stream, const char** why) {
+  auto kernel = attn_fwd_kernel<D, ROTATE, BF16>;
+  constexpr int kMaxDevices = 64;
+  static int configured[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    // The warp-role register split (setmaxnreg) hands out exactly 512 x 128 registers: launching
+    // with fewer per thread would leave the softmax warps waiting for registers forever.
+    if (attr.numRegs != 128) {
+      if (why) *why = "attention kernel was not compiled with 128 registers per thread (setmaxnreg split)";
+      return cudaErrorInvalidConfiguration;
+    }
+    configured[dev] = 1;
+  }
+  kernel<<<dim3((unsigned)p.total_units), dim3(kThreads), Cfg<D>::SMEM, stream>>>(maps.q, maps.k, maps.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
+                            cudaStream_t stream, const char** why) {
+  if (p.total_units <= 0) return cudaSuccess;
+  if (d == 128) {
+    if (rotate) return bf16 ? launch_one<128, true, true>(maps, p, stream, why) : launch_one<128, true, false>(maps, p, stream, why);
+    return bf16 ? launch_one<128, false, true>(maps, p, stream, why) : launch_one<128, false, false>(maps, p, stream, why);
+  }
+  if (rotate) return bf16 ? launch_one<64, true, true>(maps, p, stream, why) : launch_one<64, true, false>(maps, p, stream, why);
+  return bf16 ? launch_one<64, false, true>(maps, p, stream, why) : launch_one<64, false, false>(maps, p, stream, why);
+}
+
+cudaError_t read_and_clear_device_status(unsigned int* value, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(value, g_device_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  if (*value != 0u) {
+    const unsigned int zero = 0u;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+cudaError_t launch_diag_wait_timeout(unsigned long long timeout_ns, cudaStream_t stream) {
+  diag_wait_timeout_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace attnfuse

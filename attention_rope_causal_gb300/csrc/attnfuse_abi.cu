@@ -1,0 +1,288 @@
+// The C ABI of libattnfuse: argument validation, device checks, TMA descriptors, workspace
+// handling and the launch sequence of each mode.  Declared in include/attnfuse.h.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attnfuse.h"
+#include "attnfuse_internal.h"
+
+namespace attnfuse {
+
+// F_k = round(theta_k / (2 pi) * 2^64): frequency of pair k in turns per position, as a 64-bit
+// fixed-point fraction (theta_k <= 1, so F_k < 2^61.4).  theta_k = base^(-2k/d) in double.
+void rope_freqs_host(int d, double base, RopeFreqs* f) {
+  std::memset(f, 0, sizeof(*f));
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int k = 0; k < d / 2 && k < kMaxHalfDim; ++k) {
+    const double theta = std::pow(base, -2.0 * (double)k / (double)d);
+    const double scaled = std::ldexp(theta / two_pi, 64);
+    const uint64_t F = (uint64_t)std::llround(scaled);  // < 2^62: fits a signed 64-bit round
+    f->lo[k] = (uint32_t)(F & 0xFFFFFFFFull);
+    f->hi[k] = (uint32_t)(F >> 32);
+  }
+}
+
+}  // namespace attnfuse
+
+namespace {
+
+using namespace attnfuse;
+
+constexpr unsigned long long kTimeoutNs = 1000000000ull;  // 1 s on any single barrier wait
+constexpr int kMaxN = 1 << 24;
+
+thread_local char g_err[512] = "";
+
+attnfuse_status_t fail(attnfuse_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+attnfuse_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTNFUSE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+attnfuse_status_t check_dtype_d(int d, attnfuse_dtype_t dtype) {
+  if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return fail(ATTNFUSE_ERR_INVALID_ARG, "dtype %d is not bf16 (0) or fp16 (1)", (int)dtype);
+  if (d != 64 && d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "head dim d=%d is not supported (64 or 128)", d);
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status_t check_base(double base) {
+  if (!(base > 1.0) || !std::isfinite(base)) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_base must be finite and > 1");
+  return ATTNFUSE_OK;
+}
+
+// The kernels are built for sm_103a only.
+attnfuse_status_t check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(ATTNFUSE_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; libattnfuse runs on 10.3 (sm_103a)",
+                dev, major, minor);
+  return ATTNFUSE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B, N, H, d] tensor, boxes of 64 columns x 128 rows of one head, 128-byte swizzle.
+attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, int H, int d, attnfuse_dtype_t dtype,
+                              const char* name) {
+  auto fn = encode_fn();
+  if (!fn) return fail(ATTNFUSE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)N * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, dtype == ATTNFUSE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTNFUSE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return ATTNFUSE_OK;
+}
+
+size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N * (size_t)H * (size_t)d * 2u; }
+
+attnfuse_status_t validate_fwd(const void* q, const void* k, const void* v, const void* out, const float* lse, int B,
+                               int Hq, int Hkv, int N, int d, double base, attnfuse_mode_t mode,
+                               attnfuse_dtype_t dtype) {
+  if (!q || !k || !v || !out) return fail(ATTNFUSE_ERR_INVALID_ARG, "q, k, v and out must be non-null");
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "B, Hq, Hkv, N must be >= 1");
+  if (N >= kMaxN) return fail(ATTNFUSE_ERR_INVALID_ARG, "N=%d exceeds the supported maximum %d", N, kMaxN - 1);
+  if (Hq % Hkv != 0) return fail(ATTNFUSE_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE) return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0) or prerotate (1)", (int)mode);
+  attnfuse_status_t st = check_dtype_d(d, dtype);
+  if (st != ATTNFUSE_OK) return st;
+  if ((st = check_base(base)) != ATTNFUSE_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(ATTNFUSE_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const long long units = (long long)B * Hq * ((N + 255) / 256);
+  if (units > 0x7FFFFFFFLL) return fail(ATTNFUSE_ERR_INVALID_ARG, "problem too large: %lld work units", units);
+  return ATTNFUSE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attnfuse_version(void) { return "libattnfuse 0.1 (sm_103a)"; }
+
+const char* attnfuse_status_string(attnfuse_status_t s) {
+  switch (s) {
+    case ATTNFUSE_OK: return "ok";
+    case ATTNFUSE_ERR_INVALID_ARG: return "invalid argument";
+    case ATTNFUSE_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case ATTNFUSE_ERR_CUDA: return "CUDA error";
+    case ATTNFUSE_ERR_TIMEOUT: return "a kernel barrier wait timed out";
+    case ATTNFUSE_ERR_NO_MEMORY: return "out of device memory";
+  }
+  return "unknown status";
+}
+
+const char* attnfuse_last_error(void) { return g_err; }
+
+size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return 0;
+  if (mode != ATTNFUSE_PREROTATE) return 0;
+  return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, N, Hkv, d), 256);
+}
+
+attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int H, int d, double rope_base,
+                                      attnfuse_dtype_t dtype, void* stream) {
+  g_err[0] = '\0';
+  if (!x || !y) return fail(ATTNFUSE_ERR_INVALID_ARG, "x and y must be non-null");
+  if (B < 1 || N < 1 || H < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "B, N, H must be >= 1");
+  if (N >= kMaxN) return fail(ATTNFUSE_ERR_INVALID_ARG, "N=%d exceeds the supported maximum %d", N, kMaxN - 1);
+  attnfuse_status_t st = check_dtype_d(d, dtype);
+  if (st != ATTNFUSE_OK) return st;
+  if ((st = check_base(rope_base)) != ATTNFUSE_OK) return st;
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(ATTNFUSE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  const size_t bytes = tensor_bytes(B, N, H, d);
+  const char* xs = static_cast<const char*>(x);
+  const char* ys = static_cast<const char*>(y);
+  if (xs != ys && xs < ys + bytes && ys < xs + bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "x and y overlap without being equal");
+  if ((st = check_device()) != ATTNFUSE_OK) return st;
+
+  RopeApplyParams p;
+  std::memset(&p, 0, sizeof p);
+  p.job[0].x = x;
+  p.job[0].y = y;
+  p.job[0].H = H;
+  p.job[0].groups = (H + kHeadsPerGroup - 1) / kHeadsPerGroup;
+  p.njobs = 1;
+  p.N = N;
+  p.tokens = (long long)B * N;
+  p.groups_total = p.job[0].groups;
+  rope_freqs_host(d, rope_base, &p.freqs);
+  cudaError_t e = launch_rope_apply(p, d, dtype == ATTNFUSE_BF16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope_apply launch");
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                           int Hq, int Hkv, int N, int d, double rope_base, attnfuse_mode_t mode,
+                                           attnfuse_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+  g_err[0] = '\0';
+  attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, mode, dtype);
+  if (st != ATTNFUSE_OK) return st;
+  const size_t need = attnfuse_workspace_bytes(B, Hq, Hkv, N, d, mode, dtype);
+  if (workspace) {
+    if (workspace_bytes < need)
+      return fail(ATTNFUSE_ERR_INVALID_ARG, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    if (!aligned(workspace, 256)) return fail(ATTNFUSE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  if ((st = check_device()) != ATTNFUSE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.n_qblocks = (N + 255) / 256;
+  p.total_units = B * Hq * p.n_qblocks;
+  p.out = out;
+  p.lse = lse;
+  p.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
+  p.timeout_ns = kTimeoutNs;
+  rope_freqs_host(d, rope_base, &p.freqs);
+
+  const void* qa = q;
+  const void* ka = k;
+  void* owned = nullptr;
+  if (mode == ATTNFUSE_PREROTATE) {
+    void* ws = workspace;
+    if (!ws) {
+      cudaError_t e = cudaMallocAsync(&owned, need, s);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ATTNFUSE_ERR_NO_MEMORY, "cudaMallocAsync(%zu) for the rotated Q/K failed: %s", need, cudaGetErrorString(e));
+      }
+      ws = owned;
+    }
+    void* qr = ws;
+    void* kr = static_cast<char*>(ws) + round_up(tensor_bytes(B, N, Hq, d), 256);
+    RopeApplyParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    rp.job[0] = RopeJob{q, qr, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    rp.job[1] = RopeJob{k, kr, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    rp.njobs = 2;
+    rp.N = N;
+    rp.tokens = (long long)B * N;
+    rp.groups_total = rp.job[0].groups + rp.job[1].groups;
+    rp.freqs = p.freqs;
+    cudaError_t e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+    if (e != cudaSuccess) {
+      if (owned) cudaFreeAsync(owned, s);
+      return cuda_fail(e, "rope_apply launch");
+    }
+    qa = qr;
+    ka = kr;
+  }
+
+  AttnMaps maps;
+  if ((st = encode_bnhd(&maps.q, qa, B, N, Hq, d, dtype, "q")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.k, ka, B, N, Hkv, d, dtype, "k")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.v, v, B, N, Hkv, d, dtype, "v")) == ATTNFUSE_OK) {
+    const char* why = nullptr;
+    cudaError_t e = launch_attn_fwd(maps, p, d, dtype == ATTNFUSE_BF16, mode == ATTNFUSE_FUSED, s, &why);
+    if (e != cudaSuccess) st = why ? fail(ATTNFUSE_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "attention launch");
+  }
+  if (owned) cudaFreeAsync(owned, s);
+  return st;
+}
+
+attnfuse_status_t attnfuse_device_status(void* stream) {
+  g_err[0] = '\0';
+  unsigned int v = 0;
+  cudaError_t e = read_and_clear_device_status(&v, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "device status");
+  if (v != 0u) return fail(ATTNFUSE_ERR_TIMEOUT, "a kernel barrier wait ran out (device status 0x%x)", v);
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status_t attnfuse_diag_wait_timeout(uint64_t timeout_ns, void* stream) {
+  g_err[0] = '\0';
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return fail(ATTNFUSE_ERR_INVALID_ARG, "timeout_ns must be in (0, 1e9]");
+  attnfuse_status_t st = check_device();
+  if (st != ATTNFUSE_OK) return st;
+  cudaError_t e = launch_diag_wait_timeout((unsigned long long)timeout_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diag launch");
+  return ATTNFUSE_OK;
+}
+
+}  // extern "C"

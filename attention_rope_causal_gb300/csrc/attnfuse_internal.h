@@ -1,0 +1,64 @@
+// Declarations shared by the library's translation units (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rope.cuh"
+
+namespace attnfuse {
+
+// ---- pre-rotation kernel --------------------------------------------------------------------
+
+constexpr int kHeadsPerGroup = 8;
+
+struct RopeJob {
+  const void* x;  // [B, N, H, d]
+  void* y;        // [B, N, H, d], may equal x
+  int H;
+  int groups;     // ceil(H / kHeadsPerGroup)
+};
+
+struct RopeApplyParams {
+  RopeJob job[2];
+  int njobs;
+  int N;
+  long long tokens;  // B * N
+  int groups_total;  // job[0].groups + (njobs > 1 ? job[1].groups : 0)
+  RopeFreqs freqs;
+};
+
+cudaError_t launch_rope_apply(const RopeApplyParams& p, int d, bool bf16, cudaStream_t stream);
+
+// ---- attention kernel -----------------------------------------------------------------------
+
+struct AttnParams {
+  int B, Hq, Hkv, N;
+  int n_qblocks;     // ceil(N / 256): 256 query rows (two 128-row tiles) per CTA
+  int total_units;   // B * Hq * n_qblocks
+  void* out;         // [B, N, Hq, d]
+  float* lse;        // [B, Hq, N] or nullptr
+  float scale_log2;  // log2(e) / sqrt(d)
+  unsigned long long timeout_ns;  // limit on any single barrier wait
+  RopeFreqs freqs;
+};
+
+struct AttnMaps {
+  CUtensorMap q, k, v;
+};
+
+// Launches the attention kernel.  rotate = true rotates Q and K tiles on chip (fused mode).
+cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
+                            cudaStream_t stream, const char** why);
+
+// Device status word written by kernels whose barrier waits ran out (bit 0).
+cudaError_t read_and_clear_device_status(unsigned int* value, cudaStream_t stream);
+
+// Launches one CTA that waits, for at most timeout_ns, on a barrier nothing arrives on.
+cudaError_t launch_diag_wait_timeout(unsigned long long timeout_ns, cudaStream_t stream);
+
+// Fills F_k = round(theta_k / (2 pi) * 2^64), theta_k = base^(-2k/d).
+void rope_freqs_host(int d, double base, RopeFreqs* f);
+
+}  // namespace attnfuse

@@ -1,0 +1,100 @@
+// Rotary position embedding on the device: angles, cos/sin and the rotation of one 16-byte chunk
+// pair.  Shared by the pre-rotation kernel and the fused attention kernel so that both rotate Q
+// with bit-identical arithmetic.
+//
+// Convention (the pages name RoPE as a pre-multiplication transform of Q and K -- "AttnFuse Makes
+// RoPE a First-Class Attention Compilation Operation", 2026-09-13 AI papers report, paragraph 1 --
+// and print no formula; this library fixes the half-split form):
+//   theta_k = base^(-2k/d),  pairs (k, k + d/2),  angle = p * theta_k with p the token index,
+//   x'[k] = x[k] cos - x[k+d/2] sin,   x'[k+d/2] = x[k+d/2] cos + x[k] sin.
+//
+// Angles.  p * theta_k reaches 3.3e4 rad at p = 32767, where an fp32 product is off by up to
+// ~2e-3 rad.  Instead the host stores, per pair k, the frequency in turns as a 64-bit fixed-point
+// fraction F_k = round(theta_k / (2 pi) * 2^64).  The angle in turns, reduced modulo one turn, is
+// then bits [32, 64) of the integer product p * F_k (two integer instructions), read as a signed
+// 32-bit fraction in [-1/2, 1/2) turns, and sincospif() evaluates it with |argument| <= pi.
+// Angle error: <= 2^-32 turn from truncation plus one fp32 rounding of the fraction (~2e-7 rad).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace attnfuse {
+
+constexpr int kMaxHalfDim = 64;  // d <= 128
+
+struct RopeFreqs {
+  uint32_t lo[kMaxHalfDim];  // low  32 bits of F_k
+  uint32_t hi[kMaxHalfDim];  // high 32 bits of F_k
+};
+
+// cos and sin of pos * theta_k, given F_k split into (flo, fhi).
+__device__ __forceinline__ void rope_cs(uint32_t pos, uint32_t flo, uint32_t fhi, float& c, float& s) {
+  uint32_t turns = __umulhi(pos, flo) + pos * fhi;  // bits [32,64) of pos * F_k (mod 2^64)
+  float half_turns = (float)(int32_t)turns * 4.6566128730773926e-10f;  // * 2^-31
+  sincospif(half_turns, &s, &c);
+}
+
+// (c, s) <- (c, s) * (c2, s2) as unit complex numbers: the angle advances by the angle of (c2, s2).
+__device__ __forceinline__ void rope_advance(float& c, float& s, float c2, float s2) {
+  float cn = __fmaf_rn(c, c2, -__fmul_rn(s, s2));
+  float sn = __fmaf_rn(s, c2, __fmul_rn(c, s2));
+  c = cn;
+  s = sn;
+}
+
+// One rotated pair.  Written with explicit round-to-nearest intrinsics so no kernel can contract it
+// differently: every caller gets bit-identical results for equal inputs.
+__device__ __forceinline__ void rope_pair(float x, float y, float c, float s, float& xr, float& yr) {
+  xr = __fmaf_rn(x, c, -__fmul_rn(y, s));
+  yr = __fmaf_rn(y, c, __fmul_rn(x, s));
+}
+
+template <bool BF16>
+struct Pack;
+
+template <>
+struct Pack<true> {
+  __device__ __forceinline__ static void unpack(uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+
+template <>
+struct Pack<false> {
+  __device__ __forceinline__ static void unpack(uint32_t w, float& lo, float& hi) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+
+// Rotate 8 pairs held as two 16-byte chunks: xv = elements [k0, k0+8), yv = [k0+d/2, k0+d/2+8).
+template <bool BF16>
+__device__ __forceinline__ void rope_rotate_chunk(uint4& xv, uint4& yv, const float (&c)[8], const float (&s)[8]) {
+  uint32_t* xw = reinterpret_cast<uint32_t*>(&xv);
+  uint32_t* yw = reinterpret_cast<uint32_t*>(&yv);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float x0, x1, y0, y1, a0, a1, b0, b1;
+    Pack<BF16>::unpack(xw[w], x0, x1);
+    Pack<BF16>::unpack(yw[w], y0, y1);
+    rope_pair(x0, y0, c[2 * w], s[2 * w], a0, b0);
+    rope_pair(x1, y1, c[2 * w + 1], s[2 * w + 1], a1, b1);
+    xw[w] = Pack<BF16>::pack(a0, a1);
+    yw[w] = Pack<BF16>::pack(b0, b1);
+  }
+}
+
+}  // namespace attnfuse

@@ -1,0 +1,112 @@
+/*
+ * libattnfuse — causal softmax attention with Rotary Position Embedding (RoPE), forward, for
+ * NVIDIA GB300 (sm_103a).  C ABI: plain pointers and sizes, no framework types.
+ *
+ * The operation.  "AttnFuse Makes RoPE a First-Class Attention Compilation Operation" (2026-09-13
+ * AI papers report), paragraphs 1-2, and the AttnFuse abstract (arxivdaily 2609.13612): RoPE is a
+ * transformation of Q and K applied before the QK^T product, composed with the causality and
+ * softmax building blocks into one fused kernel.  Paragraphs 3-5 of the same report weigh that
+ * fused form against rotating Q and K in a separate pass first ("pre-rotation"), whose cost is
+ * memory bandwidth where the fused form's is compute; both forms are offered here.  The pages print
+ * no formula; this library fixes:
+ *     theta_k = rope_base^(-2k/d), k = 0 .. d/2-1, pairs (k, k + d/2), position = token index,
+ *     x'[k] = x[k] cos(p theta_k) - x[k+d/2] sin(p theta_k),
+ *     x'[k+d/2] = x[k+d/2] cos(p theta_k) + x[k] sin(p theta_k)       (Q and K; V is not rotated)
+ *     out[b,i,h,:] = sum_{j<=i} softmax_j(q'_{b,i,h} . k'_{b,j,h/g} / sqrt(d)) v[b,j,h/g,:]
+ *     lse[b,h,i]   = ln sum_{j<=i} exp(q'.k'/sqrt(d))                   (natural log)
+ * with g = Hq / Hkv (grouped-query attention: consecutive query heads share a KV head).
+ *
+ * Layout (row-major, contiguous, element type per `dtype`):
+ *     q, out : [B, N, Hq, d]        k, v : [B, N, Hkv, d]        lse : [B, Hq, N] float32
+ * Supported: d in {64, 128}; bf16 or fp16; B, N, Hq, Hkv >= 1; Hq % Hkv == 0; N < 2^24.
+ * Arithmetic: rotation and softmax statistics in fp32, products on the tensor cores with fp32
+ * accumulation; P and the rotated Q/K are rounded to `dtype` once.
+ *
+ * Ownership and streams.  Every buffer belongs to the caller and must be device memory (q, k, v,
+ * out, workspace 16-byte aligned; lse 4-byte aligned).  `stream` is a cudaStream_t (NULL = the
+ * legacy default stream); all work is enqueued on it and the calls return without waiting.
+ *
+ * Errors.  Arguments are validated before anything is launched; a failed call returns a status,
+ * launches nothing and leaves a message for attnfuse_last_error().  Faults raised while kernels
+ * run surface at the caller's next synchronisation.  Every barrier wait inside the kernels is
+ * bounded: if one runs out, the kernel stops, records it in a device status word that
+ * attnfuse_device_status() reads, and returns (later launches then do nothing until it is read).
+ */
+#ifndef ATTNFUSE_H_
+#define ATTNFUSE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTNFUSE_FUSED = 0, ATTNFUSE_PREROTATE = 1 } attnfuse_mode_t;
+
+typedef enum { ATTNFUSE_BF16 = 0, ATTNFUSE_FP16 = 1 } attnfuse_dtype_t;
+
+typedef enum {
+  ATTNFUSE_OK = 0,
+  ATTNFUSE_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, workspace too small */
+  ATTNFUSE_ERR_UNSUPPORTED = 2, /* d not in {64,128}, device is not compute capability 10.3 */
+  ATTNFUSE_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the CUDA error) */
+  ATTNFUSE_ERR_TIMEOUT = 4,     /* a kernel barrier wait ran out (attnfuse_device_status) */
+  ATTNFUSE_ERR_NO_MEMORY = 5    /* workspace allocation failed */
+} attnfuse_status_t;
+
+/*
+ * Causal RoPE attention forward.
+ *   mode = ATTNFUSE_FUSED:     one kernel; Q and K tiles are rotated in shared memory.
+ *   mode = ATTNFUSE_PREROTATE: a RoPE pass writes rotated Q', K' into `workspace`, then the same
+ *                              attention kernel runs on Q', K', V without rotation.
+ * Both modes compute the function in the header comment.  `lse` may be NULL (not written).
+ * `workspace` must hold attnfuse_workspace_bytes(...) bytes (0 for FUSED); if it is NULL while
+ * bytes are needed, the call allocates with cudaMallocAsync and frees with cudaFreeAsync on
+ * `stream`.  Query rows never read keys beyond their own position; rows are independent.
+ */
+attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                           int Hq, int Hkv, int N, int d, double rope_base, attnfuse_mode_t mode,
+                                           attnfuse_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
+/* Bytes of workspace attnfuse_rope_causal_fwd needs: 0 for FUSED; for PREROTATE the rotated copies
+ * of Q and K (each rounded up to 256 bytes).  Returns 0 for invalid arguments. */
+size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype);
+
+/*
+ * RoPE alone (the pre-rotation pass): y = RoPE(x) for x, y of shape [B, N, H, d], position of
+ * (b, n) = n.  y may equal x (in place); otherwise the two must not overlap.  Bounded by HBM
+ * bandwidth: it reads and writes every element once.
+ */
+attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int H, int d, double rope_base,
+                                      attnfuse_dtype_t dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word.  Returns
+ * ATTNFUSE_ERR_TIMEOUT if a kernel's barrier wait ran out since the last read, ATTNFUSE_ERR_CUDA if
+ * synchronising failed (e.g. a device fault), ATTNFUSE_OK otherwise.
+ */
+attnfuse_status_t attnfuse_device_status(void* stream);
+
+/*
+ * Diagnostic for the timeout path: launches one CTA that waits on a barrier nothing arrives on and
+ * gives up after `timeout_ns` nanoseconds (at most 1e9), setting the device status word as a real
+ * timeout would.  Nothing faults; the context stays usable.
+ */
+attnfuse_status_t attnfuse_diag_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Static description of a status code. */
+const char* attnfuse_status_string(attnfuse_status_t status);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* attnfuse_last_error(void);
+
+/* Library version string. */
+const char* attnfuse_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNFUSE_H_ */

@@ -1,0 +1,57 @@
+"""Tolerances and comparison helpers for GPU-vs-oracle parity.
+
+Output tolerances are the targets fixed for this library: bf16 max |err| <= 2e-2 and relative L2
+<= 1e-2; fp16 <= 5e-3 and <= 2e-3.  LSE: "1e-3 relative" is read as relative L2 <= 1e-3 over the
+compared rows, plus a per-row bound max |err| / max(1, |lse|) <= 5e-3 (bf16) or 1e-3 (fp16): with
+rotated Q and K rounded to bf16 once, a per-row relative bound of 1e-3 is unattainable for rows
+whose lse is near 0, so the per-row bound is measured against max(1, |lse|).
+"""
+import numpy as np
+
+TOL = {
+    "bf16": dict(max_abs=2e-2, rel_l2=1e-2, lse_row=5e-3),
+    "fp16": dict(max_abs=5e-3, rel_l2=2e-3, lse_row=1e-3),
+}
+LSE_REL_L2 = 1e-3
+
+
+def dtype_name(t):
+    import torch
+    return {torch.bfloat16: "bf16", torch.float16: "fp16"}[t]
+
+
+def errors(o_gpu, l_gpu, o_ref, l_ref):
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    d = o_gpu - o_ref
+    e = dict(max_abs=float(np.abs(d).max()) if d.size else 0.0,
+             rel_l2=float(np.linalg.norm(d) / max(np.linalg.norm(o_ref), 1e-300)))
+    if l_gpu is not None:
+        l_gpu = np.asarray(l_gpu, dtype=np.float64)
+        dl = l_gpu - l_ref
+        e["lse_rel_l2"] = float(np.linalg.norm(dl) / max(np.linalg.norm(l_ref), 1e-300))
+        e["lse_row"] = float((np.abs(dl) / np.maximum(1.0, np.abs(l_ref))).max()) if dl.size else 0.0
+    return e
+
+
+def assert_close(o_gpu, l_gpu, o_ref, l_ref, dtype: str, what: str = ""):
+    e = errors(o_gpu, l_gpu, o_ref, l_ref)
+    t = TOL[dtype]
+    assert np.all(np.isfinite(np.asarray(o_gpu, dtype=np.float64))), f"{what}: non-finite output"
+    assert e["max_abs"] <= t["max_abs"], f"{what}: max abs {e['max_abs']:.3e} > {t['max_abs']} ({e})"
+    assert e["rel_l2"] <= t["rel_l2"], f"{what}: rel L2 {e['rel_l2']:.3e} > {t['rel_l2']} ({e})"
+    if l_gpu is not None:
+        assert e["lse_rel_l2"] <= LSE_REL_L2, f"{what}: lse rel L2 {e['lse_rel_l2']:.3e} ({e})"
+        assert e["lse_row"] <= t["lse_row"], f"{what}: lse row err {e['lse_row']:.3e} ({e})"
+    return e
+
+
+def sample_rows(N: int, n_random: int, seed: int, tile: int = 128):
+    """Rows that exercise every structural case: the first rows, every tile boundary +-1, the last
+    tile, and random rows."""
+    rows = {0, 1, 2, N - 1, N - 2}
+    for b in range(tile, N, tile):
+        rows.update((b - 1, b, b + 1))
+    rows.update(range(max(0, N - tile), N, 7))
+    rng = np.random.default_rng(seed)
+    rows.update(rng.integers(0, N, size=n_random).tolist())
+    return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)

@@ -1,0 +1,92 @@
+"""CPU-side checks of the C ABI: the library builds and loads without a GPU, exports every function
+include/attnfuse.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_rope_causal_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attnfuse.h")
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced by argument checks
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attnfuse_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attnfuse_rope_causal_fwd", "attnfuse_rope_apply", "attnfuse_workspace_bytes",
+              "attnfuse_status_string", "attnfuse_last_error", "attnfuse_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(binding._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.attnfuse_status_string(code)
+    assert lib.attnfuse_version().startswith(b"libattnfuse")
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, B=1, Hq=4, Hkv=2, N=128, d=64, base=1e4, mode=0, dtype=0,
+        ws=None, ws_bytes=0):
+    return lib.attnfuse_rope_causal_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, base, mode, dtype, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(B=0), 1), (dict(N=0), 1), (dict(Hq=3, Hkv=2), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(dtype=7), 1), (dict(mode=5), 1), (dict(base=0.5), 1),
+    (dict(base=float("nan")), 1), (dict(q=FAKE + 8), 1), (dict(lse=FAKE + 2), 1), (dict(N=1 << 24), 1),
+    (dict(mode=1, ws=FAKE, ws_bytes=16), 1), (dict(mode=1, ws=FAKE + 16, ws_bytes=1 << 40), 1),
+])
+def test_forward_rejects_bad_arguments(lib, kw, status):
+    assert fwd(lib, **kw) == status
+    assert lib.attnfuse_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(d=80), 2), (dict(H=0), 1), (dict(x=FAKE, y=FAKE + 64), 1), (dict(y=FAKE + 4), 1),
+])
+def test_rope_apply_rejects_bad_arguments(lib, kw, status):
+    a = dict(x=FAKE, y=FAKE, B=1, N=16, H=2, d=64, base=1e4, dtype=0)
+    a.update(kw)
+    assert lib.attnfuse_rope_apply(a["x"], a["y"], a["B"], a["N"], a["H"], a["d"], a["base"], a["dtype"], None) == status
+
+
+def test_workspace_bytes(lib):
+    assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 0, 0) == 0
+    q = 1 * 4096 * 32 * 128 * 2
+    k = 1 * 4096 * 8 * 128 * 2
+    assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 1, 0) == q + k
+    assert lib.attnfuse_workspace_bytes(1, 1, 1, 1, 64, 1, 1) == 256 + 256
+    assert lib.attnfuse_workspace_bytes(1, 1, 1, 1, 96, 1, 1) == 0
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd(lib) == 3  # ERR_CUDA: no device; nothing was launched
+    assert lib.attnfuse_device_status(None) == 3
+
+
+def test_diag_rejects_bad_timeout(lib):
+    assert lib.attnfuse_diag_wait_timeout(0, None) == 1
+    assert lib.attnfuse_diag_wait_timeout(2_000_000_000, None) == 1
