@@ -1,0 +1,506 @@
+#!/usr/bin/env python3
+"""Benchmark: causal RoPE attention forward on GB300 through libattnfuse.
+
+Default: the Llama-3-8B attention shape (B=1, Hq=32, Hkv=8, N=4096, d=128, bf16, rope base 5e5),
+fused mode, one step = one attnfuse_rope_causal_fwd call.  Prints ONE JSON line (rank 0):
+value = causal TFLOP/s (2*B*Hq*N^2*d per step) over all ranks, plus roofline, e2e (host buffers,
+copies inside the timed region), the pre-rotate path (RoPE pass GB/s and pipeline TFLOP/s), clocks
+sampled during the timed region and the CPU oracle's throughput on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py --sweep      # crossover sweep: fused vs pre-rotate at every N, then N* per family
+
+Timing: inputs resident in HBM; W untimed warm-up steps; K timed steps, each bracketed by CUDA
+events on the launching stream; a 512 MiB write flushes L2 (129 MB) before every step, outside the
+events; barrier + synchronize on both sides; max over ranks.  Multi-GPU runs are replicas (the
+forward pass needs no collective): every rank runs the full workload on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RoPE+causal attn fwd TFLOP/s and % of GB300 bf16 peak; fused vs pre-rotate N*"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 512 * 1024 * 1024
+KERNEL_SOURCES = ("attention_rope_causal_gb300/csrc/attn_fwd.cu", "attention_rope_causal_gb300/csrc/ptx.cuh",
+                  "attention_rope_causal_gb300/csrc/rope.cuh", "attention_rope_causal_gb300/csrc/rope_apply.cu")
+
+
+# ----------------------------------------------------------------------------------------------
+# host-side helpers (no GPU needed; unit-tested on CPU)
+
+
+def load_peaks(path=None):
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent or taken on other code."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kind][workload]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def aggregate(units_per_rank_step: float, steps: int, n_ranks: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed, over the slowest rank's time."""
+    return units_per_rank_step * steps * n_ranks / max_seconds
+
+
+def crossover(ns, t_fused, t_pre):
+    """N* where fused and pre-rotate times cross: linear interpolation in N of log(t_fused/t_pre)
+    between the two bracketing sweep points.  Returns (n_star or None, description)."""
+    import math
+    r = [math.log(a / b) for a, b in zip(t_fused, t_pre)]
+    for i in range(len(ns) - 1):
+        if r[i] == 0.0:
+            return float(ns[i]), "equal at a sweep point"
+        if (r[i] < 0) != (r[i + 1] < 0):
+            n = ns[i] + (ns[i + 1] - ns[i]) * (0.0 - r[i]) / (r[i + 1] - r[i])
+            who = "fused faster below N*" if r[i] < 0 else "pre-rotate faster below N*"
+            return n, who
+    if all(x < 0 for x in r):
+        return None, f"fused faster at every N in [{ns[0]}, {ns[-1]}]"
+    return None, f"pre-rotate faster at every N in [{ns[0]}, {ns[-1]}]"
+
+
+def parse_clocks(csv_text: str, t0: float, t1: float):
+    """Median SM clock and throttle reasons from nvidia-smi CSV samples taken in [t0, t1] (epoch s)."""
+    import datetime
+    mhz, maxmhz, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in csv_text.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10 or parts[0].startswith("timestamp"):
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            continue
+        if not (t0 - 0.25 <= ts <= t1 + 0.25):
+            continue
+        try:
+            mhz.append(float(parts[2].split()[0]))
+            maxmhz = float(parts[3].split()[0])
+        except (ValueError, IndexError):
+            continue
+        for name, val in zip(names, parts[6:10]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not mhz:
+        return None
+    return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": maxmhz, "samples": len(mhz), "reasons": sorted(reasons)}
+
+
+class ClockSampler:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader", "-lms", "100"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            text = f.read()
+        os.unlink(self.file.name)
+        return parse_clocks(text, t0, t1)
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed plumbing (replicas; the only collectives are the timing barrier and max)
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------------
+# the CPU oracle as a baseline (bounded row samples of the same workload)
+
+
+def oracle_rows_flops(w, rows):
+    return float(sum(4 * w.d * (int(i) + 1) for i in rows)) * w.Hq * w.B
+
+
+def oracle_sample_rows(w, target_s: float, q, k, v):
+    """Pick an evenly strided row sample whose oracle run takes about target_s on this host."""
+    import numpy as np
+    import oracle
+    probe = np.arange(0, w.N, max(1, w.N // 32))
+    t = time.perf_counter()
+    oracle.rope_causal(q, k, v, w.rope_base, rows=probe)
+    dt = max(time.perf_counter() - t, 1e-3)
+    rate = oracle_rows_flops(w, probe) / dt
+    want = target_s * rate
+    stride = max(1, int(round(oracle_rows_flops(w, np.arange(w.N)) / max(want, 1.0))))
+    return stride
+
+
+def run_cpu_baseline(w, target_s=12.0):
+    import numpy as np
+    import oracle
+    from attention_rope_causal_gb300 import inputs
+    q, k, v = inputs.make_inputs(w)
+    stride = oracle_sample_rows(w, target_s, q, k, v)
+    rows = np.arange(0, w.N, stride)
+    t = time.perf_counter()
+    oracle.rope_causal(q, k, v, w.rope_base, rows=rows)
+    dt = time.perf_counter() - t
+    fl = oracle_rows_flops(w, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{w.name}: every {stride}th query row ({len(rows)} rows x {w.Hq} heads), fp64 C oracle, "
+                      f"{dt:.1f} s, {fl / 1e9:.1f} GFLOP causal-equivalent"}
+
+
+def run_reference_arm(args):
+    """The reference arm of this benchmark is the CPU oracle, timed as it stands on this host."""
+    import numpy as np
+    import oracle
+    from attention_rope_causal_gb300 import inputs
+    rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
+    if rank != 0:
+        return 0
+    w = inputs.NAMED[args.workload]
+    q, k, v = inputs.make_inputs(w)
+    budget = 150.0 / max(1, args.steps + args.warmup)  # seconds per step: the whole run in a few minutes
+    stride = oracle_sample_rows(w, budget, q, k, v)
+    fl_total, t_total = 0.0, 0.0
+    for s in range(args.warmup + args.steps):
+        rows = np.arange(s % stride, w.N, stride)
+        t = time.perf_counter()
+        oracle.rope_causal(q, k, v, w.rope_base, rows=rows)
+        dt = time.perf_counter() - t
+        if s >= args.warmup:
+            fl_total += oracle_rows_flops(w, rows)
+            t_total += dt
+    value = fl_total / t_total / 1e12
+    sample = (f"{w.name}: each step every {stride}th query row (offset rotating) x {w.Hq} heads, fp64 C oracle "
+              f"on {oracle.default_threads()} host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / max(1, args.steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                       "rope_base": w.rope_base},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.default_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU timing
+
+
+def time_steps(fn, steps, flush, stream):
+    """Per-step CUDA-event times (ms) of fn() with an L2 flush before each step, outside the events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def gpu_setup(w, modes):
+    import torch
+    from attention_rope_causal_gb300 import binding, inputs
+    q, k, v = (t.cuda() for t in inputs.make_inputs(w))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device="cuda")
+    ws = {m: torch.empty(max(256, binding.workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, m, q.dtype)),
+                         dtype=torch.uint8, device="cuda") for m in modes}
+    return q, k, v, out, lse, ws
+
+
+def fwd_fn(w, q, k, v, out, lse, ws, mode, stream):
+    from attention_rope_causal_gb300 import binding
+    return lambda: binding.rope_causal_fwd(q, k, v, w.rope_base, mode=mode, out=out, lse=lse, workspace=ws,
+                                           stream=stream)
+
+
+def measure_point(w, steps, warmup):
+    """Median-of-steps times (ms) for fused, pre-rotate pipeline and the RoPE pass alone."""
+    import torch
+    from attention_rope_causal_gb300 import binding
+    stream = torch.cuda.current_stream()
+    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    qr = torch.empty_like(q)
+    kr = torch.empty_like(k)
+    res = {}
+    for mode in ("fused", "prerotate"):
+        f = fwd_fn(w, q, k, v, out, lse, ws[mode], mode, stream)
+        time_steps(f, warmup, flush, stream)
+        res[mode] = statistics.median(time_steps(f, steps, flush, stream))
+
+    def rope_pass():
+        binding.rope_apply(q, w.rope_base, out=qr, stream=stream)
+        binding.rope_apply(k, w.rope_base, out=kr, stream=stream)
+    time_steps(rope_pass, warmup, flush, stream)
+    res["rope"] = statistics.median(time_steps(rope_pass, steps, flush, stream))
+    if binding.device_status() != 0:
+        raise RuntimeError(f"device status: {binding.last_error()}")
+    return res
+
+
+def run_sweep(args):
+    from attention_rope_causal_gb300 import inputs
+    peaks = load_peaks()
+    rows = []
+    for w in inputs.sweep_workloads():
+        t = measure_point(w, args.steps, args.warmup)
+        fl = w.causal_flops
+        qk_bytes = 2 * (w.B * w.N * (w.Hq + w.Hkv) * w.d * 2)
+        rec = {"workload": w.name, "N": w.N, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "dtype": w.dtype,
+               "fused_ms": t["fused"], "prerotate_ms": t["prerotate"], "rope_ms": t["rope"],
+               "fused_tflops": fl / t["fused"] / 1e9, "prerotate_tflops": fl / t["prerotate"] / 1e9,
+               "rope_gbs": qk_bytes / t["rope"] / 1e6, "fused_over_prerotate": t["fused"] / t["prerotate"]}
+        rows.append(rec)
+        print(json.dumps(rec), flush=True)
+    summary = {}
+    for fam in ("gqa", "mha"):
+        for dt in ("bf16", "fp16"):
+            pts = [r for r in rows if r["workload"].startswith(f"sweep_{fam}_") and r["dtype"] == dt]
+            pts.sort(key=lambda r: r["N"])
+            n_star, how = crossover([r["N"] for r in pts], [r["fused_ms"] for r in pts],
+                                    [r["prerotate_ms"] for r in pts])
+            summary[f"{fam}_{dt}"] = {"n_star": n_star, "note": how}
+    print(json.dumps({"sweep_summary": summary, "peaks": peaks}), flush=True)
+    return 0
+
+
+def run_only(args):
+    """Run one path alone (for profilers): W + K steps of `fused`, `prerotate` or `rope` with L2 flushes."""
+    import torch
+    from attention_rope_causal_gb300 import binding, build, inputs
+    build.build()
+    binding.load()
+    torch.cuda.set_device(0)
+    w = inputs.NAMED[args.workload]
+    stream = torch.cuda.current_stream()
+    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    if args.only == "rope":
+        qr, kr = torch.empty_like(q), torch.empty_like(k)
+
+        def f():
+            binding.rope_apply(q, w.rope_base, out=qr, stream=stream)
+            binding.rope_apply(k, w.rope_base, out=kr, stream=stream)
+    else:
+        f = fwd_fn(w, q, k, v, out, lse, ws[args.only], args.only, stream)
+    ms = time_steps(f, args.warmup + args.steps, flush, stream)[args.warmup:]
+    st = binding.device_status()
+    print(json.dumps({"only": args.only, "workload": w.name, "median_ms": statistics.median(ms), "status": st}))
+    return 0 if st == 0 else 1
+
+
+def run_ours(args):
+    import torch
+    from attention_rope_causal_gb300 import binding, build, inputs
+    rank, world, local = dist_setup(args)
+    build.build()
+    binding.load()
+    w = inputs.NAMED[args.workload]
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    step = fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)
+
+    time_steps(step, args.warmup, flush, stream)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms = time_steps(step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    st = binding.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {binding.last_error()}")
+    total_s = max_over_ranks(sum(ms) / 1e3, world)
+    value = aggregate(w.causal_flops / 1e12, args.steps, world, total_s)
+    per_launch_ms = statistics.mean(ms)
+
+    # end to end through the C ABI with host buffers: pinned H2D of q, k, v, the call, D2H of out, lse
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    time_steps(e2e_step, args.warmup, flush, stream)
+    barrier(world)
+    e2e_ms = time_steps(e2e_step, args.steps, flush, stream)
+    barrier(world)
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    # the competing pre-rotation path, and the RoPE pass alone (HBM-bound)
+    pre = fwd_fn(w, q, k, v, out, lse, ws["prerotate"], "prerotate", stream)
+    time_steps(pre, args.warmup, flush, stream)
+    pre_ms = statistics.median(time_steps(pre, max(20, args.steps // 10), flush, stream))
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+
+    def rope_pass():
+        binding.rope_apply(q, w.rope_base, out=qr, stream=stream)
+        binding.rope_apply(k, w.rope_base, out=kr, stream=stream)
+    time_steps(rope_pass, args.warmup, flush, stream)
+    rope_ms = statistics.median(time_steps(rope_pass, max(20, args.steps // 10), flush, stream))
+    rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
+    if binding.device_status() != 0:
+        raise RuntimeError(f"device status: {binding.last_error()}")
+
+    if rank != 0:
+        return 0
+    achieved = w.causal_flops / (per_launch_ms / 1e3) / 1e12
+    traffic = load_traffic("attn_fwd_fused", w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                   "rope_base": w.rope_base, "mode": "fused", "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every step (512 MiB write, outside the timed events)"},
+        "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<d=128, fused RoPE, bf16>",
+                     "peak_source": f"{peaks['source']} (dense bf16 burst)"},
+        "e2e": {"value": aggregate(w.causal_flops / 1e12, args.steps, world, e2e_s), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "prerotate": {"ms": pre_ms, "tflops": w.causal_flops / (pre_ms / 1e3) / 1e12, "rope_ms": rope_ms,
+                      "rope_gbs": rope_bytes / (rope_ms / 1e3) / 1e9,
+                      "rope_frac_of_hbm": rope_bytes / (rope_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                      "fused_over_prerotate": per_launch_ms / pre_ms},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = run_cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    from attention_rope_causal_gb300 import inputs
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=inputs.LLAMA.name, choices=sorted(inputs.NAMED))
+    ap.add_argument("--sweep", action="store_true", help="run the crossover sweep instead")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("fused", "prerotate", "rope"), help="time one path alone (for profilers)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference_arm(args)
+    if args.only:
+        return run_only(args)
+    if args.sweep:
+        from attention_rope_causal_gb300 import binding, build
+        import torch
+        build.build()
+        binding.load()
+        torch.cuda.set_device(0)
+        return run_sweep(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,5 +1,9 @@
-"""Pre-rotation kernel (attnfuse_rope_apply) against the oracle's fp64 rotation: every element
-within one unit in the last place of the output dtype of the exactly rotated value."""
+"""Pre-rotation kernel (attnfuse_rope_apply) against the oracle's fp64 rotation.
+
+Bound per element: one unit in the last place of the output dtype at the exact value, plus
+2^-20 (|x_k| + |x_{k+d/2}|) for the pair's fp32 arithmetic and its cos/sin (angle error below
+4e-7 rad).  The second term matters only where x cos and y sin nearly cancel, where no fp32
+evaluation can promise one ulp of the (tiny) result."""
 import numpy as np
 import pytest
 import torch
@@ -43,9 +47,14 @@ def test_rope_apply_matches_oracle(B, N, H, d, dtype, base, sigma):
     ref = oracle.rope_rotate(x, base, positions=np.tile(np.arange(N, dtype=np.float64), B).reshape(B * N))
     ref = ref.reshape(B, N, H, d)
     err = np.abs(y.double().numpy() - ref)
-    bound = ulp(ref, dtype)
+    xd = x.double().numpy()
+    half = d // 2
+    pair = np.abs(xd) + np.abs(np.concatenate([xd[..., half:], xd[..., :half]], axis=-1))
+    bound = ulp(ref, dtype) + 2.0 ** -20 * pair
     worst = float((err / bound).max())
-    assert worst <= 1.0, f"max error {worst:.3f} ulp"
+    assert worst <= 1.0, f"max error {worst:.3f} of the bound"
+    # and most elements are correctly rounded or one ulp off
+    assert float((err <= ulp(ref, dtype)).mean()) > 0.999
 
 
 def test_rope_apply_in_place():
