@@ -27,6 +27,11 @@ _SIGNATURES = {
                                                 ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "attnfuse_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 7),
+    "attnfuse_rope_causal_fwd_prerotate_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                                  ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                                                  ctypes.c_void_p]),
     "attnfuse_rope_apply": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_void_p]),
     "attnfuse_device_status": (ctypes.c_int, [ctypes.c_void_p]),

@@ -134,6 +134,17 @@ attnfuse_status_t validate_fwd(const void* q, const void* k, const void* v, cons
 
 }  // namespace
 
+namespace attnfuse {
+
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+}
+
+}  // namespace attnfuse
+
 extern "C" {
 
 const char* attnfuse_version(void) { return "libattnfuse 0.1 (sm_103a)"; }

@@ -61,4 +61,7 @@ cudaError_t launch_diag_wait_timeout(unsigned long long timeout_ns, cudaStream_t
 // Fills F_k = round(theta_k / (2 pi) * 2^64), theta_k = base^(-2k/d).
 void rope_freqs_host(int d, double base, RopeFreqs* f);
 
+// Sets the calling thread's attnfuse_last_error() message (printf-style).
+void set_last_error(const char* fmt, ...);
+
 }  // namespace attnfuse

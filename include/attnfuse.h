@@ -96,6 +96,32 @@ attnfuse_status_t attnfuse_device_status(void* stream);
  */
 attnfuse_status_t attnfuse_diag_wait_timeout(uint64_t timeout_ns, void* stream);
 
+/*
+ * Size of the fixed scratch buffer behind attnfuse_rope_causal_fwd_prerotate_noalloc (64 MiB: the
+ * rotated Q and K of the Llama-3-8B attention shape, B=1, N=4096, 32+8 heads, d=128, take 42 MB).
+ */
+#define ATTNFUSE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Pre-rotate forward that allocates nothing.  The AttnFuse pages have no counterpart to this call:
+ * it exists for callers that cannot allocate device memory -- e.g. a framework whose own caching
+ * allocator has reserved the GPU's memory, or code that must not risk an allocation failure or
+ * stall in the middle of a step -- and that also cannot lend a workspace.
+ *
+ * Same arguments and result as attnfuse_rope_causal_fwd with mode = ATTNFUSE_PREROTATE, except that
+ * the rotated Q and K go to a fixed buffer of ATTNFUSE_NOALLOC_SCRATCH_BYTES compiled into the
+ * library (a __device__ array: every GPU that loads the library holds it until the process exits).
+ * Calls whose rotated Q and K need more than that (attnfuse_workspace_bytes(..., PREROTATE, ...))
+ * return ATTNFUSE_ERR_INVALID_ARG before launching anything.  No cudaMalloc, cudaFree or other
+ * allocating call is made.  The first call on each device looks up the buffer's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before any stream capture.
+ * All calls share the one buffer and it keeps the last call's contents: calls that may overlap on
+ * the GPU (other streams, other host threads) race on it and must be ordered by the caller.
+ */
+attnfuse_status_t attnfuse_rope_causal_fwd_prerotate_noalloc(const void* q, const void* k, const void* v, void* out,
+                                                              float* lse, int B, int Hq, int Hkv, int N, int d,
+                                                              double rope_base, attnfuse_dtype_t dtype, void* stream);
+
 /* Static description of a status code. */
 const char* attnfuse_status_string(attnfuse_status_t status);
 
