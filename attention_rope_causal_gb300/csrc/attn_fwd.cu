@@ -33,6 +33,7 @@
 #include <type_traits>
 
 #include "attnfuse_internal.h"
+#include "exp2_poly.cuh"
 #include "ptx.cuh"
 #include "rope.cuh"
 
@@ -52,8 +53,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// Register split after setmaxnreg: 128 x (56 + 88) + 256 x 184 = 65536 = 512 threads x 128.
-constexpr uint32_t kRegsCtrl = 56, kRegsSoftmax = 184, kRegsRotate = 88;
+// Register split after setmaxnreg: 128 x (56 + 104) + 256 x 176 = 65536 = 512 threads x 128.
+constexpr uint32_t kRegsCtrl = 56, kRegsSoftmax = 176, kRegsRotate = 104;
+
+// Which 32-column chunks of a score row take their exponentials from the FMA-pipe polynomial
+// (exp2_poly.cuh) instead of the MUFU unit (bit c set = chunk c).
+constexpr uint32_t kPolyChunkMask = 0u;
 static_assert(128 * (kRegsCtrl + kRegsRotate) + 256 * kRegsSoftmax == kThreads * 128, "register split");
 
 template <int D>
@@ -113,7 +118,10 @@ __device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigne
   }
 }
 
-// Whole-warp wait with a warp-uniform outcome.
+// Whole-warp wait with a warp-uniform outcome.  Lane 0 polls (32 lanes polling one barrier word
+// would multiply the shared-memory traffic by 32); once it sees the phase complete, every lane
+// performs one try_wait of its own, which succeeds at once and gives each lane acquire ordering
+// (the phase cannot advance again before this warp has consumed it).
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, Ctrl& ctl,
                                               unsigned long long timeout_ns) {
   bool ok = wait_bar(bar, parity, ctl, timeout_ns);
@@ -134,29 +142,49 @@ __device__ __forceinline__ void pair_offsets(int r, int ck, uint32_t& xo, uint32
   }
 }
 
-// Rotate rows [0, nrows) of the Q tiles (positions q_row0 + row) with exact per-element angles,
-// the same arithmetic as the pre-rotation kernel.  Threads tid = 0 .. nthr-1 share the items.
+// Thread -> (chunk ck, first row r0) for rotating a 128-row tile with 128 threads: a thread keeps one
+// chunk (8 frequencies) and walks rows r0, r0 + RS, ... (RS = 16 for d = 128, 32 for d = 64).  Eight
+// consecutive lanes cover eight distinct 16-byte chunks of one 128-byte row (d = 128) or two rows
+// whose swizzle differs by 4 (d = 64), so every 16-byte shared access is free of bank conflicts.
+template <int D>
+__device__ __forceinline__ void rot_mapping(int rt, int& ck, int& r0) {
+  const int w = rt >> 5, lane = rt & 31;
+  if constexpr (D == 128) {
+    ck = lane & 7;
+    r0 = w * 4 + (lane >> 3);
+  } else {
+    ck = lane & 3;
+    const int q = lane >> 2;
+    r0 = w * 8 + (((q & 1) << 2) | (q >> 1));
+  }
+}
+
+template <int D>
+struct RotGeom {
+  static constexpr int PASSES = D == 128 ? 8 : 4;
+  static constexpr int RS = 128 / PASSES;
+};
+
+// Rotate, in place, the thread's rows of one 128-row tile held in shared memory at `tile`.  cs holds
+// the cos/sin of the thread's first row; step is the exact rotation by RS rows.
 template <int D, bool BF16>
-__device__ __forceinline__ void rotate_q_tiles(uint8_t* sq, int nrows, int q_row0, int tid, int nthr,
-                                               const AttnParams& p) {
-  constexpr int NCH = D / 16;
-  for (int item = tid; item < nrows * NCH; item += nthr) {
-    const int row = item / NCH;
-    const int ck = item - row * NCH;
-    const int tile = row / BM;
-    const int r = row - tile * BM;
-    float c[8], s[8];
+__device__ __forceinline__ void rotate_tile(uint32_t tile, int r0, int ck, RopeCS8 cs, const RopeCS8& step) {
+  constexpr int PASSES = RotGeom<D>::PASSES, RS = RotGeom<D>::RS;
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
-      rope_cs((uint32_t)(q_row0 + row), p.freqs.lo[ck * 8 + t], p.freqs.hi[ck * 8 + t], c[t], s[t]);
-    uint32_t xo, yo;
-    pair_offsets<D>(r, ck, xo, yo);
-    uint8_t* base = sq + (size_t)tile * Cfg<D>::TILE;
-    uint4 xv = *reinterpret_cast<uint4*>(base + xo);
-    uint4 yv = *reinterpret_cast<uint4*>(base + yo);
-    rope_rotate_chunk<BF16>(xv, yv, c, s);
-    *reinterpret_cast<uint4*>(base + xo) = xv;
-    *reinterpret_cast<uint4*>(base + yo) = yv;
+  for (int pass = 0; pass < PASSES; pass += 2) {
+    uint32_t xo0, yo0, xo1, yo1;
+    pair_offsets<D>(r0 + pass * RS, ck, xo0, yo0);
+    pair_offsets<D>(r0 + (pass + 1) * RS, ck, xo1, yo1);
+    uint4 x0 = ptx::lds128(tile + xo0), y0 = ptx::lds128(tile + yo0);
+    uint4 x1 = ptx::lds128(tile + xo1), y1 = ptx::lds128(tile + yo1);
+    rope_rotate_chunk_cs8<BF16>(x0, y0, cs);
+    rope_cs8_advance(cs, step);
+    rope_rotate_chunk_cs8<BF16>(x1, y1, cs);
+    if (pass + 2 < PASSES) rope_cs8_advance(cs, step);
+    ptx::sts128(tile + xo0, x0);
+    ptx::sts128(tile + yo0, y0);
+    ptx::sts128(tile + xo1, x1);
+    ptx::sts128(tile + yo1, y1);
   }
 }
 
@@ -196,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_addr(ctl.q_full), 1);
-    ptx::mbar_init(bar_addr(ctl.q_ready), 3 * 128);
+    ptx::mbar_init(bar_addr(ctl.q_ready), 2 * 128);
     for (int s = 0; s < KST; ++s) {
       ptx::mbar_init(bar_addr(ctl.k_full[s]), 1);
       ptx::mbar_init(bar_addr(ctl.k_ready[s]), 128);
@@ -340,9 +368,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!skip) {
       bool ok = true;
       if constexpr (ROTATE) {
+        // Each softmax warpgroup rotates its own query tile once (positions q_row0 + 128 wi + r).
         ok = wait_bar_warp(bar_addr(ctl.q_full), 0, ctl, tmo);
         if (ok) {
-          rotate_q_tiles<D, BF16>(sgen + C::OFF_Q, active1 ? 2 * BM : BM, q_row0, threadIdx.x - 128, 3 * 128, p);
+          const int wq = (warp - 4) / 4;
+          if (wq == 0 || active1) {
+            int ck, r0;
+            rot_mapping<D>(threadIdx.x - 128 - 128 * wq, ck, r0);
+            RopeCS8 cs, step;
+            rope_cs8_exact((uint32_t)(q_row0 + wq * BM + r0), p.freqs, ck * 8, cs);
+            rope_cs8_exact((uint32_t)RotGeom<D>::RS, p.freqs, ck * 8, step);
+            rotate_tile<D, BF16>(sQ + wq * C::TILE, r0, ck, cs, step);
+          }
           ptx::fence_proxy_async_smem();
           ptx::mbar_arrive(bar_addr(ctl.q_ready));
         }
@@ -371,11 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // Row max: three-input max tree, eight independent chains.
+        float acc[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int k = 0; k < 8; ++k)
+          acc[k] = ptx::fmax3(__uint_as_float(sv[0][k]), __uint_as_float(sv[0][k + 8]), __uint_as_float(sv[0][k + 16]));
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
+        for (int base = 24; base < 120; base += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i0 = base + k, i1 = base + 8 + k;
+            acc[k] = ptx::fmax3(acc[k], __uint_as_float(sv[i0 / 32][i0 % 32]), __uint_as_float(sv[i1 / 32][i1 % 32]));
+          }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = fmaxf(acc[k], __uint_as_float(sv[3][24 + k]));
+        const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
+                                    fmaxf(acc[6], acc[7]));
         const float m_new = fmaxf(m_run, mx * sl2);
         // Rescale only when some row's max grew past the threshold (warp-uniform decision, since
         // TMEM loads and stores are warp-collective); otherwise keep the stale max.
@@ -392,32 +440,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_run = m_new;
           }
         }
-        const float neg_m = -m_run;
-        float sum = 0.f;
+        // P = 2^(s * log2(e)/sqrt(d) - m) on fp32 pairs; four independent partial row sums.
+        const uint64_t SL2 = ptx::f2_pack(sl2, sl2), NM = ptx::f2_pack(-m_run, -m_run);
+        uint64_t part[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) part[k] = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[c][2 * e]), sl2, neg_m));
-            const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl2, neg_m));
-            sum += p0 + p1;
+            const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])),
+                                            SL2, NM);
+            float p0, p1;
+            if ((kPolyChunkMask >> c) & 1u) {
+              exp2_poly_pair(x2, p0, p1);
+            } else {
+              float x0, x1;
+              ptx::f2_unpack(x2, x0, x1);
+              p0 = ptx::ex2_approx(x0);
+              p1 = ptx::ex2_approx(x1);
+            }
+            part[e & 3] = ptx::f2_add(part[e & 3], ptx::f2_pack(p0, p1));
             pk[e] = Pack<BF16>::pack(p0, p1);
           }
           ptx::tmem_st16(tS + 16 * c, pk);
         }
-        l_run += sum;
+        float sum;
+        {
+          float a, bb;
+          ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), a, bb);
+          sum = a + bb;
+        }
         if (rescale) {  // O += P V for this tile is issued only after p_full, so O is stable here
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             ptx::tmem_ld32(tO + 32 * c, o);
             ptx::tmem_wait_ld();
+            const uint64_t A2 = ptx::f2_pack(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            for (int e = 0; e < 16; ++e) {
+              const uint64_t v = ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), A2);
+              float a, bb;
+              ptx::f2_unpack(v, a, bb);
+              o[2 * e] = __float_as_uint(a);
+              o[2 * e + 1] = __float_as_uint(bb);
+            }
             ptx::tmem_st32(tO + 32 * c, o);
           }
         }
+        l_run += sum;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(ctl.p_full[wi]));
@@ -451,68 +524,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::setmaxnreg_dec<kRegsRotate>();
     if constexpr (ROTATE) {
       if (!skip) {
-        bool ok = wait_bar_warp(bar_addr(ctl.q_full), 0, ctl, tmo);
-        if (ok) {
-          rotate_q_tiles<D, BF16>(sgen + C::OFF_Q, active1 ? 2 * BM : BM, q_row0, threadIdx.x - 128, 3 * 128, p);
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(bar_addr(ctl.q_ready));
-        }
         // ============================== K-tile rotation =========================================
-        // Thread mapping: fixed chunk ck (8 frequencies), rows r0 + RS * pass.  The cos/sin of the
-        // thread's rows are carried by angle addition: exact values at position r0 of key tile 0,
-        // advanced by the exact rotation of RS positions between passes and of 128 positions
-        // between tiles (error grows by ~1 fp32 rounding per step: < 3e-5 after 32768 positions).
-        const int rt = threadIdx.x - 384;
-        const int w = rt / 32;
-        int ck, r0, RS;
-        if constexpr (D == 128) {
-          ck = lane & 7;
-          r0 = w * 4 + (lane >> 3);
-          RS = 16;
-        } else {
-          // rows of one 8-lane phase differ by 4, so their chunks (ck ^ (r & 7)) never share banks
-          ck = lane & 3;
-          const int q = lane >> 2;
-          r0 = w * 8 + (((q & 1) << 2) | (q >> 1));
-          RS = 32;
-        }
-        constexpr int PASSES = D == 128 ? 8 : 4;
-        float c0[8], s0[8], cR[8], sR[8], cT[8], sT[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t lo = p.freqs.lo[ck * 8 + e], hi = p.freqs.hi[ck * 8 + e];
-          rope_cs((uint32_t)r0, lo, hi, c0[e], s0[e]);
-          rope_cs((uint32_t)RS, lo, hi, cR[e], sR[e]);
-          rope_cs((uint32_t)BN, lo, hi, cT[e], sT[e]);
-        }
+        // cos/sin are carried along the thread's rows by angle addition: exact values at row r0 of
+        // key tile 0, advanced by the exact rotation of RS rows between passes and of 128 rows
+        // between tiles (one fp32 rounding per step: relative drift < 3e-5 after 32768 positions).
+        int ck, r0;
+        rot_mapping<D>(threadIdx.x - 384, ck, r0);
+        RopeCS8 tile_cs, step, step_tile;
+        rope_cs8_exact((uint32_t)r0, p.freqs, ck * 8, tile_cs);
+        rope_cs8_exact((uint32_t)RotGeom<D>::RS, p.freqs, ck * 8, step);
+        rope_cs8_exact((uint32_t)BN, p.freqs, ck * 8, step_tile);
+        bool ok = true;
         for (int i = 0; i < n_kt && ok; ++i) {
           const int ks = i % KST, kph = (i / KST) & 1;
           if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
-          uint8_t* kt = sgen + C::OFF_K + ks * C::TILE;
-          float c[8], s[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            c[e] = c0[e];
-            s[e] = s0[e];
-          }
-#pragma unroll
-          for (int pass = 0; pass < PASSES; ++pass) {
-            uint32_t xo, yo;
-            pair_offsets<D>(r0 + pass * RS, ck, xo, yo);
-            uint4 xv = *reinterpret_cast<uint4*>(kt + xo);
-            uint4 yv = *reinterpret_cast<uint4*>(kt + yo);
-            rope_rotate_chunk<BF16>(xv, yv, c, s);
-            *reinterpret_cast<uint4*>(kt + xo) = xv;
-            *reinterpret_cast<uint4*>(kt + yo) = yv;
-            if (pass + 1 < PASSES) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) rope_advance(c[e], s[e], cR[e], sR[e]);
-            }
-          }
+          rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, tile_cs, step);
           ptx::fence_proxy_async_smem();
           ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
-#pragma unroll
-          for (int e = 0; e < 8; ++e) rope_advance(c0[e], s0[e], cT[e], sT[e]);
+          rope_cs8_advance(tile_cs, step_tile);
         }
       }
     }

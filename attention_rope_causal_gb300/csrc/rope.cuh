@@ -20,6 +20,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace attnfuse {
 
 constexpr int kMaxHalfDim = 64;  // d <= 128
@@ -94,6 +96,64 @@ __device__ __forceinline__ void rope_rotate_chunk(uint4& xv, uint4& yv, const fl
     rope_pair(x1, y1, c[2 * w + 1], s[2 * w + 1], a1, b1);
     xw[w] = Pack<BF16>::pack(a0, a1);
     yw[w] = Pack<BF16>::pack(b0, b1);
+  }
+}
+
+// ---- packed form: cos/sin of 8 consecutive frequencies as 4 fp32 pairs --------------------------
+
+struct RopeCS8 {
+  uint64_t c[4], s[4];
+};
+
+// Exact cos/sin of pos * theta_k for k = k0 .. k0 + 7.
+__device__ __forceinline__ void rope_cs8_exact(uint32_t pos, const RopeFreqs& f, int k0, RopeCS8& o) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float c0, s0, c1, s1;
+    rope_cs(pos, f.lo[k0 + 2 * j], f.hi[k0 + 2 * j], c0, s0);
+    rope_cs(pos, f.lo[k0 + 2 * j + 1], f.hi[k0 + 2 * j + 1], c1, s1);
+    o.c[j] = ptx::f2_pack(c0, c1);
+    o.s[j] = ptx::f2_pack(s0, s1);
+  }
+}
+
+// a <- a * b as unit complex numbers (angle addition), same rounding as rope_advance per lane.
+__device__ __forceinline__ void rope_cs8_advance(RopeCS8& a, const RopeCS8& b) {
+  const uint64_t zero = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t cn = ptx::f2_fma(a.c[j], b.c[j], ptx::f2_mul(a.s[j], ptx::f2_sub(zero, b.s[j])));
+    const uint64_t sn = ptx::f2_fma(a.s[j], b.c[j], ptx::f2_mul(a.c[j], b.s[j]));
+    a.c[j] = cn;
+    a.s[j] = sn;
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint64_t unpack2(uint32_t w) {
+  float lo, hi;
+  Pack<BF16>::unpack(w, lo, hi);
+  return ptx::f2_pack(lo, hi);
+}
+
+// Same rotation as rope_rotate_chunk (bit-identical per element for equal cos/sin), on fp32 pairs:
+// x' = fma(x, c, y * (-s)), y' = fma(y, c, x * s).
+template <bool BF16>
+__device__ __forceinline__ void rope_rotate_chunk_cs8(uint4& xv, uint4& yv, const RopeCS8& cs) {
+  uint32_t* xw = reinterpret_cast<uint32_t*>(&xv);
+  uint32_t* yw = reinterpret_cast<uint32_t*>(&yv);
+  const uint64_t zero = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t x = unpack2<BF16>(xw[j]);
+    const uint64_t y = unpack2<BF16>(yw[j]);
+    const uint64_t xr = ptx::f2_fma(x, cs.c[j], ptx::f2_mul(y, ptx::f2_sub(zero, cs.s[j])));
+    const uint64_t yr = ptx::f2_fma(y, cs.c[j], ptx::f2_mul(x, cs.s[j]));
+    float a0, a1, b0, b1;
+    ptx::f2_unpack(xr, a0, a1);
+    ptx::f2_unpack(yr, b0, b1);
+    xw[j] = Pack<BF16>::pack(a0, a1);
+    yw[j] = Pack<BF16>::pack(b0, b1);
   }
 }
 
