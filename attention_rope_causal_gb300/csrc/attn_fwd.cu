@@ -53,13 +53,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// Register split after setmaxnreg: 128 x (56 + 104) + 256 x 176 = 65536 = 512 threads x 128.
-constexpr uint32_t kRegsCtrl = 56, kRegsSoftmax = 176, kRegsRotate = 104;
-
 // Which 32-column chunks of a score row take their exponentials from the FMA-pipe polynomial
 // (exp2_poly.cuh) instead of the MUFU unit (bit c set = chunk c).
 constexpr uint32_t kPolyChunkMask = 0u;
-static_assert(128 * (kRegsCtrl + kRegsRotate) + 256 * kRegsSoftmax == kThreads * 128, "register split");
+
+// Register split after setmaxnreg (control warps / softmax warps / rotation warps); each sums to
+// 128 x (ctrl + rotate) + 256 x softmax = 65536 = 512 threads x 128 registers at launch.
+template <int D>
+struct Regs {
+  static constexpr uint32_t kCtrl = 64;
+  static constexpr uint32_t kSoftmax = D == 128 ? 168 : 176;
+  static constexpr uint32_t kRotate = D == 128 ? 112 : 96;
+  static_assert(128 * (kCtrl + kRotate) + 256 * kSoftmax == kThreads * 128, "register split");
+};
 
 template <int D>
 struct Cfg {
@@ -69,7 +75,8 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
   static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
   static constexpr uint32_t OFF_CTL = OFF_V + VST * TILE;
-  static constexpr uint32_t SMEM = OFF_CTL + 256 + 1024;  // + control block + alignment slack
+  static constexpr uint32_t OFF_FREQ = OFF_CTL + 256;     // F_k words: lo[64] then hi[64]
+  static constexpr uint32_t SMEM = OFF_FREQ + 512 + 1024;  // + alignment slack
   static constexpr uint32_t COL_O = 2 * BN;               // O0 at 256, O1 at 256 + D
   static_assert(COL_O + 2 * D <= kTmemCols, "TMEM budget");
 };
@@ -245,6 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
   }
+  uint32_t* sfreq = reinterpret_cast<uint32_t*>(sgen + C::OFF_FREQ);
+  if (ROTATE && threadIdx.x >= 128 && threadIdx.x < 256) {
+    const int k = threadIdx.x - 128;
+    sfreq[k] = k < 64 ? p.freqs.lo[k] : p.freqs.hi[k - 64];
+  }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&ctl.tmem_base), kTmemCols);
     ptx::tmem_relinquish();
@@ -258,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();  // setmaxnreg and tcgen05 warp-collectives need converged warps
 
   if (warp < 4) {
-    ptx::setmaxnreg_dec<kRegsCtrl>();
+    ptx::setmaxnreg_dec<Regs<D>::kCtrl>();
     if (!skip && warp == 0 && lane == 0) {
       // ================================ TMA producer ==========================================
       ptx::tma_prefetch_desc(&tmQ);
@@ -299,20 +311,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (!skip && warp == 1 && lane == 0) {
       // ================================ MMA issuer ============================================
+      // Descriptors are built once per operand tile; consecutive K-steps only add a constant to the
+      // start-address field (offsets stay inside the 14-bit field), so nothing but an add separates
+      // two tcgen05.mma issues.
       auto issue_S = [&](int iq, uint32_t kbase) {
-        const uint32_t qbase = sQ + iq * C::TILE;
+        const uint64_t dq = ptx::sdesc_sw128(sQ + iq * C::TILE, 16, 1024);
+        const uint64_t dk = ptx::sdesc_sw128(kbase, 16, 1024);
+        const uint32_t dst = tmem + iq * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-          ptx::mma_ss(tmem + iq * BN, ptx::sdesc_sw128(qbase + off, 16, 1024), ptx::sdesc_sw128(kbase + off, 16, 1024),
-                      IDESC_S, kk > 0 ? 1u : 0u);
+          const uint64_t step = (uint64_t)((kk / 4) * (kBoxBytes >> 4) + (kk % 4) * 2);
+          ptx::mma_ss(dst, dq + step, dk + step, IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_PV = [&](int iq, uint32_t vbase, bool first) {
+        const uint64_t dv = ptx::sdesc_sw128(vbase, kBoxBytes, 1024);
+        const uint32_t dst = tmem + C::COL_O + iq * D, asrc = tmem + iq * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          ptx::mma_ts(tmem + C::COL_O + iq * D, tmem + iq * BN + kk * 8,
-                      ptx::sdesc_sw128(vbase + kk * 2048, kBoxBytes, 1024), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+          ptx::mma_ts(dst, asrc + kk * 8, dv + (uint64_t)(kk * (2048 >> 4)), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
       };
       bool ok = wait_bar(bar_addr(ROTATE ? ctl.q_ready : ctl.q_full), 0, ctl, tmo);
       ptx::tc_fence_after();
@@ -328,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= 1 && i - 1 < n1) {  // P1 of the previous key tile
           const int j = i - 1, vs = j % VST, vph = (j / VST) & 1;
           if (!(ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo))) break;
-          if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
+          // V_j was already seen complete by PV0_j unless tile j is q1's alone
+          if (j >= n0 && !(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
           ptx::tc_fence_after();
           issue_PV(1, sV + vs * C::TILE, j == 0);
           ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
@@ -341,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bar_addr(ctl.k_empty[ks]));
         if (i < n0) {
           const int vs = i % VST, vph = (i / VST) & 1;
-          if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
           if (!(ok = wait_bar(bar_addr(ctl.p_full[0]), i & 1, ctl, tmo))) break;
+          if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
           ptx::tc_fence_after();
           issue_PV(0, sV + vs * C::TILE, i == 0);
           if (n1 == 0) ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
@@ -351,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && n1 > 0) {  // P1 of the last key tile
         const int j = n1 - 1, vs = j % VST, vph = (j / VST) & 1;
-        ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo) && wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo);
+        ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo) &&
+             (j < n0 || wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo));
         if (ok) {
           ptx::tc_fence_after();
           issue_PV(1, sV + vs * C::TILE, j == 0);
@@ -364,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar(bar_addr(ctl.mma_done), 0, 100000000ull);
     }
   } else if (warp < 12) {
-    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    ptx::setmaxnreg_inc<Regs<D>::kSoftmax>();
     if (!skip) {
       bool ok = true;
       if constexpr (ROTATE) {
@@ -376,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int ck, r0;
             rot_mapping<D>(threadIdx.x - 128 - 128 * wq, ck, r0);
             RopeCS8 cs, step;
-            rope_cs8_exact((uint32_t)(q_row0 + wq * BM + r0), p.freqs, ck * 8, cs);
-            rope_cs8_exact((uint32_t)RotGeom<D>::RS, p.freqs, ck * 8, step);
+            rope_cs8_exact((uint32_t)(q_row0 + wq * BM + r0), sfreq, sfreq + 64, ck * 8, cs);
+            rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
             rotate_tile<D, BF16>(sQ + wq * C::TILE, r0, ck, cs, step);
           }
           ptx::fence_proxy_async_smem();
@@ -521,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    ptx::setmaxnreg_dec<kRegsRotate>();
+    ptx::setmaxnreg_dec<Regs<D>::kRotate>();
     if constexpr (ROTATE) {
       if (!skip) {
         // ============================== K-tile rotation =========================================
@@ -531,9 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ck, r0;
         rot_mapping<D>(threadIdx.x - 384, ck, r0);
         RopeCS8 tile_cs, step, step_tile;
-        rope_cs8_exact((uint32_t)r0, p.freqs, ck * 8, tile_cs);
-        rope_cs8_exact((uint32_t)RotGeom<D>::RS, p.freqs, ck * 8, step);
-        rope_cs8_exact((uint32_t)BN, p.freqs, ck * 8, step_tile);
+        rope_cs8_exact((uint32_t)r0, sfreq, sfreq + 64, ck * 8, tile_cs);
+        rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
+        rope_cs8_exact((uint32_t)BN, sfreq, sfreq + 64, ck * 8, step_tile);
         bool ok = true;
         for (int i = 0; i < n_kt && ok; ++i) {
           const int ks = i % KST, kph = (i / KST) & 1;

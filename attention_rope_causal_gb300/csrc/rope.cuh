@@ -11,9 +11,12 @@
 // Angles.  p * theta_k reaches 3.3e4 rad at p = 32767, where an fp32 product is off by up to
 // ~2e-3 rad.  Instead the host stores, per pair k, the frequency in turns as a 64-bit fixed-point
 // fraction F_k = round(theta_k / (2 pi) * 2^64).  The angle in turns, reduced modulo one turn, is
-// then bits [32, 64) of the integer product p * F_k (two integer instructions), read as a signed
-// 32-bit fraction in [-1/2, 1/2) turns, and sincospif() evaluates it with |argument| <= pi.
-// Angle error: <= 2^-32 turn from truncation plus one fp32 rounding of the fraction (~2e-7 rad).
+// then bits [32, 64) of the integer product p * F_k (two integer instructions).  That 32-bit turn
+// fraction is reduced exactly, in integers, to the nearest quarter turn q and a remainder r in
+// [-1/2, 1/2) quarter turns; sin and cos of (pi/2) r come from minimax polynomials (odd degree 7,
+// even degree 8) fitted for this library (csrc/fit_sincos_poly.py; fp32 error <= 1.1e-7), and the
+// quarter turns swap and negate them.  Angle error: 2^-32 turn from truncation plus one fp32
+// rounding of r (< 5e-8 rad).  No table and no library call: the cost is fixed (~25 instructions).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,11 +34,31 @@ struct RopeFreqs {
   uint32_t hi[kMaxHalfDim];  // high 32 bits of F_k
 };
 
+// cos and sin of 2 pi t / 2^32 for a 32-bit turn fraction t.
+__device__ __forceinline__ void sincos_turns(uint32_t t, float& c, float& s) {
+  const uint32_t q = (t + 0x20000000u) >> 30;                  // nearest quarter turn, mod 4
+  const int32_t rem = (int32_t)(t - (q << 30));                // in [-2^29, 2^29)
+  const float r = (float)rem * 9.313225746154785e-10f;         // * 2^-30: quarter turns in [-1/2, 1/2)
+  const float z = __fmul_rn(r, r);
+  const float sp = __fmul_rn(
+      __fmaf_rn(__fmaf_rn(__fmaf_rn(-0.004624062217772007f, z, 0.07968810945749283f), z, -0.6459640860557556f), z,
+                1.5707963705062866f),
+      r);
+  const float cp = __fmaf_rn(
+      __fmaf_rn(__fmaf_rn(__fmaf_rn(0.0009058757568709552f, z, -0.020861255005002022f), z, 0.2536693811416626f), z,
+                -1.2337005138397217f),
+      z, 1.0f);
+  // rotate (cp, sp) by q quarter turns
+  const float c0 = (q & 1u) ? -sp : cp;
+  const float s0 = (q & 1u) ? cp : sp;
+  c = (q & 2u) ? -c0 : c0;
+  s = (q & 2u) ? -s0 : s0;
+}
+
 // cos and sin of pos * theta_k, given F_k split into (flo, fhi).
 __device__ __forceinline__ void rope_cs(uint32_t pos, uint32_t flo, uint32_t fhi, float& c, float& s) {
-  uint32_t turns = __umulhi(pos, flo) + pos * fhi;  // bits [32,64) of pos * F_k (mod 2^64)
-  float half_turns = (float)(int32_t)turns * 4.6566128730773926e-10f;  // * 2^-31
-  sincospif(half_turns, &s, &c);
+  const uint32_t turns = __umulhi(pos, flo) + pos * fhi;  // bits [32,64) of pos * F_k (mod 2^64)
+  sincos_turns(turns, c, s);
 }
 
 // (c, s) <- (c, s) * (c2, s2) as unit complex numbers: the angle advances by the angle of (c2, s2).
@@ -105,13 +128,15 @@ struct RopeCS8 {
   uint64_t c[4], s[4];
 };
 
-// Exact cos/sin of pos * theta_k for k = k0 .. k0 + 7.
-__device__ __forceinline__ void rope_cs8_exact(uint32_t pos, const RopeFreqs& f, int k0, RopeCS8& o) {
+// Exact cos/sin of pos * theta_k for k = k0 .. k0 + 7; lo/hi point at the F_k words (any memory
+// space; kernels pass a shared-memory copy so per-lane indices do not serialise constant loads).
+__device__ __forceinline__ void rope_cs8_exact(uint32_t pos, const uint32_t* lo, const uint32_t* hi, int k0,
+                                               RopeCS8& o) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float c0, s0, c1, s1;
-    rope_cs(pos, f.lo[k0 + 2 * j], f.hi[k0 + 2 * j], c0, s0);
-    rope_cs(pos, f.lo[k0 + 2 * j + 1], f.hi[k0 + 2 * j + 1], c1, s1);
+    rope_cs(pos, lo[k0 + 2 * j], hi[k0 + 2 * j], c0, s0);
+    rope_cs(pos, lo[k0 + 2 * j + 1], hi[k0 + 2 * j + 1], c1, s1);
     o.c[j] = ptx::f2_pack(c0, c1);
     o.s[j] = ptx::f2_pack(s0, s1);
   }
