@@ -10,16 +10,19 @@
 // Relative-Position Attention via Structure-Aware Kernels", prerequisites: FlashAttention and
 // online softmax), in fp32 and with base-2 exponentials (same page, technical novelty (4)).
 //
-// Structure (one CTA = 256 query rows of one (b, h) = two 128-row tiles q0, q1; 512 threads):
-//   warp 0        TMA producer: Q once, then K and V tiles (128 keys) through 2-stage rings.
+// Structure: persistent, one CTA (512 threads) per SM walking a list of work units; a unit is 256
+// query rows of one (b, h) = two 128-row tiles q0, q1.
+//   warp 0        TMA producer: per unit Q, and K and V tiles (128 keys) through 2-stage rings.
 //   warp 1        tcgen05.mma issuer; owns the tensor-memory allocation (512 columns:
 //                 S0 | S1 | O0 | O1, P_i written over the first half of S_i).
 //   warps 4-7     softmax for q0 (thread = query row = TMEM lane), epilogue for q0.
 //   warps 8-11    softmax for q1, epilogue for q1.
-//   warps 12-15   fused mode: rotate each K tile in shared memory before its QK^T MMA.
-//   (warps 4-15 also rotate the Q tiles once, at the start, in fused mode.)
+//   warps 12-15   fused mode: rotate the Q tiles and every K tile in shared memory before their
+//                 QK^T MMAs.
 // MMA order per key tile i: S0_i, PV1_{i-1}, S1_i, PV0_i, so that each softmax warpgroup works on
-// one tile while the tensor cores run the other's products.  Fully masked key tiles are never
+// one tile while the tensor cores run the other's products; the pending PV1 of a unit's last tile
+// is issued after the next unit's first S0, and the next unit's Q is loaded as soon as the last
+// QK^T of the current unit is done with the Q buffer.  Fully masked key tiles are never
 // loaded (tile i runs for query tile qt only while i <= qt); the diagonal tile is masked per
 // element.  Softmax rescales O only when a row max grows by more than 2^8, which keeps the result
 // exact (the stale max is used consistently for P, l and lse).
@@ -57,14 +60,15 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // (exp2_poly.cuh) instead of the MUFU unit (bit c set = chunk c).
 constexpr uint32_t kPolyChunkMask = 0u;
 
-// Register split after setmaxnreg (control warps / softmax warps / rotation warps); each sums to
-// 128 x (ctrl + rotate) + 256 x softmax = 65536 = 512 threads x 128 registers at launch.
+// Register split after setmaxnreg (control warps / softmax warps / rotation warps).  The total,
+// 128 x (ctrl + rotate) + 256 x softmax, must not exceed the 512 x 128 registers the CTA is launched
+// with, or the softmax warps' setmaxnreg.inc would wait forever.
 template <int D>
 struct Regs {
-  static constexpr uint32_t kCtrl = 64;
-  static constexpr uint32_t kSoftmax = D == 128 ? 168 : 176;
-  static constexpr uint32_t kRotate = D == 128 ? 112 : 96;
-  static_assert(128 * (kCtrl + kRotate) + 256 * kSoftmax == kThreads * 128, "register split");
+  static constexpr uint32_t kCtrl = 80;
+  static constexpr uint32_t kSoftmax = 168;
+  static constexpr uint32_t kRotate = 88;
+  static_assert(128 * (kCtrl + kRotate) + 256 * kSoftmax <= kThreads * 128, "register split");
 };
 
 template <int D>
@@ -82,7 +86,7 @@ struct Cfg {
 };
 
 struct __align__(8) Ctrl {
-  uint64_t q_full, q_ready;
+  uint64_t q_full, q_ready, q_empty;
   uint64_t k_full[KST], k_ready[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[2], p_full[2], o_full[2];
@@ -172,10 +176,12 @@ struct RotGeom {
   static constexpr int RS = 128 / PASSES;
 };
 
-// Rotate, in place, the thread's rows of one 128-row tile held in shared memory at `tile`.  cs holds
-// the cos/sin of the thread's first row; step is the exact rotation by RS rows.
+// Rotate, in place, the thread's rows of one 128-row tile held in shared memory at `tile`.  On entry
+// cs holds the cos/sin of the thread's first row r0; it is advanced by `step` (the exact rotation of
+// RS rows) after every pass, so on return it holds the values of row r0 + 128 -- the thread's first
+// row of the next tile.
 template <int D, bool BF16>
-__device__ __forceinline__ void rotate_tile(uint32_t tile, int r0, int ck, RopeCS8 cs, const RopeCS8& step) {
+__device__ __forceinline__ void rotate_tile(uint32_t tile, int r0, int ck, RopeCS8& cs, const RopeCS8& step) {
   constexpr int PASSES = RotGeom<D>::PASSES, RS = RotGeom<D>::RS;
 #pragma unroll
   for (int pass = 0; pass < PASSES; pass += 2) {
@@ -187,13 +193,48 @@ __device__ __forceinline__ void rotate_tile(uint32_t tile, int r0, int ck, RopeC
     rope_rotate_chunk_cs8<BF16>(x0, y0, cs);
     rope_cs8_advance(cs, step);
     rope_rotate_chunk_cs8<BF16>(x1, y1, cs);
-    if (pass + 2 < PASSES) rope_cs8_advance(cs, step);
+    rope_cs8_advance(cs, step);
     ptx::sts128(tile + xo0, x0);
     ptx::sts128(tile + yo0, y0);
     ptx::sts128(tile + xo1, x1);
     ptx::sts128(tile + yo1, y1);
   }
 }
+
+// ---- persistent schedule -------------------------------------------------------------------
+// Work unit = (b, h, 256-row query block t), numbered longest-first (t descending).  CTA c of G
+// processes units c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the longest-first order), which evens
+// out the causal work across CTAs without a shared counter.  Every role walks the same sequence.
+struct Unit {
+  int b, h, hk, q_row0, n0, n1, n_kt;
+  bool active1;
+};
+
+__device__ __forceinline__ int unit_of_round(int round, int c, int G) {
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
+  Unit x;
+  const int bh_count = p.B * p.Hq;
+  const int t = p.n_qblocks - 1 - u / bh_count;
+  const int bh = u - (u / bh_count) * bh_count;
+  x.b = bh / p.Hq;
+  x.h = bh - x.b * p.Hq;
+  x.hk = x.h / (p.Hq / p.Hkv);
+  x.q_row0 = t * 2 * BM;
+  x.active1 = x.q_row0 + BM < p.N;
+  x.n0 = 2 * t + 1;                  // key tiles for q0 (tile 2t is its diagonal)
+  x.n1 = x.active1 ? 2 * t + 2 : 0;  // key tiles for q1
+  x.n_kt = x.active1 ? x.n1 : x.n0;
+  return x;
+}
+
+#define FOR_EACH_UNIT(U)                                                         \
+  for (int rnd_ = 0; rnd_ * (int)gridDim.x < p.total_units; ++rnd_)             \
+    if (const int u_ = unit_of_round(rnd_, blockIdx.x, gridDim.x); u_ >= p.total_units) \
+      break;                                                                     \
+    else if (const Unit U = decode_unit(u_, p); true)
 
 template <int D, bool ROTATE, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -215,23 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // ---- work unit: (b, h, 256-row query block t); blocks are numbered longest-first ----------
-  const int bh_count = p.B * p.Hq;
-  const int unit = blockIdx.x;
-  const int t = p.n_qblocks - 1 - unit / bh_count;
-  const int bh = unit - (unit / bh_count) * bh_count;
-  const int b = bh / p.Hq;
-  const int h = bh - b * p.Hq;
-  const int hk = h / (p.Hq / p.Hkv);
-  const int q_row0 = t * 2 * BM;
-  const bool active1 = q_row0 + BM < p.N;
-  const int n0 = 2 * t + 1;                // key tiles for q0 (tile 2t is its diagonal)
-  const int n1 = active1 ? 2 * t + 2 : 0;  // key tiles for q1
-  const int n_kt = active1 ? n1 : n0;
-
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_addr(ctl.q_full), 1);
-    ptx::mbar_init(bar_addr(ctl.q_ready), 2 * 128);
+    ptx::mbar_init(bar_addr(ctl.q_ready), 128);
+    ptx::mbar_init(bar_addr(ctl.q_empty), 1);
     for (int s = 0; s < KST; ++s) {
       ptx::mbar_init(bar_addr(ctl.k_full[s]), 1);
       ptx::mbar_init(bar_addr(ctl.k_ready[s]), 128);
@@ -273,41 +301,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::setmaxnreg_dec<Regs<D>::kCtrl>();
     if (!skip && warp == 0 && lane == 0) {
       // ================================ TMA producer ==========================================
+      // Per unit: K_0/V_0 first (their ring stages free up early), then Q once the previous
+      // unit's QK^T products are done with the Q buffer, then the remaining K/V tiles.
       ptx::tma_prefetch_desc(&tmQ);
       ptx::tma_prefetch_desc(&tmK);
       ptx::tma_prefetch_desc(&tmV);
-      const int nq = active1 ? 2 : 1;
-      ptx::mbar_arrive_expect_tx(bar_addr(ctl.q_full), (uint32_t)nq * C::TILE);
-      for (int i = 0; i < nq; ++i)
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          ptx::tma_load_4d(sQ + i * C::TILE + bx * kBoxBytes, &tmQ, bar_addr(ctl.q_full), bx * 64, h,
-                           q_row0 + i * BM, b);
-      int k_issued = 0, v_issued = 0;
+      int gk = 0, gv = 0, uc = 0;
       bool ok = true;
-      for (int i = 0; i < n_kt && ok; ++i) {
-        const int ks = i % KST, kph = (i / KST) & 1;
-        if (!(ok = wait_bar(bar_addr(ctl.k_empty[ks]), kph ^ 1, ctl, tmo))) break;
-        ptx::mbar_arrive_expect_tx(bar_addr(ctl.k_full[ks]), C::TILE);
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          ptx::tma_load_4d(sK + ks * C::TILE + bx * kBoxBytes, &tmK, bar_addr(ctl.k_full[ks]), bx * 64, hk, i * BN,
-                           b);
-        ++k_issued;
-        const int vs = i % VST, vph = (i / VST) & 1;
-        if (!(ok = wait_bar(bar_addr(ctl.v_empty[vs]), vph ^ 1, ctl, tmo))) break;
-        ptx::mbar_arrive_expect_tx(bar_addr(ctl.v_full[vs]), C::TILE);
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          ptx::tma_load_4d(sV + vs * C::TILE + bx * kBoxBytes, &tmV, bar_addr(ctl.v_full[vs]), bx * 64, hk, i * BN,
-                           b);
-        ++v_issued;
+      FOR_EACH_UNIT(U) {
+        auto load_kv = [&](int i) -> bool {
+          const int ks = gk % KST, kph = (gk / KST) & 1;
+          if (!wait_bar(bar_addr(ctl.k_empty[ks]), kph ^ 1, ctl, tmo)) return false;
+          ptx::mbar_arrive_expect_tx(bar_addr(ctl.k_full[ks]), C::TILE);
+          for (int bx = 0; bx < C::NBOX; ++bx)
+            ptx::tma_load_4d(sK + ks * C::TILE + bx * kBoxBytes, &tmK, bar_addr(ctl.k_full[ks]), bx * 64, U.hk,
+                             i * BN, U.b);
+          ++gk;
+          const int vs = gv % VST, vph = (gv / VST) & 1;
+          if (!wait_bar(bar_addr(ctl.v_empty[vs]), vph ^ 1, ctl, tmo)) return false;
+          ptx::mbar_arrive_expect_tx(bar_addr(ctl.v_full[vs]), C::TILE);
+          for (int bx = 0; bx < C::NBOX; ++bx)
+            ptx::tma_load_4d(sV + vs * C::TILE + bx * kBoxBytes, &tmV, bar_addr(ctl.v_full[vs]), bx * 64, U.hk,
+                             i * BN, U.b);
+          ++gv;
+          return true;
+        };
+        if (!(ok = load_kv(0))) break;
+        if (uc > 0 && !(ok = wait_bar(bar_addr(ctl.q_empty), (uc - 1) & 1, ctl, tmo))) break;
+        const int nq = U.active1 ? 2 : 1;
+        ptx::mbar_arrive_expect_tx(bar_addr(ctl.q_full), (uint32_t)nq * C::TILE);
+        for (int i = 0; i < nq; ++i)
+          for (int bx = 0; bx < C::NBOX; ++bx)
+            ptx::tma_load_4d(sQ + i * C::TILE + bx * kBoxBytes, &tmQ, bar_addr(ctl.q_full), bx * 64, U.h,
+                             U.q_row0 + i * BM, U.b);
+        ++uc;
+        for (int i = 1; i < U.n_kt && ok; ++i) ok = load_kv(i);
+        if (!ok) break;
       }
       if (!ok) {
         // Let every copy already issued land before shared memory is released.
         const unsigned long long drain = 100000000ull;
-        drain_bar(bar_addr(ctl.q_full), 0, drain);
+        if (uc > 0) drain_bar(bar_addr(ctl.q_full), (uc - 1) & 1, drain);
         for (int s = 0; s < KST; ++s)
-          if (k_issued > s) drain_bar(bar_addr(ctl.k_full[s]), ((k_issued - 1 - s) / KST) & 1, drain);
+          if (gk > s) drain_bar(bar_addr(ctl.k_full[s]), ((gk - 1 - s) / KST) & 1, drain);
         for (int s = 0; s < VST; ++s)
-          if (v_issued > s) drain_bar(bar_addr(ctl.v_full[s]), ((v_issued - 1 - s) / VST) & 1, drain);
+          if (gv > s) drain_bar(bar_addr(ctl.v_full[s]), ((gv - 1 - s) / VST) & 1, drain);
       }
     } else if (!skip && warp == 1 && lane == 0) {
       // ================================ MMA issuer ============================================
@@ -331,53 +369,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BN / 16; ++kk)
           ptx::mma_ts(dst, asrc + kk * 8, dv + (uint64_t)(kk * (2048 >> 4)), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_bar(bar_addr(ROTATE ? ctl.q_ready : ctl.q_full), 0, ctl, tmo);
-      ptx::tc_fence_after();
-      for (int i = 0; i < n_kt && ok; ++i) {
-        const int ks = i % KST, kph = (i / KST) & 1;
-        if (!(ok = wait_bar(bar_addr(ROTATE ? ctl.k_ready[ks] : ctl.k_full[ks]), kph, ctl, tmo))) break;
+      // Order per key tile i: S0_i, PV1 of the previous q1 step (possibly the previous unit's last),
+      // S1_i, PV0_i.  The q1 product of a tile is issued one tile later, so both softmax warpgroups
+      // overlap the other tile's products, also across unit boundaries.
+      int gk = 0, gv = 0, gp0 = 0, gp1 = 0, uc = 0;
+      bool ok = true;
+      bool pend = false, pend_vwait = false, pend_first = false, pend_last = false;
+      int pend_vs = 0, pend_vph = 0;
+      auto flush_pv1 = [&]() -> bool {
+        if (!wait_bar(bar_addr(ctl.p_full[1]), gp1 & 1, ctl, tmo)) return false;
+        if (pend_vwait && !wait_bar(bar_addr(ctl.v_full[pend_vs]), pend_vph, ctl, tmo)) return false;
         ptx::tc_fence_after();
-        const uint32_t kbase = sK + ks * C::TILE;
-        if (i < n0) {
-          issue_S(0, kbase);
-          ptx::mma_commit(bar_addr(ctl.s_full[0]));
-        }
-        if (i >= 1 && i - 1 < n1) {  // P1 of the previous key tile
-          const int j = i - 1, vs = j % VST, vph = (j / VST) & 1;
-          if (!(ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo))) break;
-          // V_j was already seen complete by PV0_j unless tile j is q1's alone
-          if (j >= n0 && !(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
+        issue_PV(1, sV + pend_vs * C::TILE, pend_first);
+        ptx::mma_commit(bar_addr(ctl.v_empty[pend_vs]));
+        if (pend_last) ptx::mma_commit(bar_addr(ctl.o_full[1]));
+        ++gp1;
+        pend = false;
+        return true;
+      };
+      FOR_EACH_UNIT(U) {
+        if (!(ok = wait_bar(bar_addr(ROTATE ? ctl.q_ready : ctl.q_full), uc & 1, ctl, tmo))) break;
+        ++uc;
+        ptx::tc_fence_after();
+        for (int i = 0; i < U.n_kt && ok; ++i) {
+          const int ks = gk % KST, kph = (gk / KST) & 1;
+          if (!(ok = wait_bar(bar_addr(ROTATE ? ctl.k_ready[ks] : ctl.k_full[ks]), kph, ctl, tmo))) break;
           ptx::tc_fence_after();
-          issue_PV(1, sV + vs * C::TILE, j == 0);
-          ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
-          if (j == n1 - 1) ptx::mma_commit(bar_addr(ctl.o_full[1]));
+          const uint32_t kbase = sK + ks * C::TILE;
+          const int vs = gv % VST, vph = (gv / VST) & 1;
+          if (i < U.n0) {
+            issue_S(0, kbase);
+            ptx::mma_commit(bar_addr(ctl.s_full[0]));
+          }
+          if (pend && !(ok = flush_pv1())) break;
+          if (i < U.n1) {
+            issue_S(1, kbase);
+            ptx::mma_commit(bar_addr(ctl.s_full[1]));
+          }
+          if (i == U.n_kt - 1) ptx::mma_commit(bar_addr(ctl.q_empty));  // all of this unit's QK^T done
+          ptx::mma_commit(bar_addr(ctl.k_empty[ks]));
+          ++gk;
+          if (i < U.n0) {
+            if (!(ok = wait_bar(bar_addr(ctl.p_full[0]), gp0 & 1, ctl, tmo))) break;
+            if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
+            ptx::tc_fence_after();
+            issue_PV(0, sV + vs * C::TILE, i == 0);
+            if (U.n1 == 0) ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
+            if (i == U.n0 - 1) ptx::mma_commit(bar_addr(ctl.o_full[0]));
+            ++gp0;
+          }
+          if (i < U.n1) {
+            pend = true;
+            pend_vs = vs;
+            pend_vph = vph;
+            pend_vwait = i >= U.n0;  // V_i not yet seen complete when no PV0 used it
+            pend_first = i == 0;
+            pend_last = i == U.n1 - 1;
+          }
+          ++gv;
         }
-        if (i < n1) {
-          issue_S(1, kbase);
-          ptx::mma_commit(bar_addr(ctl.s_full[1]));
-        }
-        ptx::mma_commit(bar_addr(ctl.k_empty[ks]));
-        if (i < n0) {
-          const int vs = i % VST, vph = (i / VST) & 1;
-          if (!(ok = wait_bar(bar_addr(ctl.p_full[0]), i & 1, ctl, tmo))) break;
-          if (!(ok = wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo))) break;
-          ptx::tc_fence_after();
-          issue_PV(0, sV + vs * C::TILE, i == 0);
-          if (n1 == 0) ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
-          if (i == n0 - 1) ptx::mma_commit(bar_addr(ctl.o_full[0]));
-        }
+        if (!ok) break;
       }
-      if (ok && n1 > 0) {  // P1 of the last key tile
-        const int j = n1 - 1, vs = j % VST, vph = (j / VST) & 1;
-        ok = wait_bar(bar_addr(ctl.p_full[1]), j & 1, ctl, tmo) &&
-             (j < n0 || wait_bar(bar_addr(ctl.v_full[vs]), vph, ctl, tmo));
-        if (ok) {
-          ptx::tc_fence_after();
-          issue_PV(1, sV + vs * C::TILE, j == 0);
-          ptx::mma_commit(bar_addr(ctl.v_empty[vs]));
-          ptx::mma_commit(bar_addr(ctl.o_full[1]));
-        }
-      }
+      if (ok && pend) ok = flush_pv1();
       // Every MMA issued must finish before tensor memory is freed.
       ptx::mma_commit(bar_addr(ctl.mma_done));
       drain_bar(bar_addr(ctl.mma_done), 0, 100000000ull);
@@ -385,141 +438,131 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     ptx::setmaxnreg_inc<Regs<D>::kSoftmax>();
     if (!skip) {
-      bool ok = true;
-      if constexpr (ROTATE) {
-        // Each softmax warpgroup rotates its own query tile once (positions q_row0 + 128 wi + r).
-        ok = wait_bar_warp(bar_addr(ctl.q_full), 0, ctl, tmo);
-        if (ok) {
-          const int wq = (warp - 4) / 4;
-          if (wq == 0 || active1) {
-            int ck, r0;
-            rot_mapping<D>(threadIdx.x - 128 - 128 * wq, ck, r0);
-            RopeCS8 cs, step;
-            rope_cs8_exact((uint32_t)(q_row0 + wq * BM + r0), sfreq, sfreq + 64, ck * 8, cs);
-            rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
-            rotate_tile<D, BF16>(sQ + wq * C::TILE, r0, ck, cs, step);
-          }
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(bar_addr(ctl.q_ready));
-        }
-      }
       // ================================ softmax + epilogue ====================================
       const int wi = (warp - 4) / 4;  // which query tile
-      const int qt = 2 * t + wi;
-      const int n_steps = wi == 0 ? n0 : n1;
       const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
       const uint32_t tS = tmem + lane_off + wi * BN;
       const uint32_t tO = tmem + lane_off + C::COL_O + wi * D;
       const float sl2 = p.scale_log2;
-      float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < n_steps && ok; ++j) {
-        if (!(ok = wait_bar_warp(bar_addr(ctl.s_full[wi]), j & 1, ctl, tmo))) break;
-        ptx::tc_fence_after();
-        uint32_t sv[4][32];
+      int gs = 0, uo = 0;
+      bool ok = true;
+      FOR_EACH_UNIT(U) {
+        const int n_steps = wi == 0 ? U.n0 : U.n1;
+        if (n_steps == 0) continue;
+        const int qt = U.q_row0 / BM + wi;
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < n_steps && ok; ++j) {
+          if (!(ok = wait_bar_warp(bar_addr(ctl.s_full[wi]), gs & 1, ctl, tmo))) break;
+          ++gs;
+          ptx::tc_fence_after();
+          uint32_t sv[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sv[c]);
-        ptx::tmem_wait_ld();
-        if (j == n_steps - 1) {  // diagonal tile: key column c is visible to row r iff c <= r
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sv[c]);
+          ptx::tmem_wait_ld();
+          if (j == n_steps - 1) {  // diagonal tile: key column c is visible to row r iff c <= r
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
-        }
-        // Row max: three-input max tree, eight independent chains.
-        float acc[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          acc[k] = ptx::fmax3(__uint_as_float(sv[0][k]), __uint_as_float(sv[0][k + 8]), __uint_as_float(sv[0][k + 16]));
-#pragma unroll
-        for (int base = 24; base < 120; base += 16)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int i0 = base + k, i1 = base + 8 + k;
-            acc[k] = ptx::fmax3(acc[k], __uint_as_float(sv[i0 / 32][i0 % 32]), __uint_as_float(sv[i1 / 32][i1 % 32]));
+              for (int e = 0; e < 32; ++e)
+                if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
           }
+          // Row max: three-input max tree, eight independent chains.
+          float acc[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = fmaxf(acc[k], __uint_as_float(sv[3][24 + k]));
-        const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
-                                    fmaxf(acc[6], acc[7]));
-        const float m_new = fmaxf(m_run, mx * sl2);
-        // Rescale only when some row's max grew past the threshold (warp-uniform decision, since
-        // TMEM loads and stores are warp-collective); otherwise keep the stale max.
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          m_run = m_new;
-        } else {
-          const bool need = m_new > m_run + kRescaleThreshold;
-          rescale = __any_sync(0xFFFFFFFFu, need);
-          if (need) {
-            alpha = ptx::ex2_approx(m_run - m_new);
-            l_run *= alpha;
-            m_run = m_new;
-          }
-        }
-        // P = 2^(s * log2(e)/sqrt(d) - m) on fp32 pairs; four independent partial row sums.
-        const uint64_t SL2 = ptx::f2_pack(sl2, sl2), NM = ptx::f2_pack(-m_run, -m_run);
-        uint64_t part[4];
+          for (int k = 0; k < 8; ++k)
+            acc[k] = ptx::fmax3(__uint_as_float(sv[0][k]), __uint_as_float(sv[0][k + 8]),
+                                __uint_as_float(sv[0][k + 16]));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) part[k] = ptx::f2_pack(0.f, 0.f);
+          for (int base = 24; base < 120; base += 16)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16)
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])),
-                                            SL2, NM);
-            float p0, p1;
-            if ((kPolyChunkMask >> c) & 1u) {
-              exp2_poly_pair(x2, p0, p1);
-            } else {
-              float x0, x1;
-              ptx::f2_unpack(x2, x0, x1);
-              p0 = ptx::ex2_approx(x0);
-              p1 = ptx::ex2_approx(x1);
+            for (int k = 0; k < 8; ++k) {
+              const int i0 = base + k, i1 = base + 8 + k;
+              acc[k] = ptx::fmax3(acc[k], __uint_as_float(sv[i0 / 32][i0 % 32]), __uint_as_float(sv[i1 / 32][i1 % 32]));
             }
-            part[e & 3] = ptx::f2_add(part[e & 3], ptx::f2_pack(p0, p1));
-            pk[e] = Pack<BF16>::pack(p0, p1);
-          }
-          ptx::tmem_st16(tS + 16 * c, pk);
-        }
-        float sum;
-        {
-          float a, bb;
-          ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), a, bb);
-          sum = a + bb;
-        }
-        if (rescale) {  // O += P V for this tile is issued only after p_full, so O is stable here
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + 32 * c, o);
-            ptx::tmem_wait_ld();
-            const uint64_t A2 = ptx::f2_pack(alpha, alpha);
+          for (int k = 0; k < 8; ++k) acc[k] = fmaxf(acc[k], __uint_as_float(sv[3][24 + k]));
+          const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
+                                      fmaxf(acc[6], acc[7]));
+          const float m_new = fmaxf(m_run, mx * sl2);
+          // Rescale only when some row's max grew past the threshold (warp-uniform decision, since
+          // TMEM loads and stores are warp-collective); otherwise keep the stale max.
+          float alpha = 1.f;
+          bool rescale = false;
+          if (j == 0) {
+            m_run = m_new;
+          } else {
+            const bool need = m_new > m_run + kRescaleThreshold;
+            rescale = __any_sync(0xFFFFFFFFu, need);
+            if (need) {
+              alpha = ptx::ex2_approx(m_run - m_new);
+              l_run *= alpha;
+              m_run = m_new;
+            }
+          }
+          // P = 2^(s * log2(e)/sqrt(d) - m) on fp32 pairs; four independent partial row sums.
+          const uint64_t SL2 = ptx::f2_pack(sl2, sl2), NM = ptx::f2_pack(-m_run, -m_run);
+          uint64_t part[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) part[k] = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16)
+            uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const uint64_t v = ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), A2);
-              float a, bb;
-              ptx::f2_unpack(v, a, bb);
-              o[2 * e] = __float_as_uint(a);
-              o[2 * e + 1] = __float_as_uint(bb);
+              const uint64_t x2 = ptx::f2_fma(
+                  ptx::f2_pack(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), SL2, NM);
+              float p0, p1;
+              if ((kPolyChunkMask >> c) & 1u) {
+                exp2_poly_pair(x2, p0, p1);
+              } else {
+                float x0, x1;
+                ptx::f2_unpack(x2, x0, x1);
+                p0 = ptx::ex2_approx(x0);
+                p1 = ptx::ex2_approx(x1);
+              }
+              part[e & 3] = ptx::f2_add(part[e & 3], ptx::f2_pack(p0, p1));
+              pk[e] = Pack<BF16>::pack(p0, p1);
             }
-            ptx::tmem_st32(tO + 32 * c, o);
+            ptx::tmem_st16(tS + 16 * c, pk);
           }
+          float sum;
+          {
+            float a, bb;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), a, bb);
+            sum = a + bb;
+          }
+          if (rescale) {  // O += P V for this tile is issued only after p_full, so O is stable here
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tO + 32 * c, o);
+              ptx::tmem_wait_ld();
+              const uint64_t A2 = ptx::f2_pack(alpha, alpha);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const uint64_t v =
+                    ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), A2);
+                float a, bb;
+                ptx::f2_unpack(v, a, bb);
+                o[2 * e] = __float_as_uint(a);
+                o[2 * e + 1] = __float_as_uint(bb);
+              }
+              ptx::tmem_st32(tO + 32 * c, o);
+            }
+          }
+          l_run += sum;
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_addr(ctl.p_full[wi]));
         }
-        l_run += sum;
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(ctl.p_full[wi]));
-      }
-      if (ok && n_steps > 0) ok = wait_bar_warp(bar_addr(ctl.o_full[wi]), 0, ctl, tmo);
-      if (ok && n_steps > 0) {
+        if (!ok) break;
+        if (!(ok = wait_bar_warp(bar_addr(ctl.o_full[wi]), uo & 1, ctl, tmo))) break;
+        ++uo;
         ptx::tc_fence_after();
         const int row = qt * BM + r;
         const float inv_l = 1.f / l_run;
-        T* orow = reinterpret_cast<T*>(p.out) + (((size_t)b * p.N + row) * p.Hq + h) * D;
+        T* orow = reinterpret_cast<T*>(p.out) + (((size_t)U.b * p.N + row) * p.Hq + U.h) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -536,31 +579,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (row < p.N && p.lse != nullptr)
-          p.lse[((size_t)b * p.Hq + h) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
+          p.lse[((size_t)U.b * p.Hq + U.h) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
+        // The O reads above completed (wait::ld) before this warpgroup's next p_full arrive, which
+        // is what lets the next unit's first O += P V overwrite O.
       }
     }
   } else {
     ptx::setmaxnreg_dec<Regs<D>::kRotate>();
     if constexpr (ROTATE) {
       if (!skip) {
-        // ============================== K-tile rotation =========================================
-        // cos/sin are carried along the thread's rows by angle addition: exact values at row r0 of
-        // key tile 0, advanced by the exact rotation of RS rows between passes and of 128 rows
-        // between tiles (one fp32 rounding per step: relative drift < 3e-5 after 32768 positions).
+        // ============================== Q and K tile rotation ===================================
+        // cos/sin are carried along the thread's rows by angle addition with the exact rotation of
+        // RS rows: exact at the first row of a query tile, and for the keys exact at the first
+        // row of every 16th key tile (one fp32 rounding per step, at most 128 steps between exact
+        // values: relative drift < 1e-5).  Per unit: K_0, then the query tiles (they land after
+        // the previous unit's last QK^T), then K_1, K_2, ...
+        constexpr int kReseed = 16;
         int ck, r0;
         rot_mapping<D>(threadIdx.x - 384, ck, r0);
-        RopeCS8 tile_cs, step, step_tile;
-        rope_cs8_exact((uint32_t)r0, sfreq, sfreq + 64, ck * 8, tile_cs);
+        RopeCS8 step;
         rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
-        rope_cs8_exact((uint32_t)BN, sfreq, sfreq + 64, ck * 8, step_tile);
+        int gk = 0, uc = 0;
         bool ok = true;
-        for (int i = 0; i < n_kt && ok; ++i) {
-          const int ks = i % KST, kph = (i / KST) & 1;
-          if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
-          rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, tile_cs, step);
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
-          rope_cs8_advance(tile_cs, step_tile);
+        FOR_EACH_UNIT(U) {
+          RopeCS8 kcs;
+          for (int i = 0; i < U.n_kt && ok; ++i) {
+            if (i % kReseed == 0) rope_cs8_exact((uint32_t)(i * BN + r0), sfreq, sfreq + 64, ck * 8, kcs);
+            const int ks = gk % KST, kph = (gk / KST) & 1;
+            if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
+            ++gk;
+            rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
+            if (i == 0) {
+              if (!(ok = wait_bar_warp(bar_addr(ctl.q_full), uc & 1, ctl, tmo))) break;
+              ++uc;
+              for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
+                RopeCS8 qcs;
+                rope_cs8_exact((uint32_t)(U.q_row0 + tq * BM + r0), sfreq, sfreq + 64, ck * 8, qcs);
+                rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
+              }
+              ptx::fence_proxy_async_smem();
+              ptx::mbar_arrive(bar_addr(ctl.q_ready));
+            }
+          }
+          if (!ok) break;
         }
       }
     }
@@ -602,6 +665,7 @@ cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t s
   auto kernel = attn_fwd_kernel<D, ROTATE, BF16>;
   constexpr int kMaxDevices = 64;
   static int configured[kMaxDevices] = {0};
+  static int sm_count[kMaxDevices] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -618,9 +682,16 @@ cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t s
       if (why) *why = "attention kernel was not compiled with 128 registers per thread (setmaxnreg split)";
       return cudaErrorInvalidConfiguration;
     }
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = sms;
     configured[dev] = 1;
   }
-  kernel<<<dim3((unsigned)p.total_units), dim3(kThreads), Cfg<D>::SMEM, stream>>>(maps.q, maps.k, maps.v, p);
+  // Persistent: one CTA per SM (shared memory and registers admit only one), each walking its share
+  // of the work units.
+  const int grid = p.total_units < sm_count[dev] ? p.total_units : sm_count[dev];
+  kernel<<<dim3((unsigned)grid), dim3(kThreads), Cfg<D>::SMEM, stream>>>(maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
 
