@@ -301,6 +301,17 @@ def fwd_fn(w, q, k, v, out, lse, ws, mode, stream):
                                            stream=stream)
 
 
+def rope_pass_fn(w, stream):
+    """The RoPE pass of the pre-rotate path as one launch over Q and K: attnfuse_rope_apply on a
+    [B, N, Hq + Hkv, d] tensor moves the same bytes as the pipeline's combined Q/K launch."""
+    import torch
+    from attention_rope_causal_gb300 import binding
+    g = torch.Generator(device="cpu").manual_seed(w.seed)
+    x = torch.randn((w.B, w.N, w.Hq + w.Hkv, w.d), generator=g).to(w.torch_dtype).cuda()
+    y = torch.empty_like(x)
+    return lambda: binding.rope_apply(x, w.rope_base, out=y, stream=stream)
+
+
 def measure_point(w, steps, warmup):
     """Median-of-steps times (ms) for fused, pre-rotate pipeline and the RoPE pass alone."""
     import torch
@@ -308,17 +319,12 @@ def measure_point(w, steps, warmup):
     stream = torch.cuda.current_stream()
     q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    qr = torch.empty_like(q)
-    kr = torch.empty_like(k)
     res = {}
     for mode in ("fused", "prerotate"):
         f = fwd_fn(w, q, k, v, out, lse, ws[mode], mode, stream)
         time_steps(f, warmup, flush, stream)
         res[mode] = statistics.median(time_steps(f, steps, flush, stream))
-
-    def rope_pass():
-        binding.rope_apply(q, w.rope_base, out=qr, stream=stream)
-        binding.rope_apply(k, w.rope_base, out=kr, stream=stream)
+    rope_pass = rope_pass_fn(w, stream)
     time_steps(rope_pass, warmup, flush, stream)
     res["rope"] = statistics.median(time_steps(rope_pass, steps, flush, stream))
     if binding.device_status() != 0:
@@ -364,11 +370,7 @@ def run_only(args):
     q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     if args.only == "rope":
-        qr, kr = torch.empty_like(q), torch.empty_like(k)
-
-        def f():
-            binding.rope_apply(q, w.rope_base, out=qr, stream=stream)
-            binding.rope_apply(k, w.rope_base, out=kr, stream=stream)
+        f = rope_pass_fn(w, stream)
     else:
         f = fwd_fn(w, q, k, v, out, lse, ws[args.only], args.only, stream)
     ms = time_steps(f, args.warmup + args.steps, flush, stream)[args.warmup:]
@@ -432,11 +434,7 @@ def run_ours(args):
     pre = fwd_fn(w, q, k, v, out, lse, ws["prerotate"], "prerotate", stream)
     time_steps(pre, args.warmup, flush, stream)
     pre_ms = statistics.median(time_steps(pre, max(20, args.steps // 10), flush, stream))
-    qr, kr = torch.empty_like(q), torch.empty_like(k)
-
-    def rope_pass():
-        binding.rope_apply(q, w.rope_base, out=qr, stream=stream)
-        binding.rope_apply(k, w.rope_base, out=kr, stream=stream)
+    rope_pass = rope_pass_fn(w, stream)
     time_steps(rope_pass, args.warmup, flush, stream)
     rope_ms = statistics.median(time_steps(rope_pass, max(20, args.steps // 10), flush, stream))
     rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
