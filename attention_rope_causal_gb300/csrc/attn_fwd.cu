@@ -24,8 +24,10 @@
 // is issued after the next unit's first S0, and the next unit's Q is loaded as soon as the last
 // QK^T of the current unit is done with the Q buffer.  Fully masked key tiles are never
 // loaded (tile i runs for query tile qt only while i <= qt); the diagonal tile is masked per
-// element.  Softmax rescales O only when a row max grows by more than 2^8, which keeps the result
-// exact (the stale max is used consistently for P, l and lse).
+// element.  The softmax takes a row's max from its first key tile only and computes every later
+// tile's P against that running max, without a max pass; only when a row of P sums past 2^15 (a
+// score outgrew the max by ~15 in log2 units) is that tile redone with its own max and O and l
+// rescaled.  The result stays exact: the max used is applied consistently to P, l and lse.
 //
 // Every barrier wait gives up after AttnParams::timeout_ns: the CTA then records bit 0 in the
 // device status word, stops its loops, lets its copies and MMAs land, frees tensor memory and
@@ -54,7 +56,10 @@ constexpr int VST = 2;   // V ring depth
 constexpr uint32_t kBoxBytes = 128 * 128;  // 128 rows x 64 16-bit columns, 128-byte swizzled
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// A tile's P = 2^(s - m) is computed with the running max m of the earlier tiles; only when some row
+// of P sums past this bound (some score exceeded m by more than ~15 in log2 units, so P could leave
+// the range of the 16-bit operand type) is the tile redone with its own max.
+constexpr float kSumCap = 32768.0f;
 
 // Which 32-column chunks of a score row take their exponentials from the FMA-pipe polynomial
 // (exp2_poly.cuh) instead of the MUFU unit (bit c set = chunk c).
@@ -70,6 +75,116 @@ struct Regs {
   static constexpr uint32_t kRotate = 88;
   static_assert(128 * (kCtrl + kRotate) + 256 * kSoftmax <= kThreads * 128, "register split");
 };
+
+// Row max of 128 scores held as fp32 bit patterns: three-input max tree, eight independent chains.
+__device__ __forceinline__ float row_max128(const uint32_t (&sv)[4][32]) {
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    acc[k] = ptx::fmax3(__uint_as_float(sv[0][k]), __uint_as_float(sv[0][k + 8]), __uint_as_float(sv[0][k + 16]));
+#pragma unroll
+  for (int base = 24; base < 120; base += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i0 = base + k, i1 = base + 8 + k;
+      acc[k] = ptx::fmax3(acc[k], __uint_as_float(sv[i0 / 32][i0 % 32]), __uint_as_float(sv[i1 / 32][i1 % 32]));
+    }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = fmaxf(acc[k], __uint_as_float(sv[3][24 + k]));
+  return ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+}
+
+// P = 2^(s * sl2 - m) for one row of 128 scores on fp32 pairs, packed to the operand type into
+// pk (64 words); returns the row sum (four independent partials).
+template <bool BF16>
+__device__ __forceinline__ float softmax_p(const uint32_t (&sv)[4][32], float sl2, float m, uint32_t (&pk)[64]) {
+  const uint64_t SL2 = ptx::f2_pack(sl2, sl2), NM = ptx::f2_pack(-m, -m);
+  uint64_t part[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) part[k] = ptx::f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint64_t x2 =
+          ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), SL2, NM);
+      float p0, p1;
+      if ((kPolyChunkMask >> c) & 1u) {
+        exp2_poly_pair(x2, p0, p1);
+      } else {
+        float x0, x1;
+        ptx::f2_unpack(x2, x0, x1);
+        p0 = ptx::ex2_approx(x0);
+        p1 = ptx::ex2_approx(x1);
+      }
+      part[e & 3] = ptx::f2_add(part[e & 3], ptx::f2_pack(p0, p1));
+      pk[16 * c + e] = Pack<BF16>::pack(p0, p1);
+    }
+  }
+  float a, b;
+  ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), a, b);
+  return a + b;
+}
+
+// Rare path of the softmax, taken by a whole warp when some row's P summed past kSumCap (its scores
+// outgrew the running max): rows with `need` take the tile's own max, rescale l and O, and P is
+// recomputed from S (still intact in tensor memory) and stored.  Returns the row sum and the updated
+// max and denominator.  Kept out of line so that the common path's register allocation does not
+// carry it.
+struct RowState {
+  float sum, m, l;
+};
+template <int D, bool BF16>
+__device__ __noinline__ RowState softmax_redo(uint32_t tS, uint32_t tO, int r, bool diag, bool need, float sl2,
+                                              float m_run, float l_run) {
+  float mx = -INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    uint32_t t[16];
+    ptx::tmem_ld16(tS + 16 * c, t);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (!(diag && 16 * c + e > r)) mx = fmaxf(mx, __uint_as_float(t[e]));
+  }
+  float alpha = 1.f;
+  if (need) {
+    const float m_new = fmaxf(m_run, mx * sl2);
+    alpha = ptx::ex2_approx(m_run - m_new);
+    l_run *= alpha;
+    m_run = m_new;
+  }
+  // The previous O += P V finished before s_full; this tile's waits for p_full.
+  for (int c = 0; c < D / 16; ++c) {
+    uint32_t o[16];
+    ptx::tmem_ld16(tO + 16 * c, o);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+    ptx::tmem_st16(tO + 16 * c, o);
+  }
+  const float nm = -m_run;
+  float sum = 0.f;
+  for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16) (columns
+    uint32_t pk[16];              // already read: the loads run ahead of the stores)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t t[16];
+      ptx::tmem_ld16(tS + 32 * c + 16 * h, t);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int col = 32 * c + 16 * h + 2 * e;
+        const float x0 = (diag && col > r) ? -INFINITY : fmaf(__uint_as_float(t[2 * e]), sl2, nm);
+        const float x1 = (diag && col + 1 > r) ? -INFINITY : fmaf(__uint_as_float(t[2 * e + 1]), sl2, nm);
+        const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+        sum += p0 + p1;
+        pk[8 * h + e] = Pack<BF16>::pack(p0, p1);
+      }
+    }
+    ptx::tmem_st16(tS + 16 * c, pk);
+  }
+  return RowState{sum, m_run, l_run};
+}
 
 template <int D>
 struct Cfg {
@@ -456,100 +571,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(bar_addr(ctl.s_full[wi]), gs & 1, ctl, tmo))) break;
           ++gs;
           ptx::tc_fence_after();
+          const bool diag = j == n_steps - 1;  // key column c is visible to row r iff c <= r
           uint32_t sv[4][32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sv[c]);
           ptx::tmem_wait_ld();
-          if (j == n_steps - 1) {  // diagonal tile: key column c is visible to row r iff c <= r
+          if (diag) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
               for (int e = 0; e < 32; ++e)
                 if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
           }
-          // Row max: three-input max tree, eight independent chains.
-          float acc[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            acc[k] = ptx::fmax3(__uint_as_float(sv[0][k]), __uint_as_float(sv[0][k + 8]),
-                                __uint_as_float(sv[0][k + 16]));
-#pragma unroll
-          for (int base = 24; base < 120; base += 16)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int i0 = base + k, i1 = base + 8 + k;
-              acc[k] = ptx::fmax3(acc[k], __uint_as_float(sv[i0 / 32][i0 % 32]), __uint_as_float(sv[i1 / 32][i1 % 32]));
-            }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc[k] = fmaxf(acc[k], __uint_as_float(sv[3][24 + k]));
-          const float mx = ptx::fmax3(ptx::fmax3(acc[0], acc[1], acc[2]), ptx::fmax3(acc[3], acc[4], acc[5]),
-                                      fmaxf(acc[6], acc[7]));
-          const float m_new = fmaxf(m_run, mx * sl2);
-          // Rescale only when some row's max grew past the threshold (warp-uniform decision, since
-          // TMEM loads and stores are warp-collective); otherwise keep the stale max.
-          float alpha = 1.f;
-          bool rescale = false;
-          if (j == 0) {
-            m_run = m_new;
+          if (j == 0) m_run = row_max128(sv) * sl2;  // the first tile of a row sets the max
+          // P with the running max, kept in registers until the row sums pass the check (S stays
+          // intact in tensor memory until then).
+          uint32_t pk[64];
+          float sum = softmax_p<BF16>(sv, sl2, m_run, pk);
+          const bool need = !(sum <= kSumCap);  // also catches inf / nan
+          if (__any_sync(0xFFFFFFFFu, need)) {
+            const RowState st = softmax_redo<D, BF16>(tS, tO, r, diag, need, sl2, m_run, l_run);
+            sum = st.sum;
+            m_run = st.m;
+            l_run = st.l;
           } else {
-            const bool need = m_new > m_run + kRescaleThreshold;
-            rescale = __any_sync(0xFFFFFFFFu, need);
-            if (need) {
-              alpha = ptx::ex2_approx(m_run - m_new);
-              l_run *= alpha;
-              m_run = m_new;
-            }
-          }
-          // P = 2^(s * log2(e)/sqrt(d) - m) on fp32 pairs; four independent partial row sums.
-          const uint64_t SL2 = ptx::f2_pack(sl2, sl2), NM = ptx::f2_pack(-m_run, -m_run);
-          uint64_t part[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) part[k] = ptx::f2_pack(0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {  // S columns [32 c, 32 c + 32) -> P words [16 c, 16 c + 16)
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const uint64_t x2 = ptx::f2_fma(
-                  ptx::f2_pack(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), SL2, NM);
-              float p0, p1;
-              if ((kPolyChunkMask >> c) & 1u) {
-                exp2_poly_pair(x2, p0, p1);
-              } else {
-                float x0, x1;
-                ptx::f2_unpack(x2, x0, x1);
-                p0 = ptx::ex2_approx(x0);
-                p1 = ptx::ex2_approx(x1);
-              }
-              part[e & 3] = ptx::f2_add(part[e & 3], ptx::f2_pack(p0, p1));
-              pk[e] = Pack<BF16>::pack(p0, p1);
-            }
-            ptx::tmem_st16(tS + 16 * c, pk);
-          }
-          float sum;
-          {
-            float a, bb;
-            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(part[0], part[1]), ptx::f2_add(part[2], part[3])), a, bb);
-            sum = a + bb;
-          }
-          if (rescale) {  // O += P V for this tile is issued only after p_full, so O is stable here
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              ptx::tmem_ld32(tO + 32 * c, o);
-              ptx::tmem_wait_ld();
-              const uint64_t A2 = ptx::f2_pack(alpha, alpha);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const uint64_t v =
-                    ptx::f2_mul(ptx::f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), A2);
-                float a, bb;
-                ptx::f2_unpack(v, a, bb);
-                o[2 * e] = __float_as_uint(a);
-                o[2 * e + 1] = __float_as_uint(bb);
-              }
-              ptx::tmem_st32(tO + 32 * c, o);
-            }
+            for (int c = 0; c < 4; ++c)
+              ptx::tmem_st16(tS + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
           }
           l_run += sum;
           ptx::tmem_wait_st();

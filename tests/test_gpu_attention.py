@@ -104,6 +104,25 @@ def test_rescale_path_one_hot(mode):
     assert np.abs(out[:, [0, 1, 127, 128, 300, 639]].double().numpy() - o_ref).max() <= TOL["fp16"]["max_abs"]
 
 
+@pytest.mark.parametrize("mode", ["fused", "prerotate"])
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_running_max_jumps(mode, dt):
+    # q_63 = 8 and k_63 = c_t on key tile t, in the pair with the slowest frequency (theta ~ 2.6e-6
+    # at base 5e5, so cos((i-j) theta) ~ 1): every score of key tile t is shifted by about
+    # 8 c_t / sqrt(128) nats, which is 1.02 c_t in log2 units, on top of the N(0,1) scores.  With
+    # c = 0, 12, 30, 15, 36 a row's running max grows by ~12 at key tile 1 (kept: P reaches 2^12),
+    # by ~18 at tile 2 (the tile is redone with its own max) and by ~6 at tile 4.  Every element is
+    # compared with the oracle.
+    B, N, Hq, Hkv, d = 1, 640, 4, 2, 128
+    q, k, v = draw(B, N, Hq, Hkv, d, dt, seed=21)
+    c = torch.tensor([0.0, 12.0, 30.0, 15.0, 36.0]).repeat_interleave(128)[:N]
+    q[..., 63] = 8.0
+    k[..., 63] = c.view(1, N, 1).to(k.dtype)
+    o_ref, l_ref = oracle.rope_causal(q, k, v, 5e5)
+    out, lse = run_gpu(q, k, v, 5e5, mode)
+    assert_close(out.double().numpy(), lse.double().numpy(), o_ref, l_ref, dt, f"max jumps {mode} {dt}")
+
+
 def test_lse_optional():
     q, k, v = draw(1, 200, 2, 1, 64, "bf16", seed=3)
     out_a, _ = binding.rope_causal_fwd(q.cuda(), k.cuda(), v.cuda(), 1e4, want_lse=False)
