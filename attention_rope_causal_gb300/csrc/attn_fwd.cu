@@ -10,8 +10,9 @@
 // Relative-Position Attention via Structure-Aware Kernels", prerequisites: FlashAttention and
 // online softmax), in fp32 and with base-2 exponentials (same page, technical novelty (4)).
 //
-// Structure: persistent, one CTA (512 threads) per SM walking a list of work units; a unit is 256
-// query rows of one (b, h) = two 128-row tiles q0, q1.
+// Structure: persistent, one CTA (512 threads) per SM walking a list of work units; a unit is two
+// 128-row query tiles q0, q1 that share every K and V tile: two heads of one KV group on the same
+// rows when the group size is even, else two consecutive row blocks of one head.
 //   warp 0        TMA producer: per unit Q, and K and V tiles (128 keys) through 2-stage rings.
 //   warp 1        tcgen05.mma issuer; owns the tensor-memory allocation (512 columns:
 //                 S0 | S1 | O0 | O1, P_i written over the first half of S_i).
@@ -68,11 +69,12 @@ constexpr uint32_t kPolyChunkMask = 0u;
 // Register split after setmaxnreg (control warps / softmax warps / rotation warps).  The total,
 // 128 x (ctrl + rotate) + 256 x softmax, must not exceed the 512 x 128 registers the CTA is launched
 // with, or the softmax warps' setmaxnreg.inc would wait forever.
-template <int D>
+template <int D, bool ROTATE>
 struct Regs {
-  static constexpr uint32_t kCtrl = 80;
-  static constexpr uint32_t kSoftmax = 168;
-  static constexpr uint32_t kRotate = 88;
+  // Without rotation the rotation warps are idle and the softmax warps take their registers.
+  static constexpr uint32_t kCtrl = ROTATE ? 88 : 80;
+  static constexpr uint32_t kSoftmax = ROTATE ? 168 : 176;
+  static constexpr uint32_t kRotate = ROTATE ? 88 : 80;
   static_assert(128 * (kCtrl + kRotate) + 256 * kSoftmax <= kThreads * 128, "register split");
 };
 
@@ -317,12 +319,16 @@ __device__ __forceinline__ void rotate_tile(uint32_t tile, int r0, int ck, RopeC
 }
 
 // ---- persistent schedule -------------------------------------------------------------------
-// Work unit = (b, h, 256-row query block t), numbered longest-first (t descending).  CTA c of G
+// Work unit = (b, head pair, 128-row block t) or (b, h, 256-row block t), numbered longest-first
+// (t descending).  CTA c of G
 // processes units c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the longest-first order), which evens
 // out the causal work across CTAs without a shared counter.  Every role walks the same sequence.
 struct Unit {
-  int b, h, hk, q_row0, n0, n1, n_kt;
+  int b, hk, n0, n1, n_kt;
+  int h0, h1, r0, r1;  // query tile i: head h_i, first row r_i
   bool active1;
+  __device__ __forceinline__ int head(int i) const { return i == 0 ? h0 : h1; }
+  __device__ __forceinline__ int row(int i) const { return i == 0 ? r0 : r1; }
 };
 
 __device__ __forceinline__ int unit_of_round(int round, int c, int G) {
@@ -331,14 +337,31 @@ __device__ __forceinline__ int unit_of_round(int round, int c, int G) {
 
 __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
   Unit x;
+  if (p.head_pairs) {
+    // Two query heads of one KV group on the same 128 rows: q0 = head 2 j, q1 = head 2 j + 1, both
+    // over key tiles 0 .. t (t = the diagonal tile).
+    const int pairs = p.B * (p.Hq / 2);
+    const int t = p.n_qblocks - 1 - u / pairs;
+    const int bj = u - (u / pairs) * pairs;
+    x.b = bj / (p.Hq / 2);
+    x.h0 = 2 * (bj - x.b * (p.Hq / 2));
+    x.h1 = x.h0 + 1;
+    x.hk = x.h0 / (p.Hq / p.Hkv);
+    x.r0 = x.r1 = t * BM;
+    x.active1 = true;
+    x.n0 = x.n1 = x.n_kt = t + 1;
+    return x;
+  }
+  // Two consecutive 128-row tiles of one head: q0 rows 256 t.., q1 rows 256 t + 128..
   const int bh_count = p.B * p.Hq;
   const int t = p.n_qblocks - 1 - u / bh_count;
   const int bh = u - (u / bh_count) * bh_count;
   x.b = bh / p.Hq;
-  x.h = bh - x.b * p.Hq;
-  x.hk = x.h / (p.Hq / p.Hkv);
-  x.q_row0 = t * 2 * BM;
-  x.active1 = x.q_row0 + BM < p.N;
+  x.h0 = x.h1 = bh - x.b * p.Hq;
+  x.hk = x.h0 / (p.Hq / p.Hkv);
+  x.r0 = t * 2 * BM;
+  x.r1 = x.r0 + BM;
+  x.active1 = x.r1 < p.N;
   x.n0 = 2 * t + 1;                  // key tiles for q0 (tile 2t is its diagonal)
   x.n1 = x.active1 ? 2 * t + 2 : 0;  // key tiles for q1
   x.n_kt = x.active1 ? x.n1 : x.n0;
@@ -413,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();  // setmaxnreg and tcgen05 warp-collectives need converged warps
 
   if (warp < 4) {
-    ptx::setmaxnreg_dec<Regs<D>::kCtrl>();
+    ptx::setmaxnreg_dec<Regs<D, ROTATE>::kCtrl>();
     if (!skip && warp == 0 && lane == 0) {
       // ================================ TMA producer ==========================================
       // Per unit: K_0/V_0 first (their ring stages free up early), then Q once the previous
@@ -447,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(bar_addr(ctl.q_full), (uint32_t)nq * C::TILE);
         for (int i = 0; i < nq; ++i)
           for (int bx = 0; bx < C::NBOX; ++bx)
-            ptx::tma_load_4d(sQ + i * C::TILE + bx * kBoxBytes, &tmQ, bar_addr(ctl.q_full), bx * 64, U.h,
-                             U.q_row0 + i * BM, U.b);
+            ptx::tma_load_4d(sQ + i * C::TILE + bx * kBoxBytes, &tmQ, bar_addr(ctl.q_full), bx * 64, U.head(i),
+                             U.row(i), U.b);
         ++uc;
         for (int i = 1; i < U.n_kt && ok; ++i) ok = load_kv(i);
         if (!ok) break;
@@ -551,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar(bar_addr(ctl.mma_done), 0, 100000000ull);
     }
   } else if (warp < 12) {
-    ptx::setmaxnreg_inc<Regs<D>::kSoftmax>();
+    ptx::setmaxnreg_inc<Regs<D, ROTATE>::kSoftmax>();
     if (!skip) {
       // ================================ softmax + epilogue ====================================
       const int wi = (warp - 4) / 4;  // which query tile
@@ -565,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       FOR_EACH_UNIT(U) {
         const int n_steps = wi == 0 ? U.n0 : U.n1;
         if (n_steps == 0) continue;
-        const int qt = U.q_row0 / BM + wi;
+        const int qt = U.row(wi) / BM;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_steps && ok; ++j) {
           if (!(ok = wait_bar_warp(bar_addr(ctl.s_full[wi]), gs & 1, ctl, tmo))) break;
@@ -610,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int row = qt * BM + r;
         const float inv_l = 1.f / l_run;
-        T* orow = reinterpret_cast<T*>(p.out) + (((size_t)U.b * p.N + row) * p.Hq + U.h) * D;
+        const int head = U.head(wi);
+        T* orow = reinterpret_cast<T*>(p.out) + (((size_t)U.b * p.N + row) * p.Hq + head) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -627,13 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (row < p.N && p.lse != nullptr)
-          p.lse[((size_t)U.b * p.Hq + U.h) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
+          p.lse[((size_t)U.b * p.Hq + head) * p.N + row] = (m_run + log2f(l_run)) * kLn2;
         // The O reads above completed (wait::ld) before this warpgroup's next p_full arrive, which
         // is what lets the next unit's first O += P V overwrite O.
       }
     }
   } else {
-    ptx::setmaxnreg_dec<Regs<D>::kRotate>();
+    ptx::setmaxnreg_dec<Regs<D, ROTATE>::kRotate>();
     if constexpr (ROTATE) {
       if (!skip) {
         // ============================== Q and K tile rotation ===================================
@@ -664,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++uc;
               for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
                 RopeCS8 qcs;
-                rope_cs8_exact((uint32_t)(U.q_row0 + tq * BM + r0), sfreq, sfreq + 64, ck * 8, qcs);
+                rope_cs8_exact((uint32_t)(U.row(tq) + r0), sfreq, sfreq + 64, ck * 8, qcs);
                 rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
               }
               ptx::fence_proxy_async_smem();

@@ -224,8 +224,12 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.N = N;
-  p.n_qblocks = (N + 255) / 256;
-  p.total_units = B * Hq * p.n_qblocks;
+  // GQA with an even group size pairs two query heads of a KV group on the same rows (equal key
+  // ranges: no half-empty last step, finer units for the persistent schedule); otherwise a unit is
+  // two consecutive 128-row tiles of one head.
+  p.head_pairs = (Hq / Hkv) % 2 == 0 ? 1 : 0;
+  p.n_qblocks = p.head_pairs ? (N + 127) / 128 : (N + 255) / 256;
+  p.total_units = p.head_pairs ? B * (Hq / 2) * p.n_qblocks : B * Hq * p.n_qblocks;
   p.out = out;
   p.lse = lse;
   p.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));

@@ -35,8 +35,10 @@ cudaError_t launch_rope_apply(const RopeApplyParams& p, int d, bool bf16, cudaSt
 
 struct AttnParams {
   int B, Hq, Hkv, N;
-  int n_qblocks;     // ceil(N / 256): 256 query rows (two 128-row tiles) per CTA
-  int total_units;   // B * Hq * n_qblocks
+  int head_pairs;    // 1: a work unit is two query heads of one KV group on the same 128 rows
+                     // (Hq / Hkv even); 0: two consecutive 128-row tiles of one head
+  int n_qblocks;     // query blocks per head: ceil(N / 128) with head pairs, ceil(N / 256) without
+  int total_units;   // B * Hq * n_qblocks, halved with head pairs
   void* out;         // [B, N, Hq, d]
   float* lse;        // [B, Hq, N] or nullptr
   float scale_log2;  // log2(e) / sqrt(d)
