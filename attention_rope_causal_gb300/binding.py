@@ -14,10 +14,11 @@ import torch
 
 from . import build as _build
 
-ATTNFUSE_FUSED, ATTNFUSE_PREROTATE = 0, 1
+ATTNFUSE_FUSED, ATTNFUSE_PREROTATE, ATTNFUSE_AUTO = 0, 1, 2
 ATTNFUSE_BF16, ATTNFUSE_FP16 = 0, 1
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_TIMEOUT", 5: "ERR_NO_MEMORY"}
-MODES = {"fused": ATTNFUSE_FUSED, "prerotate": ATTNFUSE_PREROTATE}
+MODES = {"fused": ATTNFUSE_FUSED, "prerotate": ATTNFUSE_PREROTATE, "auto": ATTNFUSE_AUTO}
+MODE_NAMES = {v: k for k, v in MODES.items()}
 DTYPES = {torch.bfloat16: ATTNFUSE_BF16, torch.float16: ATTNFUSE_FP16}
 
 # Every function the header declares, with its ctypes signature.
@@ -27,6 +28,7 @@ _SIGNATURES = {
                                                 ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "attnfuse_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 7),
+    "attnfuse_select_mode": (ctypes.c_int, [ctypes.c_int] * 6),
     "attnfuse_rope_causal_fwd_prerotate_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -91,6 +93,11 @@ def _ptr(t):
 
 def workspace_bytes(B, Hq, Hkv, N, d, mode="fused", dtype=torch.bfloat16) -> int:
     return int(load().attnfuse_workspace_bytes(B, Hq, Hkv, N, d, MODES[mode], DTYPES[dtype]))
+
+
+def select_mode(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> str:
+    """The mode ``auto`` resolves to for this shape (``attnfuse_select_mode``)."""
+    return MODE_NAMES[int(load().attnfuse_select_mode(B, Hq, Hkv, N, d, DTYPES[dtype]))]
 
 
 def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, lse=None, want_lse: bool = True,

@@ -120,7 +120,8 @@ attnfuse_status_t validate_fwd(const void* q, const void* k, const void* v, cons
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "B, Hq, Hkv, N must be >= 1");
   if (N >= kMaxN) return fail(ATTNFUSE_ERR_INVALID_ARG, "N=%d exceeds the supported maximum %d", N, kMaxN - 1);
   if (Hq % Hkv != 0) return fail(ATTNFUSE_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE) return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0) or prerotate (1)", (int)mode);
+  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE && mode != ATTNFUSE_AUTO)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0), prerotate (1) or auto (2)", (int)mode);
   attnfuse_status_t st = check_dtype_d(d, dtype);
   if (st != ATTNFUSE_OK) return st;
   if ((st = check_base(base)) != ATTNFUSE_OK) return st;
@@ -163,9 +164,21 @@ const char* attnfuse_status_string(attnfuse_status_t s) {
 
 const char* attnfuse_last_error(void) { return g_err; }
 
+attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype) {
+  (void)d;
+  (void)dtype;
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0) return ATTNFUSE_FUSED;
+  // Measured on GB300 (bench.py --sweep): with 4:1 GQA, pre-rotation wins at every N in [2048,
+  // 16384] (both dtypes); with MHA d=64 the crossover is N* ~ 4000 (3980 bf16, 4030 fp16).
+  const bool gqa = Hq / Hkv >= 2;
+  const int n_star = gqa ? 2048 : 4000;
+  return N >= n_star ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
+}
+
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return 0;
+  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, N, d, dtype);
   if (mode != ATTNFUSE_PREROTATE) return 0;
   return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, N, Hkv, d), 256);
 }
@@ -209,6 +222,7 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
   g_err[0] = '\0';
   attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, mode, dtype);
   if (st != ATTNFUSE_OK) return st;
+  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, N, d, dtype);
   const size_t need = attnfuse_workspace_bytes(B, Hq, Hkv, N, d, mode, dtype);
   if (workspace) {
     if (workspace_bytes < need)

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-typedef enum { ATTNFUSE_FUSED = 0, ATTNFUSE_PREROTATE = 1 } attnfuse_mode_t;
+typedef enum { ATTNFUSE_FUSED = 0, ATTNFUSE_PREROTATE = 1, ATTNFUSE_AUTO = 2 } attnfuse_mode_t;
 
 typedef enum { ATTNFUSE_BF16 = 0, ATTNFUSE_FP16 = 1 } attnfuse_dtype_t;
 
@@ -60,6 +60,7 @@ typedef enum {
  *   mode = ATTNFUSE_FUSED:     one kernel; Q and K tiles are rotated in shared memory.
  *   mode = ATTNFUSE_PREROTATE: a RoPE pass writes rotated Q', K' into `workspace`, then the same
  *                              attention kernel runs on Q', K', V without rotation.
+ *   mode = ATTNFUSE_AUTO:      whichever of the two attnfuse_select_mode returns for the shape.
  * Both modes compute the function in the header comment.  `lse` may be NULL (not written).
  * `workspace` must hold attnfuse_workspace_bytes(...) bytes (0 for FUSED); if it is NULL while
  * bytes are needed, the call allocates with cudaMallocAsync and frees with cudaFreeAsync on
@@ -71,8 +72,20 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
                                            void* stream);
 
 /* Bytes of workspace attnfuse_rope_causal_fwd needs: 0 for FUSED; for PREROTATE the rotated copies
- * of Q and K (each rounded up to 256 bytes).  Returns 0 for invalid arguments. */
+ * of Q and K (each rounded up to 256 bytes); for AUTO those of the selected mode.  Returns 0 for
+ * invalid arguments. */
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype);
+
+/*
+ * The faster of FUSED and PREROTATE for a shape on GB300, from the measured fused-vs-pre-rotate
+ * crossover ("Rotation Calculus" in "AttnFuse Makes RoPE a First-Class Attention Compilation
+ * Operation", paragraph 2, made a runtime choice): grouped-query attention (Hq / Hkv >= 2) with
+ * N >= 2048 -> PREROTATE (measured faster at every N from 2048 to 16384); multi-head attention
+ * (Hq == Hkv) with N >= 4000 -> PREROTATE (measured N* ~ 4000); everything else -> FUSED.
+ * Host-only and pure: no device access; arguments it cannot judge (non-positive sizes, Hq not a
+ * multiple of Hkv) give FUSED.
+ */
+attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype);
 
 /*
  * RoPE alone (the pre-rotation pass): y = RoPE(x) for x, y of shape [B, N, H, d], position of

@@ -52,7 +52,8 @@ def fwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, B=1, Hq=4, Hkv=2, N=128
 
 @pytest.mark.parametrize("kw,status", [
     (dict(q=None), 1), (dict(out=None), 1), (dict(B=0), 1), (dict(N=0), 1), (dict(Hq=3, Hkv=2), 1),
-    (dict(d=96), 2), (dict(d=256), 2), (dict(dtype=7), 1), (dict(mode=5), 1), (dict(base=0.5), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(dtype=7), 1), (dict(mode=5), 1), (dict(mode=-1), 1),
+    (dict(base=0.5), 1), (dict(mode=2, B=0), 1),
     (dict(base=float("nan")), 1), (dict(q=FAKE + 8), 1), (dict(lse=FAKE + 2), 1), (dict(N=1 << 24), 1),
     (dict(mode=1, ws=FAKE, ws_bytes=16), 1), (dict(mode=1, ws=FAKE + 16, ws_bytes=1 << 40), 1),
 ])
@@ -77,6 +78,26 @@ def test_workspace_bytes(lib):
     assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 1, 0) == q + k
     assert lib.attnfuse_workspace_bytes(1, 1, 1, 1, 64, 1, 1) == 256 + 256
     assert lib.attnfuse_workspace_bytes(1, 1, 1, 1, 96, 1, 1) == 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,mode", [
+    (1, 32, 8, 4096, 1), (4, 32, 8, 2048, 1), (1, 32, 8, 16384, 1), (8, 32, 8, 1024, 0),  # GQA 4:1
+    (1, 8, 4, 3000, 1), (1, 64, 8, 2047, 0),                                           # other groups
+    (2, 16, 16, 2048, 0), (1, 16, 16, 3999, 0), (1, 16, 16, 4000, 1), (1, 16, 16, 32768, 1),  # MHA
+    (0, 16, 16, 4096, 0), (1, 6, 4, 4096, 0),                                          # not judged
+])
+def test_select_mode_follows_the_measured_crossover(lib, B, Hq, Hkv, N, mode):
+    for d in (64, 128):
+        for dtype in (0, 1):
+            assert lib.attnfuse_select_mode(B, Hq, Hkv, N, d, dtype) == mode
+
+
+def test_auto_mode_workspace_is_that_of_the_selected_mode(lib):
+    for shape in ((1, 32, 8, 4096, 128), (2, 16, 16, 2048, 64), (1, 16, 16, 8192, 64)):
+        sel = lib.attnfuse_select_mode(*shape, 0)
+        assert lib.attnfuse_workspace_bytes(*shape, 2, 0) == lib.attnfuse_workspace_bytes(*shape, sel, 0)
+    assert binding.select_mode(1, 32, 8, 4096, 128) == "prerotate"
+    assert binding.select_mode(2, 16, 16, 2048, 64) == "fused"
 
 
 def test_valid_call_without_gpu_fails_cleanly(lib):

@@ -123,6 +123,20 @@ def test_running_max_jumps(mode, dt):
     assert_close(out.double().numpy(), lse.double().numpy(), o_ref, l_ref, dt, f"max jumps {mode} {dt}")
 
 
+@pytest.mark.parametrize("shape", [(1, 2048, 4, 2, 64, "bf16"), (1, 300, 4, 4, 64, "fp16")])
+def test_auto_mode_runs_the_selected_mode(shape):
+    # mode "auto" resolves on the host to fused or pre-rotate (attnfuse_select_mode) and then runs
+    # exactly that path: bitwise the same result, and within the oracle tolerance.
+    B, N, Hq, Hkv, d, dt = shape
+    q, k, v = draw(B, N, Hq, Hkv, d, dt, seed=31)
+    sel = binding.select_mode(B, Hq, Hkv, N, d, q.dtype)
+    oa, la = run_gpu(q, k, v, 1e4, "auto")
+    os_, ls = run_gpu(q, k, v, 1e4, sel)
+    assert torch.equal(oa, os_) and torch.equal(la, ls)
+    o_ref, l_ref = oracle.rope_causal(q, k, v, 1e4)
+    assert_close(oa.double().numpy(), la.double().numpy(), o_ref, l_ref, dt, f"auto ({sel}) {shape}")
+
+
 def test_lse_optional():
     q, k, v = draw(1, 200, 2, 1, 64, "bf16", seed=3)
     out_a, _ = binding.rope_causal_fwd(q.cuda(), k.cuda(), v.cuda(), 1e4, want_lse=False)
