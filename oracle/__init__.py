@@ -11,7 +11,9 @@ ctypes.  What it computes, and the passages it follows, are stated in that file'
   Compilation Operation", 2026-09-13 AI papers report, paragraph 1; AttnFuse abstract), half-split
   pairs (k, k+d/2), theta_k = base^(-2k/d), position = token index;
 * causal softmax attention (same report, paragraph 2: causality and softmax building blocks),
-  scale 1/sqrt(d), natural-log log-sum-exp per row, GQA head h -> kv head floor(h*Hkv/Hq).
+  scale 1/sqrt(d), natural-log log-sum-exp per row, GQA head h -> kv head floor(h*Hkv/Hq);
+* RoPE variants (``rotary_dim``, ``interleaved``): only the first r entries rotated with
+  theta_k = base^(-2k/r), and adjacent pairs (2k, 2k+1) instead of (k, k+r/2).
 """
 from __future__ import annotations
 
@@ -58,6 +60,15 @@ def _load():
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_int]
+            lib.orc_rope_rotate_ex.restype = ctypes.c_int
+            lib.orc_rope_rotate_ex.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                               ctypes.c_double, ctypes.c_void_p, ctypes.c_int]
+            lib.orc_rope_causal_ex.restype = ctypes.c_int
+            lib.orc_rope_causal_ex.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
+                                               ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -92,8 +103,11 @@ def _as_raw(x):
     raise TypeError(f"oracle accepts float64/float16 arrays or torch bf16/fp16/fp64 tensors, got {x.dtype}")
 
 
-def rope_rotate(x, base: float, positions=None, threads: int | None = None) -> np.ndarray:
+def rope_rotate(x, base: float, positions=None, threads: int | None = None, rotary_dim: int | None = None,
+                interleaved: bool = False) -> np.ndarray:
     """Rotate x of shape [..., R, H, d] (R rows of H heads); row r sits at positions[r] (default: r).
+
+    rotary_dim (default d) rotates only the first rotary_dim entries; interleaved pairs (2k, 2k+1).
 
     Leading dimensions are flattened into rows, so for [B, N, H, d] the default position of (b, n) is
     n only when B == 1; pass ``positions`` explicitly (or use :func:`rope_rotate_bnhd`) otherwise.
@@ -111,22 +125,27 @@ def rope_rotate(x, base: float, positions=None, threads: int | None = None) -> n
         if pos.size != rows:
             raise ValueError(f"positions has {pos.size} entries for {rows} rows")
     out = np.empty(shape, dtype=np.float64)
-    rc = _load().orc_rope_rotate(raw.ctypes.data, dt, rows, H, d, pos.ctypes.data, float(base), out.ctypes.data,
-                                 int(threads or default_threads()))
+    r = d if rotary_dim is None else int(rotary_dim)
+    rc = _load().orc_rope_rotate_ex(raw.ctypes.data, dt, rows, H, d, r, int(bool(interleaved)), pos.ctypes.data,
+                                    float(base), out.ctypes.data, int(threads or default_threads()))
     if rc != 0:
-        raise RuntimeError("orc_rope_rotate failed")
+        raise RuntimeError("orc_rope_rotate_ex failed")
     return out
 
 
-def rope_rotate_bnhd(x, base: float, threads: int | None = None) -> np.ndarray:
+def rope_rotate_bnhd(x, base: float, threads: int | None = None, rotary_dim: int | None = None,
+                     interleaved: bool = False) -> np.ndarray:
     """Rotate x of shape [B, N, H, d] with position = token index n (the library's convention)."""
     B, N = x.shape[0], x.shape[1]
     pos = np.tile(np.arange(N, dtype=np.float64), B)
-    return rope_rotate(x, base, positions=pos, threads=threads)
+    return rope_rotate(x, base, positions=pos, threads=threads, rotary_dim=rotary_dim, interleaved=interleaved)
 
 
-def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None):
+def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None, rotary_dim: int | None = None,
+                interleaved: bool = False):
     """Causal softmax attention with RoPE on q and k.
+
+    rotary_dim (default d) and interleaved select the RoPE variant (see :func:`rope_rotate`).
 
     q: [B, N, Hq, d]; k, v: [B, N, Hkv, d] (same dtype: bf16/fp16 torch tensors, fp16 or fp64 arrays).
     rows: optional 1-D sequence of query positions to evaluate (default: all N in order).
@@ -156,8 +175,10 @@ def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None):
     lse = np.zeros((B, Hq, n_sel), dtype=np.float64)
     if n_sel == 0:
         return out, lse
-    rc = _load().orc_rope_causal(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, dq, B, Hq, Hkv, N, d, float(base),
-                                 sel_ptr, n_sel, out.ctypes.data, lse.ctypes.data, int(threads or default_threads()))
+    r = d if rotary_dim is None else int(rotary_dim)
+    rc = _load().orc_rope_causal_ex(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, dq, B, Hq, Hkv, N, d, r,
+                                    int(bool(interleaved)), float(base), sel_ptr, n_sel, out.ctypes.data,
+                                    lse.ctypes.data, int(threads or default_threads()))
     if rc != 0:
-        raise RuntimeError("orc_rope_causal failed")
+        raise RuntimeError("orc_rope_causal_ex failed")
     return out, lse

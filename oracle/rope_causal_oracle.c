@@ -17,6 +17,13 @@
  *       x'[k+d/2]   = x[k+d/2]   cos(p theta_k) + x[k]     sin(p theta_k)
  *   with p the token index.  V is not rotated.
  *
+ *   Variants (the "_ex" entry points): a rotary dimension r <= d rotates only the first r entries
+ *   of each head vector, with theta_k = base^(-2k/r), k = 0 .. r/2-1, and leaves entries r .. d-1
+ *   unchanged; the interleaved form pairs (2k, 2k+1) instead of (k, k+r/2):
+ *       x'[2k]   = x[2k]   cos(p theta_k) - x[2k+1] sin(p theta_k)
+ *       x'[2k+1] = x[2k+1] cos(p theta_k) + x[2k]   sin(p theta_k)
+ *   Both are the same plane rotations as the half-split form on a permuted set of planes.
+ *
  *   Causal softmax attention.  Same report, paragraph 2 (causality and softmax building blocks):
  *       s_ij = (q'_i . k'_j) / sqrt(d)      for j <= i   (keys j > i are excluded)
  *       o_i  = sum_j softmax_j(s_ij) v_j
@@ -63,21 +70,35 @@ static double load_elem(const void *p, int dtype, size_t idx) {
   return dtype == ORC_BF16 ? decode_bf16(h) : decode_f16(h);
 }
 
-/* theta_k = base^(-2k/d) for k in [0, d/2). */
-static void rope_frequencies(int d, double base, double *theta) {
-  for (int k = 0; k < d / 2; ++k) theta[k] = pow(base, -2.0 * (double)k / (double)d);
+/* Which entries of a head vector are rotated, and how they are paired. */
+typedef struct {
+  int d;           /* head dimension */
+  int r;           /* rotary dimension: entries [0, r) are rotated, [r, d) copied; even, 2 <= r <= d */
+  int interleaved; /* 0: pairs (k, k + r/2); 1: pairs (2k, 2k + 1) */
+} rope_form_t;
+
+/* theta_k = base^(-2k/r) for k in [0, r/2). */
+static void rope_frequencies(int r, double base, double *theta) {
+  for (int k = 0; k < r / 2; ++k) theta[k] = pow(base, -2.0 * (double)k / (double)r);
 }
 
-/* Rotate one head vector x[0..d) that sits at position pos (half-split pairs). */
-static void rope_rotate_vec(const double *x, double *y, int d, double pos, const double *theta) {
-  int half = d / 2;
+/* Rotate one head vector x[0..d) that sits at position pos. */
+static void rope_rotate_vec(const double *x, double *y, rope_form_t f, double pos, const double *theta) {
+  int half = f.r / 2;
   for (int k = 0; k < half; ++k) {
     double angle = pos * theta[k];
     double c = cos(angle), s = sin(angle);
-    double a = x[k], b = x[k + half];
-    y[k] = a * c - b * s;
-    y[k + half] = b * c + a * s;
+    int ia = f.interleaved ? 2 * k : k;
+    int ib = f.interleaved ? 2 * k + 1 : k + half;
+    double a = x[ia], b = x[ib];
+    y[ia] = a * c - b * s;
+    y[ib] = b * c + a * s;
   }
+  for (int e = f.r; e < f.d; ++e) y[e] = x[e];
+}
+
+static int form_ok(rope_form_t f) {
+  return f.d >= 2 && f.r >= 2 && f.r <= f.d && (f.r % 2) == 0 && (f.interleaved == 0 || f.interleaved == 1);
 }
 
 /* ------------------------------------------------------------------------------------------- */
@@ -132,7 +153,8 @@ static int orc_run(orc_pool_t *pool, int nthreads) {
 typedef struct {
   const void *x;
   int dtype;
-  int H, d;
+  int H;
+  rope_form_t form;
   const double *positions;
   const double *theta;
   double *out;
@@ -140,24 +162,32 @@ typedef struct {
 
 static void rot_item(void *vctx, int64_t r, double *scratch) {
   rot_ctx_t *c = (rot_ctx_t *)vctx;
+  int d = c->form.d;
   for (int h = 0; h < c->H; ++h) {
-    size_t base = ((size_t)r * c->H + h) * c->d;
-    for (int e = 0; e < c->d; ++e) scratch[e] = load_elem(c->x, c->dtype, base + e);
-    rope_rotate_vec(scratch, c->out + base, c->d, c->positions[r], c->theta);
+    size_t base = ((size_t)r * c->H + h) * d;
+    for (int e = 0; e < d; ++e) scratch[e] = load_elem(c->x, c->dtype, base + e);
+    rope_rotate_vec(scratch, c->out + base, c->form, c->positions[r], c->theta);
   }
 }
 
-int orc_rope_rotate(const void *x, int dtype, int64_t rows, int H, int d, const double *positions, double base,
-                    double *out, int nthreads) {
-  if (!x || !positions || !out || rows < 0 || H < 1 || d < 2 || (d % 2) != 0) return -1;
-  double *theta = (double *)malloc(sizeof(double) * (size_t)(d / 2));
+int orc_rope_rotate_ex(const void *x, int dtype, int64_t rows, int H, int d, int rotary_dim, int interleaved,
+                       const double *positions, double base, double *out, int nthreads) {
+  rope_form_t f = {d, rotary_dim, interleaved};
+  if (!x || !positions || !out || rows < 0 || H < 1 || !form_ok(f)) return -1;
+  double *theta = (double *)malloc(sizeof(double) * (size_t)(f.r / 2));
   if (!theta) return -1;
-  rope_frequencies(d, base, theta);
-  rot_ctx_t ctx = {x, dtype, H, d, positions, theta, out};
+  rope_frequencies(f.r, base, theta);
+  rot_ctx_t ctx = {x, dtype, H, f, positions, theta, out};
   orc_pool_t pool = {rot_item, &ctx, rows, 0, (size_t)d, 0};
   int rc = orc_run(&pool, nthreads);
   free(theta);
   return rc;
+}
+
+int orc_rope_rotate(const void *x, int dtype, int64_t rows, int H, int d, const double *positions, double base,
+                    double *out, int nthreads) {
+  if (d < 2 || (d % 2) != 0) return -1;
+  return orc_rope_rotate_ex(x, dtype, rows, H, d, d, 0, positions, base, out, nthreads);
 }
 
 /* ------------------------------------------------------------------------------------------- */
@@ -169,6 +199,7 @@ typedef struct {
   const void *q, *v;
   int dtype;
   int B, Hq, Hkv, N, d;
+  rope_form_t form;
   const double *theta;
   const double *krot; /* [B, N, Hkv, d] rotated keys */
   const int64_t *sel;
@@ -179,7 +210,8 @@ typedef struct {
 typedef struct {
   const void *k;
   int dtype;
-  int Hkv, d;
+  int Hkv;
+  rope_form_t form;
   int N;
   const double *theta;
   double *krot;
@@ -188,10 +220,11 @@ typedef struct {
 static void krot_item(void *vctx, int64_t bn, double *scratch) {
   krot_ctx_t *c = (krot_ctx_t *)vctx;
   int n = (int)(bn % c->N);
+  int d = c->form.d;
   for (int h = 0; h < c->Hkv; ++h) {
-    size_t base = ((size_t)bn * c->Hkv + h) * c->d;
-    for (int e = 0; e < c->d; ++e) scratch[e] = load_elem(c->k, c->dtype, base + e);
-    rope_rotate_vec(scratch, c->krot + base, c->d, (double)n, c->theta);
+    size_t base = ((size_t)bn * c->Hkv + h) * d;
+    for (int e = 0; e < d; ++e) scratch[e] = load_elem(c->k, c->dtype, base + e);
+    rope_rotate_vec(scratch, c->krot + base, c->form, (double)n, c->theta);
   }
 }
 
@@ -209,7 +242,7 @@ static void attn_item(void *vctx, int64_t item, double *scratch) {
 
   size_t qbase = (((size_t)b * c->N + (size_t)i) * c->Hq + h) * d;
   for (int e = 0; e < d; ++e) qraw[e] = load_elem(c->q, c->dtype, qbase + e);
-  rope_rotate_vec(qraw, qrot, d, (double)i, c->theta);
+  rope_rotate_vec(qraw, qrot, c->form, (double)i, c->theta);
 
   double scale = 1.0 / sqrt((double)d);
   double mx = -INFINITY;
@@ -235,35 +268,42 @@ static void attn_item(void *vctx, int64_t item, double *scratch) {
   if (c->lse) c->lse[((size_t)b * c->Hq + h) * c->n_sel + (size_t)s] = mx + log(denom);
 }
 
-int orc_rope_causal(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
-                    double base, const int64_t *sel_rows, int64_t n_sel, double *out, double *lse, int nthreads) {
-  if (!q || !k || !v || !out || B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 2 || (d % 2) != 0 || (Hq % Hkv) != 0)
-    return -1;
+int orc_rope_causal_ex(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
+                       int rotary_dim, int interleaved, double base, const int64_t *sel_rows, int64_t n_sel,
+                       double *out, double *lse, int nthreads) {
+  rope_form_t f = {d, rotary_dim, interleaved};
+  if (!q || !k || !v || !out || B < 1 || Hq < 1 || Hkv < 1 || N < 1 || !form_ok(f) || (Hq % Hkv) != 0) return -1;
   if (!sel_rows) n_sel = N;
   if (n_sel < 0) return -1;
   if (sel_rows)
     for (int64_t s = 0; s < n_sel; ++s)
       if (sel_rows[s] < 0 || sel_rows[s] >= N) return -1;
 
-  double *theta = (double *)malloc(sizeof(double) * (size_t)(d / 2));
+  double *theta = (double *)malloc(sizeof(double) * (size_t)(f.r / 2));
   double *krot = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N * (size_t)Hkv * (size_t)d);
   if (!theta || !krot) {
     free(theta);
     free(krot);
     return -1;
   }
-  rope_frequencies(d, base, theta);
+  rope_frequencies(f.r, base, theta);
 
-  krot_ctx_t kctx = {k, dtype, Hkv, d, N, theta, krot};
+  krot_ctx_t kctx = {k, dtype, Hkv, f, N, theta, krot};
   orc_pool_t kpool = {krot_item, &kctx, (int64_t)B * N, 0, (size_t)d, 0};
   int rc = orc_run(&kpool, nthreads);
 
   if (rc == 0) {
-    attn_ctx_t actx = {q, v, dtype, B, Hq, Hkv, N, d, theta, krot, sel_rows, n_sel, out, lse};
+    attn_ctx_t actx = {q, v, dtype, B, Hq, Hkv, N, d, f, theta, krot, sel_rows, n_sel, out, lse};
     orc_pool_t apool = {attn_item, &actx, (int64_t)B * Hq * n_sel, 0, (size_t)(2 * d + N), 0};
     rc = orc_run(&apool, nthreads);
   }
   free(theta);
   free(krot);
   return rc;
+}
+
+int orc_rope_causal(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
+                    double base, const int64_t *sel_rows, int64_t n_sel, double *out, double *lse, int nthreads) {
+  if (d < 2 || (d % 2) != 0) return -1;
+  return orc_rope_causal_ex(q, k, v, dtype, B, Hq, Hkv, N, d, d, 0, base, sel_rows, n_sel, out, lse, nthreads);
 }
