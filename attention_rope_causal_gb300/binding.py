@@ -21,12 +21,25 @@ MODES = {"fused": ATTNFUSE_FUSED, "prerotate": ATTNFUSE_PREROTATE, "auto": ATTNF
 MODE_NAMES = {v: k for k, v in MODES.items()}
 DTYPES = {torch.bfloat16: ATTNFUSE_BF16, torch.float16: ATTNFUSE_FP16}
 
+class RopeOpts(ctypes.Structure):
+    """attnfuse_rope_opts_t: rotary_dim (0 = d) and interleaved (0 = half-split pairs)."""
+    _fields_ = [("rotary_dim", ctypes.c_int), ("interleaved", ctypes.c_int)]
+
+
 # Every function the header declares, with its ctypes signature.
 _SIGNATURES = {
     "attnfuse_rope_causal_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "attnfuse_rope_causal_fwd_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                                   ctypes.POINTER(RopeOpts), ctypes.c_void_p]),
+    "attnfuse_rope_apply_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.POINTER(RopeOpts),
+                                              ctypes.c_void_p]),
     "attnfuse_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 7),
     "attnfuse_select_mode": (ctypes.c_int, [ctypes.c_int] * 6),
     "attnfuse_rope_causal_fwd_prerotate_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -100,11 +113,18 @@ def select_mode(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> str:
     return MODE_NAMES[int(load().attnfuse_select_mode(B, Hq, Hkv, N, d, DTYPES[dtype]))]
 
 
+def _opts(rotary_dim, interleaved):
+    if rotary_dim is None and not interleaved:
+        return None
+    return RopeOpts(int(rotary_dim or 0), int(bool(interleaved)))
+
+
 def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, lse=None, want_lse: bool = True,
-                    workspace=None, stream=None):
-    """Causal RoPE attention forward through ``attnfuse_rope_causal_fwd``.
+                    workspace=None, stream=None, rotary_dim=None, interleaved: bool = False):
+    """Causal RoPE attention forward through ``attnfuse_rope_causal_fwd`` (``_ex`` for a RoPE variant).
 
     q: [B, N, Hq, d], k/v: [B, N, Hkv, d] CUDA tensors (bf16 or fp16, contiguous).
+    rotary_dim / interleaved select a RoPE variant (attnfuse_rope_opts_t).
     Returns (out [B, N, Hq, d], lse [B, Hq, N] float32 or None).
     """
     B, N, Hq, d = q.shape
@@ -119,21 +139,33 @@ def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, ls
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    _check(load().attnfuse_rope_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
-                                           float(rope_base), MODES[mode], DTYPES[q.dtype], ws_ptr, ws_bytes,
-                                           _stream_ptr(stream)))
+    opts = _opts(rotary_dim, interleaved)
+    if opts is None:
+        _check(load().attnfuse_rope_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
+                                               float(rope_base), MODES[mode], DTYPES[q.dtype], ws_ptr, ws_bytes,
+                                               _stream_ptr(stream)))
+    else:
+        _check(load().attnfuse_rope_causal_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
+                                                  float(rope_base), MODES[mode], DTYPES[q.dtype], ws_ptr, ws_bytes,
+                                                  ctypes.byref(opts), _stream_ptr(stream)))
     return out, lse
 
 
-def rope_apply(x, rope_base: float, out=None, stream=None):
-    """y = RoPE(x) for x [B, N, H, d] through ``attnfuse_rope_apply`` (out may be x: in place)."""
+def rope_apply(x, rope_base: float, out=None, stream=None, rotary_dim=None, interleaved: bool = False):
+    """y = RoPE(x) for x [B, N, H, d] through ``attnfuse_rope_apply`` (out may be x: in place);
+    ``attnfuse_rope_apply_ex`` for a RoPE variant."""
     B, N, H, d = x.shape
     if not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA tensor")
     if out is None:
         out = torch.empty_like(x)
-    _check(load().attnfuse_rope_apply(_ptr(x), _ptr(out), B, N, H, d, float(rope_base), DTYPES[x.dtype],
-                                      _stream_ptr(stream)))
+    opts = _opts(rotary_dim, interleaved)
+    if opts is None:
+        _check(load().attnfuse_rope_apply(_ptr(x), _ptr(out), B, N, H, d, float(rope_base), DTYPES[x.dtype],
+                                          _stream_ptr(stream)))
+    else:
+        _check(load().attnfuse_rope_apply_ex(_ptr(x), _ptr(out), B, N, H, d, float(rope_base), DTYPES[x.dtype],
+                                             ctypes.byref(opts), _stream_ptr(stream)))
     return out
 
 

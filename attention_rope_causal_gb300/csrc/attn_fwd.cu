@@ -318,6 +318,38 @@ __device__ __forceinline__ void rotate_tile(uint32_t tile, int r0, int ck, RopeC
   }
 }
 
+// Byte offset, inside a 128-row tile of 128-byte swizzled boxes, of 16-byte chunk c (elements
+// [8c, 8c + 8)) of row r: box c / 8, logical chunk c % 8 stored at physical chunk (c % 8) ^ (r & 7).
+__device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
+  return (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)r * 128u + (uint32_t)((((c & 7) ^ (r & 7))) * 16);
+}
+
+// rotate_tile for the RoPE variants: the thread's chunk pair ck works only if ck < R (= rotary_dim
+// / 16); its chunks are ck and ck + R (pairs (k, k + rotary_dim/2)) or the adjacent 2 ck, 2 ck + 1
+// (pairs (2k, 2k + 1)), with frequencies 8 ck .. 8 ck + 7 either way.  Same carried cos/sin walk.
+template <int D, bool BF16>
+__device__ __forceinline__ void rotate_tile_variant(uint32_t tile, int r0, int ck, RopeCS8& cs, const RopeCS8& step,
+                                                    int R, bool interleaved) {
+  constexpr int PASSES = RotGeom<D>::PASSES, RS = RotGeom<D>::RS;
+  if (ck >= R) return;
+  const int ca = interleaved ? 2 * ck : ck, cb = interleaved ? 2 * ck + 1 : ck + R;
+#pragma unroll
+  for (int pass = 0; pass < PASSES; ++pass) {
+    const int row = r0 + pass * RS;
+    const uint32_t xo = chunk_offset(row, ca), yo = chunk_offset(row, cb);
+    uint4 x = ptx::lds128(tile + xo), y = ptx::lds128(tile + yo);
+    if (interleaved) {
+      rope_rotate_chunk_il_cs8<BF16>(x, cs, 0);
+      rope_rotate_chunk_il_cs8<BF16>(y, cs, 1);
+    } else {
+      rope_rotate_chunk_cs8<BF16>(x, y, cs);
+    }
+    rope_cs8_advance(cs, step);
+    ptx::sts128(tile + xo, x);
+    ptx::sts128(tile + yo, y);
+  }
+}
+
 // ---- persistent schedule -------------------------------------------------------------------
 // Work unit = (b, head pair, 128-row block t) or (b, h, 256-row block t), numbered longest-first
 // (t descending).  CTA c of G
@@ -374,7 +406,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
       break;                                                                     \
     else if (const Unit U = decode_unit(u_, p); true)
 
-template <int D, bool ROTATE, bool BF16>
+template <int D, bool ROTATE, bool BF16, bool VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
@@ -680,7 +712,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ks = gk % KST, kph = (gk / KST) & 1;
             if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
             ++gk;
-            rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
+            // Half-split over all d entries: the tuned path; other RoPE forms (VARIANT kernels) take
+            // rotate_tile_variant.
+            if constexpr (VARIANT)
+              rotate_tile_variant<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step, p.rot_chunks, p.interleaved != 0);
+            else
+              rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
             if (i == 0) {
@@ -689,7 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
                 RopeCS8 qcs;
                 rope_cs8_exact((uint32_t)(U.row(tq) + r0), sfreq, sfreq + 64, ck * 8, qcs);
-                rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
+                if constexpr (VARIANT)
+                  rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0);
+                else
+                  rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
               }
               ptx::fence_proxy_async_smem();
               ptx::mbar_arrive(bar_addr(ctl.q_ready));
@@ -732,9 +772,9 @@ __global__ void diag_wait_timeout_kernel(unsigned long long timeout_ns) {
   __syncthreads();
 }
 
-template <int D, bool ROTATE, bool BF16>
+template <int D, bool ROTATE, bool BF16, bool VARIANT>
 cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t stream, const char** why) {
-  auto kernel = attn_fwd_kernel<D, ROTATE, BF16>;
+  auto kernel = attn_fwd_kernel<D, ROTATE, BF16, VARIANT>;
   constexpr int kMaxDevices = 64;
   static int configured[kMaxDevices] = {0};
   static int sm_count[kMaxDevices] = {0};
@@ -772,12 +812,25 @@ cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t s
 cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
                             cudaStream_t stream, const char** why) {
   if (p.total_units <= 0) return cudaSuccess;
+  const bool variant = rotate && !(p.rot_chunks == d / 16 && p.interleaved == 0);
   if (d == 128) {
-    if (rotate) return bf16 ? launch_one<128, true, true>(maps, p, stream, why) : launch_one<128, true, false>(maps, p, stream, why);
-    return bf16 ? launch_one<128, false, true>(maps, p, stream, why) : launch_one<128, false, false>(maps, p, stream, why);
+    if (variant)
+      return bf16 ? launch_one<128, true, true, true>(maps, p, stream, why)
+                  : launch_one<128, true, false, true>(maps, p, stream, why);
+    if (rotate)
+      return bf16 ? launch_one<128, true, true, false>(maps, p, stream, why)
+                  : launch_one<128, true, false, false>(maps, p, stream, why);
+    return bf16 ? launch_one<128, false, true, false>(maps, p, stream, why)
+                : launch_one<128, false, false, false>(maps, p, stream, why);
   }
-  if (rotate) return bf16 ? launch_one<64, true, true>(maps, p, stream, why) : launch_one<64, true, false>(maps, p, stream, why);
-  return bf16 ? launch_one<64, false, true>(maps, p, stream, why) : launch_one<64, false, false>(maps, p, stream, why);
+  if (variant)
+    return bf16 ? launch_one<64, true, true, true>(maps, p, stream, why)
+                : launch_one<64, true, false, true>(maps, p, stream, why);
+  if (rotate)
+    return bf16 ? launch_one<64, true, true, false>(maps, p, stream, why)
+                : launch_one<64, true, false, false>(maps, p, stream, why);
+  return bf16 ? launch_one<64, false, true, false>(maps, p, stream, why)
+              : launch_one<64, false, false, false>(maps, p, stream, why);
 }
 
 cudaError_t read_and_clear_device_status(unsigned int* value, cudaStream_t stream) {

@@ -17,11 +17,11 @@ namespace attnfuse {
 
 // F_k = round(theta_k / (2 pi) * 2^64): frequency of pair k in turns per position, as a 64-bit
 // fixed-point fraction (theta_k <= 1, so F_k < 2^61.4).  theta_k = base^(-2k/d) in double.
-void rope_freqs_host(int d, double base, RopeFreqs* f) {
+void rope_freqs_host(int r, double base, RopeFreqs* f) {
   std::memset(f, 0, sizeof(*f));
   const double two_pi = 6.283185307179586476925286766559;
-  for (int k = 0; k < d / 2 && k < kMaxHalfDim; ++k) {
-    const double theta = std::pow(base, -2.0 * (double)k / (double)d);
+  for (int k = 0; k < r / 2 && k < kMaxHalfDim; ++k) {
+    const double theta = std::pow(base, -2.0 * (double)k / (double)r);
     const double scaled = std::ldexp(theta / two_pi, 64);
     const uint64_t F = (uint64_t)std::llround(scaled);  // < 2^62: fits a signed 64-bit round
     f->lo[k] = (uint32_t)(F & 0xFFFFFFFFull);
@@ -113,6 +113,17 @@ attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, i
 
 size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N * (size_t)H * (size_t)d * 2u; }
 
+// Resolves a RoPE variant: rotary dimension r (0 -> d) and pairing; checks r in [16, d], r % 16 == 0.
+attnfuse_status_t resolve_opts(const attnfuse_rope_opts_t* o, int d, int* r, int* interleaved) {
+  *r = (o && o->rotary_dim) ? o->rotary_dim : d;
+  *interleaved = o ? o->interleaved : 0;
+  if (*r < 16 || *r > d || (*r % 16) != 0)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rotary_dim=%d must be 0 or a multiple of 16 in [16, d=%d]", *r, d);
+  if (*interleaved != 0 && *interleaved != 1)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "interleaved=%d must be 0 or 1", *interleaved);
+  return ATTNFUSE_OK;
+}
+
 attnfuse_status_t validate_fwd(const void* q, const void* k, const void* v, const void* out, const float* lse, int B,
                                int Hq, int Hkv, int N, int d, double base, attnfuse_mode_t mode,
                                attnfuse_dtype_t dtype) {
@@ -185,6 +196,11 @@ size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_m
 
 attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int H, int d, double rope_base,
                                       attnfuse_dtype_t dtype, void* stream) {
+  return attnfuse_rope_apply_ex(x, y, B, N, H, d, rope_base, dtype, nullptr, stream);
+}
+
+attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, int H, int d, double rope_base,
+                                         attnfuse_dtype_t dtype, const attnfuse_rope_opts_t* opts, void* stream) {
   g_err[0] = '\0';
   if (!x || !y) return fail(ATTNFUSE_ERR_INVALID_ARG, "x and y must be non-null");
   if (B < 1 || N < 1 || H < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "B, N, H must be >= 1");
@@ -197,6 +213,8 @@ attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int 
   const char* xs = static_cast<const char*>(x);
   const char* ys = static_cast<const char*>(y);
   if (xs != ys && xs < ys + bytes && ys < xs + bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "x and y overlap without being equal");
+  int rdim = 0, il = 0;
+  if ((st = resolve_opts(opts, d, &rdim, &il)) != ATTNFUSE_OK) return st;
   if ((st = check_device()) != ATTNFUSE_OK) return st;
 
   RopeApplyParams p;
@@ -209,7 +227,9 @@ attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int 
   p.N = N;
   p.tokens = (long long)B * N;
   p.groups_total = p.job[0].groups;
-  rope_freqs_host(d, rope_base, &p.freqs);
+  p.rot_chunks = rdim / 16;
+  p.interleaved = il;
+  rope_freqs_host(rdim, rope_base, &p.freqs);
   cudaError_t e = launch_rope_apply(p, d, dtype == ATTNFUSE_BF16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rope_apply launch");
   return ATTNFUSE_OK;
@@ -219,9 +239,20 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
                                            int Hq, int Hkv, int N, int d, double rope_base, attnfuse_mode_t mode,
                                            attnfuse_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                            void* stream) {
+  return attnfuse_rope_causal_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, mode, dtype, workspace,
+                                     workspace_bytes, nullptr, stream);
+}
+
+attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                                              int B, int Hq, int Hkv, int N, int d, double rope_base,
+                                              attnfuse_mode_t mode, attnfuse_dtype_t dtype, void* workspace,
+                                              size_t workspace_bytes, const attnfuse_rope_opts_t* opts,
+                                              void* stream) {
   g_err[0] = '\0';
   attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, mode, dtype);
   if (st != ATTNFUSE_OK) return st;
+  int rdim = 0, il = 0;
+  if ((st = resolve_opts(opts, d, &rdim, &il)) != ATTNFUSE_OK) return st;
   if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, N, d, dtype);
   const size_t need = attnfuse_workspace_bytes(B, Hq, Hkv, N, d, mode, dtype);
   if (workspace) {
@@ -248,7 +279,9 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
   p.lse = lse;
   p.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
   p.timeout_ns = kTimeoutNs;
-  rope_freqs_host(d, rope_base, &p.freqs);
+  p.rot_chunks = rdim / 16;
+  p.interleaved = il;
+  rope_freqs_host(rdim, rope_base, &p.freqs);
 
   const void* qa = q;
   const void* ka = k;
@@ -273,6 +306,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
     rp.N = N;
     rp.tokens = (long long)B * N;
     rp.groups_total = rp.job[0].groups + rp.job[1].groups;
+    rp.rot_chunks = p.rot_chunks;
+    rp.interleaved = p.interleaved;
     rp.freqs = p.freqs;
     cudaError_t e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
     if (e != cudaSuccess) {

@@ -26,7 +26,9 @@ struct RopeApplyParams {
   int N;
   long long tokens;  // B * N
   int groups_total;  // job[0].groups + (njobs > 1 ? job[1].groups : 0)
-  RopeFreqs freqs;
+  int rot_chunks;    // rotary_dim / 16: item ck < rot_chunks rotates (frequencies 8 ck .. 8 ck + 7)
+  int interleaved;   // 0: pairs (k, k + rotary_dim/2); 1: pairs (2k, 2k + 1)
+  RopeFreqs freqs;   // F_k for k < rotary_dim / 2
 };
 
 cudaError_t launch_rope_apply(const RopeApplyParams& p, int d, bool bf16, cudaStream_t stream);
@@ -42,6 +44,8 @@ struct AttnParams {
   void* out;         // [B, N, Hq, d]
   float* lse;        // [B, Hq, N] or nullptr
   float scale_log2;  // log2(e) / sqrt(d)
+  int rot_chunks;    // rotary_dim / 16 (fused mode: rotation thread chunk ck < rot_chunks works)
+  int interleaved;   // 0: pairs (k, k + rotary_dim/2); 1: pairs (2k, 2k + 1)
   unsigned long long timeout_ns;  // limit on any single barrier wait
   RopeFreqs freqs;
 };
@@ -60,8 +64,8 @@ cudaError_t read_and_clear_device_status(unsigned int* value, cudaStream_t strea
 // Launches one CTA that waits, for at most timeout_ns, on a barrier nothing arrives on.
 cudaError_t launch_diag_wait_timeout(unsigned long long timeout_ns, cudaStream_t stream);
 
-// Fills F_k = round(theta_k / (2 pi) * 2^64), theta_k = base^(-2k/d).
-void rope_freqs_host(int d, double base, RopeFreqs* f);
+// Fills F_k = round(theta_k / (2 pi) * 2^64), theta_k = base^(-2k/r), k < r/2 (r = rotary dimension).
+void rope_freqs_host(int r, double base, RopeFreqs* f);
 
 // Sets the calling thread's attnfuse_last_error() message (printf-style).
 void set_last_error(const char* fmt, ...);

@@ -122,6 +122,20 @@ __device__ __forceinline__ void rope_rotate_chunk(uint4& xv, uint4& yv, const fl
   }
 }
 
+// Interleaved pairing: rotate the 4 pairs (2k, 2k+1) held in one 16-byte chunk, pair w of the chunk
+// with cos/sin c[w], s[w] (same arithmetic per pair as rope_pair).
+template <bool BF16>
+__device__ __forceinline__ void rope_rotate_chunk_il(uint4& v, const float* c, const float* s) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float e, o, a, b;
+    Pack<BF16>::unpack(w[j], e, o);
+    rope_pair(e, o, c[j], s[j], a, b);
+    w[j] = Pack<BF16>::pack(a, b);
+  }
+}
+
 // ---- packed form: cos/sin of 8 consecutive frequencies as 4 fp32 pairs --------------------------
 
 struct RopeCS8 {
@@ -180,6 +194,18 @@ __device__ __forceinline__ void rope_rotate_chunk_cs8(uint4& xv, uint4& yv, cons
     xw[j] = Pack<BF16>::pack(a0, a1);
     yw[j] = Pack<BF16>::pack(b0, b1);
   }
+}
+
+// Interleaved pairing with carried cos/sin: chunk `half` (0 or 1) of the thread's two adjacent
+// chunks holds the pairs of frequencies 4 half .. 4 half + 3 of cs.
+template <bool BF16>
+__device__ __forceinline__ void rope_rotate_chunk_il_cs8(uint4& v, const RopeCS8& cs, int half) {
+  float c[4], s[4];
+  ptx::f2_unpack(cs.c[2 * half], c[0], c[1]);
+  ptx::f2_unpack(cs.c[2 * half + 1], c[2], c[3]);
+  ptx::f2_unpack(cs.s[2 * half], s[0], s[1]);
+  ptx::f2_unpack(cs.s[2 * half + 1], s[2], s[3]);
+  rope_rotate_chunk_il<BF16>(v, c, s);
 }
 
 }  // namespace attnfuse

@@ -5,11 +5,12 @@
 // bandwidth, fused rotation costs compute).
 //
 // It is an elementwise stream, bounded by HBM bandwidth: every element is read once and written
-// once.  Work item = (token, head group of up to kHeadsPerGroup heads, 16-byte chunk index ck).
-// Eight (d = 128) or four (d = 64) consecutive threads cover the two contiguous half-rows of one
-// head, so each warp-wide 16-byte load or store touches whole 128-byte segments.  A thread
-// computes the cos/sin of its 8 frequencies once and applies them to every head of its group,
-// keeping 4 heads (8 loads of 16 bytes) in flight.
+// once.  Work item = (token, head group of up to kHeadsPerGroup heads, item index ck < d/16), each
+// item two 16-byte chunks of a head row.  Consecutive threads cover contiguous 16-byte chunks, so
+// each warp-wide 16-byte load or store touches whole 128-byte segments.  A thread computes the
+// cos/sin of its 8 frequencies once and applies them to every head of its group, keeping 4 heads
+// (8 loads of 16 bytes) in flight.  RoPE variants: only the first rotary_dim entries rotate (the
+// rest are copied), in half-split or interleaved pairs.
 #include <cuda_runtime.h>
 
 #include "attnfuse_internal.h"
@@ -23,8 +24,7 @@ constexpr int kThreads = 256;
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads) rope_apply_kernel(const __grid_constant__ RopeApplyParams p) {
-  constexpr int HALF = D / 2;
-  constexpr int NCH = HALF / 8;  // 16-byte chunks per half-row
+  constexpr int NCH = D / 16;  // work items per head row; each covers two 16-byte chunks
   const long long item = (long long)blockIdx.x * kThreads + threadIdx.x;
   const long long per_token = (long long)p.groups_total * NCH;
   const long long token = item / per_token;
@@ -43,33 +43,52 @@ __global__ void __launch_bounds__(kThreads) rope_apply_kernel(const __grid_const
   const int h0 = g * kHeadsPerGroup;
   const int nh = min(kHeadsPerGroup, jb.H - h0);
 
+  // Chunks (16 bytes = 8 elements) of a row: the first 2R = rotary_dim / 8 are rotated.  Item ck < R
+  // rotates, with frequencies 8 ck .. 8 ck + 7, either chunks ck and ck + R (pairs (k, k + r/2)) or
+  // the adjacent chunks 2 ck, 2 ck + 1 (pairs (2k, 2k + 1)).  Items ck >= R copy chunks 2 ck and
+  // 2 ck + 1 when the output is not the input.
+  const int R = p.rot_chunks;
+  const bool rotate = ck < R;
+  if (!rotate && jb.x == jb.y) return;
+  const int ca = rotate && !p.interleaved ? ck : 2 * ck;
+  const int cb = rotate && !p.interleaved ? ck + R : 2 * ck + 1;
+
   float c[8], s[8];
+  if (rotate) {
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const int k = ck * 8 + t;
-    rope_cs(pos, p.freqs.lo[k], p.freqs.hi[k], c[t], s[t]);
+    for (int t = 0; t < 8; ++t) {
+      const int k = ck * 8 + t;
+      rope_cs(pos, p.freqs.lo[k], p.freqs.hi[k], c[t], s[t]);
+    }
   }
 
   const size_t row_bytes = (size_t)D * 2;
-  const size_t off0 = ((size_t)token * jb.H + h0) * row_bytes + (size_t)ck * 16;
+  const size_t off0 = ((size_t)token * jb.H + h0) * row_bytes;
   const char* xb = reinterpret_cast<const char*>(jb.x) + off0;
   char* yb = reinterpret_cast<char*>(jb.y) + off0;
 
   for (int h = 0; h < nh; h += 4) {
-    uint4 xv[4], yv[4];
+    uint4 av[4], bv[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (h + u < nh) {
-        xv[u] = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(h + u) * row_bytes));
-        yv[u] = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(h + u) * row_bytes + HALF * 2));
+        av[u] = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(h + u) * row_bytes + ca * 16));
+        bv[u] = __ldg(reinterpret_cast<const uint4*>(xb + (size_t)(h + u) * row_bytes + cb * 16));
       }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (h + u < nh) {
-        rope_rotate_chunk<BF16>(xv[u], yv[u], c, s);
-        *reinterpret_cast<uint4*>(yb + (size_t)(h + u) * row_bytes) = xv[u];
-        *reinterpret_cast<uint4*>(yb + (size_t)(h + u) * row_bytes + HALF * 2) = yv[u];
+        if (rotate) {
+          if (p.interleaved) {
+            rope_rotate_chunk_il<BF16>(av[u], c, s);
+            rope_rotate_chunk_il<BF16>(bv[u], c + 4, s + 4);
+          } else {
+            rope_rotate_chunk<BF16>(av[u], bv[u], c, s);
+          }
+        }
+        *reinterpret_cast<uint4*>(yb + (size_t)(h + u) * row_bytes + ca * 16) = av[u];
+        *reinterpret_cast<uint4*>(yb + (size_t)(h + u) * row_bytes + cb * 16) = bv[u];
       }
     }
   }

@@ -96,6 +96,33 @@ attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int 
                                       attnfuse_dtype_t dtype, void* stream);
 
 /*
+ * RoPE variants (extensions of the rotation the pages name, "AttnFuse Makes RoPE a First-Class
+ * Attention Compilation Operation", paragraph 1; the pages fix no pairing or rotary dimension).
+ *   rotary_dim: only entries [0, r) of each head vector are rotated, with theta_k = base^(-2k/r),
+ *               k < r/2; entries [r, d) pass through unchanged.  0 means r = d.  Otherwise
+ *               16 <= r <= d and r a multiple of 16.
+ *   interleaved: 0 pairs (k, k + r/2) (half-split, the default form); 1 pairs (2k, 2k + 1).
+ * A NULL pointer to the struct means { 0, 0 }: the functions without _ex.
+ */
+typedef struct {
+  int rotary_dim;
+  int interleaved;
+} attnfuse_rope_opts_t;
+
+/* attnfuse_rope_causal_fwd with a RoPE variant (opts may be NULL); same arguments otherwise.
+ * Invalid opts give ATTNFUSE_ERR_INVALID_ARG. */
+attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                                              int B, int Hq, int Hkv, int N, int d, double rope_base,
+                                              attnfuse_mode_t mode, attnfuse_dtype_t dtype, void* workspace,
+                                              size_t workspace_bytes, const attnfuse_rope_opts_t* opts,
+                                              void* stream);
+
+/* attnfuse_rope_apply with a RoPE variant (opts may be NULL).  Out of place, the entries that are
+ * not rotated are copied to y; in place they are left as they are. */
+attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, int H, int d, double rope_base,
+                                         attnfuse_dtype_t dtype, const attnfuse_rope_opts_t* opts, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word.  Returns
  * ATTNFUSE_ERR_TIMEOUT if a kernel's barrier wait ran out since the last read, ATTNFUSE_ERR_CUDA if
  * synchronising failed (e.g. a device fault), ATTNFUSE_OK otherwise.

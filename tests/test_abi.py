@@ -100,6 +100,15 @@ def test_auto_mode_workspace_is_that_of_the_selected_mode(lib):
     assert binding.select_mode(2, 16, 16, 2048, 64) == "fused"
 
 
+@pytest.mark.parametrize("r,il,status", [(8, 0, 1), (24, 0, 1), (80, 1, 1), (-16, 0, 1), (64, 2, 1), (64, -1, 1)])
+def test_variant_options_are_checked_before_the_device(lib, r, il, status):
+    opts = binding.RopeOpts(r, il)
+    assert lib.attnfuse_rope_causal_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 128, 64, 1e4, 0, 0, None, 0,
+                                           ctypes.byref(opts), None) == status
+    assert lib.attnfuse_rope_apply_ex(FAKE, FAKE, 1, 16, 2, 64, 1e4, 0, ctypes.byref(opts), None) == status
+    assert b"rotary_dim" in lib.attnfuse_last_error() or b"interleaved" in lib.attnfuse_last_error()
+
+
 def test_valid_call_without_gpu_fails_cleanly(lib):
     import torch
     if torch.cuda.is_available():
