@@ -13,7 +13,10 @@ ctypes.  What it computes, and the passages it follows, are stated in that file'
 * causal softmax attention (same report, paragraph 2: causality and softmax building blocks),
   scale 1/sqrt(d), natural-log log-sum-exp per row, GQA head h -> kv head floor(h*Hkv/Hq);
 * RoPE variants (``rotary_dim``, ``interleaved``): only the first r entries rotated with
-  theta_k = base^(-2k/r), and adjacent pairs (2k, 2k+1) instead of (k, k+r/2).
+  theta_k = base^(-2k/r), and adjacent pairs (2k, 2k+1) instead of (k, k+r/2);
+* more keys than queries (k, v with Nk >= Nq tokens: the queries are the last Nq, so query i sees
+  keys j <= Nk - Nq + i) and explicit rotation positions (``q_positions``, ``k_positions``), which
+  change the angles only.
 """
 from __future__ import annotations
 
@@ -69,6 +72,12 @@ def _load():
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
                                                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.orc_rope_causal_kv.restype = ctypes.c_int
+            lib.orc_rope_causal_kv.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -141,15 +150,29 @@ def rope_rotate_bnhd(x, base: float, threads: int | None = None, rotary_dim: int
     return rope_rotate(x, base, positions=pos, threads=threads, rotary_dim=rotary_dim, interleaved=interleaved)
 
 
+def _positions(pos, B: int, n: int, what: str):
+    if pos is None:
+        return None
+    if hasattr(pos, "detach"):
+        pos = pos.detach().cpu().numpy()
+    a = np.ascontiguousarray(np.asarray(pos, dtype=np.float64).reshape(-1))
+    if a.size != B * n:
+        raise ValueError(f"{what} has {a.size} entries, expected B * {n} = {B * n}")
+    return a
+
+
 def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None, rotary_dim: int | None = None,
-                interleaved: bool = False):
+                interleaved: bool = False, q_positions=None, k_positions=None):
     """Causal softmax attention with RoPE on q and k.
 
     rotary_dim (default d) and interleaved select the RoPE variant (see :func:`rope_rotate`).
 
-    q: [B, N, Hq, d]; k, v: [B, N, Hkv, d] (same dtype: bf16/fp16 torch tensors, fp16 or fp64 arrays).
-    rows: optional 1-D sequence of query positions to evaluate (default: all N in order).
-    Returns (out [B, R, Hq, d] float64, lse [B, Hq, R] float64) with R = len(rows) or N.
+    q: [B, Nq, Hq, d]; k, v: [B, Nk, Hkv, d] with Nk >= Nq (same dtype: bf16/fp16 torch tensors, fp16 or
+    fp64 arrays).  The queries are the last Nq of the Nk tokens: query i sees keys j <= (Nk - Nq) + i.
+    q_positions [B, Nq] / k_positions [B, Nk] (integers; default (Nk - Nq) + i and j) are the rotation
+    positions; they change the angles only, never the mask.
+    rows: optional 1-D sequence of query rows to evaluate (default: all Nq in order).
+    Returns (out [B, R, Hq, d] float64, lse [B, Hq, R] float64) with R = len(rows) or Nq.
     """
     qr, dq = _as_raw(q)
     kr, dk = _as_raw(k)
@@ -159,11 +182,15 @@ def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None, rot
     if qr.ndim != 4 or kr.ndim != 4 or vr.ndim != 4:
         raise ValueError("q, k, v must be 4-D [B, N, H, d]")
     B, N, Hq, d = qr.shape
-    Hkv = kr.shape[2]
-    if kr.shape != (B, N, Hkv, d) or vr.shape != (B, N, Hkv, d):
-        raise ValueError("k and v must be [B, N, Hkv, d] matching q")
+    Nk, Hkv = kr.shape[1], kr.shape[2]
+    if kr.shape != (B, Nk, Hkv, d) or vr.shape != (B, Nk, Hkv, d):
+        raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
+    if Nk < N:
+        raise ValueError("k and v must hold at least as many tokens as q")
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
+    qp = _positions(q_positions, B, N, "q_positions")
+    kp = _positions(k_positions, B, Nk, "k_positions")
     if rows is None:
         sel_ptr, n_sel, sel = None, N, None
     else:
@@ -175,6 +202,14 @@ def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None, rot
     lse = np.zeros((B, Hq, n_sel), dtype=np.float64)
     if n_sel == 0:
         return out, lse
+    r = d if rotary_dim is None else int(rotary_dim)
+    rc = _load().orc_rope_causal_kv(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, dq, B, Hq, Hkv, N, Nk, d, r,
+                                    int(bool(interleaved)), float(base), None if qp is None else qp.ctypes.data,
+                                    None if kp is None else kp.ctypes.data, sel_ptr, n_sel, out.ctypes.data,
+                                    lse.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("orc_rope_causal_kv failed")
+    return out, lse
     r = d if rotary_dim is None else int(rotary_dim)
     rc = _load().orc_rope_causal_ex(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, dq, B, Hq, Hkv, N, d, r,
                                     int(bool(interleaved)), float(base), sel_ptr, n_sel, out.ctypes.data,

@@ -30,7 +30,16 @@
  *       lse_i = max_j s_ij + ln sum_j exp(s_ij - max_j s_ij)     (natural log)
  *   GQA: query head h reads key/value head floor(h / (Hq/Hkv)).
  *
- * Layouts (row-major, contiguous): q, out [B, N, Hq, d]; k, v [B, N, Hkv, d]; lse [B, Hq, N].
+ *   Key length and positions (the "_kv" entry point).  The pages fix neither; this library takes
+ *   the plainest general reading of "causal" when there are Nk >= Nq keys (a prefill that extends
+ *   a cache of Nk - Nq earlier tokens): the Nq queries are the last Nq of the Nk tokens, so query i
+ *   sees keys j <= (Nk - Nq) + i.  The rotation position of query i is (Nk - Nq) + i and that of key
+ *   j is j, unless explicit per-token positions are given (any integers, one per query and one per
+ *   key); positions change only the angles, never the mask.  Nk == Nq with default positions is the
+ *   definition above.
+ *
+ * Layouts (row-major, contiguous): q, out [B, N, Hq, d]; k, v [B, N, Hkv, d]; lse [B, Hq, N]
+ * (with the "_kv" entry: q, out [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d]; lse [B, Hq, Nq]).
  * Inputs may be raw bf16 or fp16 bit patterns (decoded exactly to double here) or doubles.
  */
 #include <math.h>
@@ -198,10 +207,11 @@ int orc_rope_rotate(const void *x, int dtype, int64_t rows, int H, int d, const 
 typedef struct {
   const void *q, *v;
   int dtype;
-  int B, Hq, Hkv, N, d;
+  int B, Hq, Hkv, Nq, Nk, d;
   rope_form_t form;
   const double *theta;
-  const double *krot; /* [B, N, Hkv, d] rotated keys */
+  const double *qpos; /* [B, Nq] rotation positions of the queries, or NULL: (Nk - Nq) + i */
+  const double *krot; /* [B, Nk, Hkv, d] rotated keys */
   const int64_t *sel;
   int64_t n_sel;
   double *out, *lse;
@@ -212,23 +222,27 @@ typedef struct {
   int dtype;
   int Hkv;
   rope_form_t form;
-  int N;
+  int Nk;
   const double *theta;
+  const double *kpos; /* [B, Nk] rotation positions of the keys, or NULL: j */
   double *krot;
 } krot_ctx_t;
 
-static void krot_item(void *vctx, int64_t bn, double *scratch) {
+/* One item = one key token (b, j): rotate its Hkv head vectors. */
+static void krot_item(void *vctx, int64_t bj, double *scratch) {
   krot_ctx_t *c = (krot_ctx_t *)vctx;
-  int n = (int)(bn % c->N);
+  int j = (int)(bj % c->Nk);
+  double pos = c->kpos ? c->kpos[bj] : (double)j;
   int d = c->form.d;
   for (int h = 0; h < c->Hkv; ++h) {
-    size_t base = ((size_t)bn * c->Hkv + h) * d;
+    size_t base = ((size_t)bj * c->Hkv + h) * d;
     for (int e = 0; e < d; ++e) scratch[e] = load_elem(c->k, c->dtype, base + e);
-    rope_rotate_vec(scratch, c->krot + base, c->form, (double)n, c->theta);
+    rope_rotate_vec(scratch, c->krot + base, c->form, pos, c->theta);
   }
 }
 
-/* One item = one (b, h, selected row). scratch holds: raw q (d), rotated q (d), scores (N). */
+/* One item = one (b, h, selected query row i). scratch holds: raw q (d), rotated q (d), scores (Nk).
+ * Query i sees keys j <= last = (Nk - Nq) + i. */
 static void attn_item(void *vctx, int64_t item, double *scratch) {
   attn_ctx_t *c = (attn_ctx_t *)vctx;
   int64_t s = item % c->n_sel;
@@ -240,47 +254,52 @@ static void attn_item(void *vctx, int64_t item, double *scratch) {
   int d = c->d;
   double *qraw = scratch, *qrot = scratch + d, *score = scratch + 2 * d;
 
-  size_t qbase = (((size_t)b * c->N + (size_t)i) * c->Hq + h) * d;
+  int64_t last = (int64_t)(c->Nk - c->Nq) + i;
+  size_t qbase = (((size_t)b * c->Nq + (size_t)i) * c->Hq + h) * d;
   for (int e = 0; e < d; ++e) qraw[e] = load_elem(c->q, c->dtype, qbase + e);
-  rope_rotate_vec(qraw, qrot, c->form, (double)i, c->theta);
+  double qp = c->qpos ? c->qpos[(size_t)b * c->Nq + (size_t)i] : (double)last;
+  rope_rotate_vec(qraw, qrot, c->form, qp, c->theta);
 
   double scale = 1.0 / sqrt((double)d);
   double mx = -INFINITY;
-  for (int64_t j = 0; j <= i; ++j) { /* causal: keys j <= i only */
-    const double *kr = c->krot + (((size_t)b * c->N + (size_t)j) * c->Hkv + hk) * d;
+  for (int64_t j = 0; j <= last; ++j) { /* causal: keys j <= last only */
+    const double *kr = c->krot + (((size_t)b * c->Nk + (size_t)j) * c->Hkv + hk) * d;
     double dot = 0.0;
     for (int e = 0; e < d; ++e) dot += qrot[e] * kr[e];
     score[j] = dot * scale;
     if (score[j] > mx) mx = score[j];
   }
   double denom = 0.0;
-  for (int64_t j = 0; j <= i; ++j) {
+  for (int64_t j = 0; j <= last; ++j) {
     score[j] = exp(score[j] - mx);
     denom += score[j];
   }
   double *o = c->out + (((size_t)b * c->n_sel + (size_t)s) * c->Hq + h) * d;
   for (int e = 0; e < d; ++e) o[e] = 0.0;
-  for (int64_t j = 0; j <= i; ++j) {
+  for (int64_t j = 0; j <= last; ++j) {
     double p = score[j] / denom;
-    size_t vbase = (((size_t)b * c->N + (size_t)j) * c->Hkv + hk) * d;
+    size_t vbase = (((size_t)b * c->Nk + (size_t)j) * c->Hkv + hk) * d;
     for (int e = 0; e < d; ++e) o[e] += p * load_elem(c->v, c->dtype, vbase + e);
   }
   if (c->lse) c->lse[((size_t)b * c->Hq + h) * c->n_sel + (size_t)s] = mx + log(denom);
 }
 
-int orc_rope_causal_ex(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
-                       int rotary_dim, int interleaved, double base, const int64_t *sel_rows, int64_t n_sel,
-                       double *out, double *lse, int nthreads) {
+/* Public entry 3: the general form.  Nq queries, the last Nq of Nk >= Nq tokens; q_pos [B, Nq]
+ * and k_pos [B, Nk] are the rotation positions (either may be NULL for the defaults). */
+int orc_rope_causal_kv(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int Nq, int Nk,
+                       int d, int rotary_dim, int interleaved, double base, const double *q_pos, const double *k_pos,
+                       const int64_t *sel_rows, int64_t n_sel, double *out, double *lse, int nthreads) {
   rope_form_t f = {d, rotary_dim, interleaved};
-  if (!q || !k || !v || !out || B < 1 || Hq < 1 || Hkv < 1 || N < 1 || !form_ok(f) || (Hq % Hkv) != 0) return -1;
-  if (!sel_rows) n_sel = N;
+  if (!q || !k || !v || !out || B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < Nq || !form_ok(f) || (Hq % Hkv) != 0)
+    return -1;
+  if (!sel_rows) n_sel = Nq;
   if (n_sel < 0) return -1;
   if (sel_rows)
     for (int64_t s = 0; s < n_sel; ++s)
-      if (sel_rows[s] < 0 || sel_rows[s] >= N) return -1;
+      if (sel_rows[s] < 0 || sel_rows[s] >= Nq) return -1;
 
   double *theta = (double *)malloc(sizeof(double) * (size_t)(f.r / 2));
-  double *krot = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N * (size_t)Hkv * (size_t)d);
+  double *krot = (double *)malloc(sizeof(double) * (size_t)B * (size_t)Nk * (size_t)Hkv * (size_t)d);
   if (!theta || !krot) {
     free(theta);
     free(krot);
@@ -288,18 +307,25 @@ int orc_rope_causal_ex(const void *q, const void *k, const void *v, int dtype, i
   }
   rope_frequencies(f.r, base, theta);
 
-  krot_ctx_t kctx = {k, dtype, Hkv, f, N, theta, krot};
-  orc_pool_t kpool = {krot_item, &kctx, (int64_t)B * N, 0, (size_t)d, 0};
+  krot_ctx_t kctx = {k, dtype, Hkv, f, Nk, theta, k_pos, krot};
+  orc_pool_t kpool = {krot_item, &kctx, (int64_t)B * Nk, 0, (size_t)d, 0};
   int rc = orc_run(&kpool, nthreads);
 
   if (rc == 0) {
-    attn_ctx_t actx = {q, v, dtype, B, Hq, Hkv, N, d, f, theta, krot, sel_rows, n_sel, out, lse};
-    orc_pool_t apool = {attn_item, &actx, (int64_t)B * Hq * n_sel, 0, (size_t)(2 * d + N), 0};
+    attn_ctx_t actx = {q, v, dtype, B, Hq, Hkv, Nq, Nk, d, f, theta, q_pos, krot, sel_rows, n_sel, out, lse};
+    orc_pool_t apool = {attn_item, &actx, (int64_t)B * Hq * n_sel, 0, (size_t)(2 * d + Nk), 0};
     rc = orc_run(&apool, nthreads);
   }
   free(theta);
   free(krot);
   return rc;
+}
+
+int orc_rope_causal_ex(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
+                       int rotary_dim, int interleaved, double base, const int64_t *sel_rows, int64_t n_sel,
+                       double *out, double *lse, int nthreads) {
+  return orc_rope_causal_kv(q, k, v, dtype, B, Hq, Hkv, N, N, d, rotary_dim, interleaved, base, NULL, NULL, sel_rows,
+                            n_sel, out, lse, nthreads);
 }
 
 int orc_rope_causal(const void *q, const void *k, const void *v, int dtype, int B, int Hq, int Hkv, int N, int d,
