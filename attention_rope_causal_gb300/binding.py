@@ -22,8 +22,10 @@ MODE_NAMES = {v: k for k, v in MODES.items()}
 DTYPES = {torch.bfloat16: ATTNFUSE_BF16, torch.float16: ATTNFUSE_FP16}
 
 class RopeOpts(ctypes.Structure):
-    """attnfuse_rope_opts_t: rotary_dim (0 = d) and interleaved (0 = half-split pairs)."""
-    _fields_ = [("rotary_dim", ctypes.c_int), ("interleaved", ctypes.c_int)]
+    """attnfuse_rope_opts_t: rotary_dim (0 = d), interleaved (0 = half-split pairs), kv_len (0 = N) and the
+    device pointers of the int32 query / key position arrays (NULL = defaults)."""
+    _fields_ = [("rotary_dim", ctypes.c_int), ("interleaved", ctypes.c_int), ("kv_len", ctypes.c_int),
+                ("q_positions", ctypes.c_void_p), ("k_positions", ctypes.c_void_p)]
 
 
 # Every function the header declares, with its ctypes signature.
@@ -41,6 +43,7 @@ _SIGNATURES = {
                                               ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.POINTER(RopeOpts),
                                               ctypes.c_void_p]),
     "attnfuse_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 7),
+    "attnfuse_workspace_bytes_ex": (ctypes.c_size_t, [ctypes.c_int] * 7 + [ctypes.POINTER(RopeOpts)]),
     "attnfuse_select_mode": (ctypes.c_int, [ctypes.c_int] * 6),
     "attnfuse_rope_causal_fwd_prerotate_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
@@ -104,8 +107,11 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def workspace_bytes(B, Hq, Hkv, N, d, mode="fused", dtype=torch.bfloat16) -> int:
-    return int(load().attnfuse_workspace_bytes(B, Hq, Hkv, N, d, MODES[mode], DTYPES[dtype]))
+def workspace_bytes(B, Hq, Hkv, N, d, mode="fused", dtype=torch.bfloat16, kv_len=None) -> int:
+    if kv_len is None:
+        return int(load().attnfuse_workspace_bytes(B, Hq, Hkv, N, d, MODES[mode], DTYPES[dtype]))
+    opts = RopeOpts(0, 0, int(kv_len), None, None)
+    return int(load().attnfuse_workspace_bytes_ex(B, Hq, Hkv, N, d, MODES[mode], DTYPES[dtype], ctypes.byref(opts)))
 
 
 def select_mode(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> str:
@@ -113,22 +119,33 @@ def select_mode(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> str:
     return MODE_NAMES[int(load().attnfuse_select_mode(B, Hq, Hkv, N, d, DTYPES[dtype]))]
 
 
-def _opts(rotary_dim, interleaved):
-    if rotary_dim is None and not interleaved:
+def _positions(pos, n_tokens: int, name: str):
+    if pos is None:
         return None
-    return RopeOpts(int(rotary_dim or 0), int(bool(interleaved)))
+    if not (pos.is_cuda and pos.dtype == torch.int32 and pos.is_contiguous() and pos.numel() == n_tokens):
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor of {n_tokens} elements")
+    return pos.data_ptr()
+
+
+def _opts(rotary_dim, interleaved, kv_len=0, q_positions=None, k_positions=None):
+    if rotary_dim is None and not interleaved and not kv_len and q_positions is None and k_positions is None:
+        return None
+    return RopeOpts(int(rotary_dim or 0), int(bool(interleaved)), int(kv_len), q_positions, k_positions)
 
 
 def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, lse=None, want_lse: bool = True,
-                    workspace=None, stream=None, rotary_dim=None, interleaved: bool = False):
-    """Causal RoPE attention forward through ``attnfuse_rope_causal_fwd`` (``_ex`` for a RoPE variant).
+                    workspace=None, stream=None, rotary_dim=None, interleaved: bool = False, q_positions=None,
+                    k_positions=None):
+    """Causal RoPE attention forward through ``attnfuse_rope_causal_fwd`` (``_ex`` with any option).
 
-    q: [B, N, Hq, d], k/v: [B, N, Hkv, d] CUDA tensors (bf16 or fp16, contiguous).
-    rotary_dim / interleaved select a RoPE variant (attnfuse_rope_opts_t).
+    q: [B, N, Hq, d], k/v: [B, Nk, Hkv, d] CUDA tensors (bf16 or fp16, contiguous), Nk >= N: the
+    queries are the last N of the Nk tokens (query i sees keys j <= Nk - N + i).
+    rotary_dim / interleaved select a RoPE variant; q_positions [B, N] / k_positions [B, Nk] (CUDA
+    int32) replace the default rotation positions Nk - N + i / j (attnfuse_rope_opts_t).
     Returns (out [B, N, Hq, d], lse [B, Hq, N] float32 or None).
     """
     B, N, Hq, d = q.shape
-    Hkv = k.shape[2]
+    Nk, Hkv = k.shape[1], k.shape[2]
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
@@ -139,7 +156,8 @@ def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, ls
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    opts = _opts(rotary_dim, interleaved)
+    opts = _opts(rotary_dim, interleaved, Nk if Nk != N else 0, _positions(q_positions, B * N, "q_positions"),
+                 _positions(k_positions, B * Nk, "k_positions"))
     if opts is None:
         _check(load().attnfuse_rope_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
                                                float(rope_base), MODES[mode], DTYPES[q.dtype], ws_ptr, ws_bytes,
@@ -151,15 +169,16 @@ def rope_causal_fwd(q, k, v, rope_base: float, mode: str = "fused", out=None, ls
     return out, lse
 
 
-def rope_apply(x, rope_base: float, out=None, stream=None, rotary_dim=None, interleaved: bool = False):
+def rope_apply(x, rope_base: float, out=None, stream=None, rotary_dim=None, interleaved: bool = False,
+               positions=None):
     """y = RoPE(x) for x [B, N, H, d] through ``attnfuse_rope_apply`` (out may be x: in place);
-    ``attnfuse_rope_apply_ex`` for a RoPE variant."""
+    ``attnfuse_rope_apply_ex`` for a RoPE variant or explicit positions ([B, N] CUDA int32)."""
     B, N, H, d = x.shape
     if not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA tensor")
     if out is None:
         out = torch.empty_like(x)
-    opts = _opts(rotary_dim, interleaved)
+    opts = _opts(rotary_dim, interleaved, 0, _positions(positions, B * N, "positions"))
     if opts is None:
         _check(load().attnfuse_rope_apply(_ptr(x), _ptr(out), B, N, H, d, float(rope_base), DTYPES[x.dtype],
                                           _stream_ptr(stream)))

@@ -2,6 +2,7 @@
 //
 // What it computes: for every batch b, query head h (KV head h / (Hq/Hkv)) and query row i,
 //   o_i = sum_{j <= i} softmax_j(q'_i . k'_j / sqrt(d)) v_j   and   lse_i = ln sum_{j<=i} exp(...),
+// (with Nk > N keys the queries are the last N tokens and the sums run over j <= Nk - N + i),
 // where q', k' are RoPE-rotated (fused mode) or were rotated beforehand (pre-rotate mode: the
 // kernel then runs with ROTATE = false on already-rotated inputs).  RoPE is a pre-multiplication
 // transform and the causal mask and softmax are building blocks of one fused kernel ("AttnFuse Makes
@@ -137,7 +138,7 @@ struct RowState {
   float sum, m, l;
 };
 template <int D, bool BF16>
-__device__ __noinline__ RowState softmax_redo(uint32_t tS, uint32_t tO, int r, bool diag, bool need, float sl2,
+__device__ __noinline__ RowState softmax_redo(uint32_t tS, uint32_t tO, int lim, bool diag, bool need, float sl2,
                                               float m_run, float l_run) {
   float mx = -INFINITY;
   for (int c = 0; c < 8; ++c) {
@@ -146,7 +147,7 @@ __device__ __noinline__ RowState softmax_redo(uint32_t tS, uint32_t tO, int r, b
     ptx::tmem_wait_ld();
 #pragma unroll
     for (int e = 0; e < 16; ++e)
-      if (!(diag && 16 * c + e > r)) mx = fmaxf(mx, __uint_as_float(t[e]));
+      if (!(diag && 16 * c + e > lim)) mx = fmaxf(mx, __uint_as_float(t[e]));
   }
   float alpha = 1.f;
   if (need) {
@@ -176,8 +177,8 @@ __device__ __noinline__ RowState softmax_redo(uint32_t tS, uint32_t tO, int r, b
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int col = 32 * c + 16 * h + 2 * e;
-        const float x0 = (diag && col > r) ? -INFINITY : fmaf(__uint_as_float(t[2 * e]), sl2, nm);
-        const float x1 = (diag && col + 1 > r) ? -INFINITY : fmaf(__uint_as_float(t[2 * e + 1]), sl2, nm);
+        const float x0 = (diag && col > lim) ? -INFINITY : fmaf(__uint_as_float(t[2 * e]), sl2, nm);
+        const float x1 = (diag && col + 1 > lim) ? -INFINITY : fmaf(__uint_as_float(t[2 * e + 1]), sl2, nm);
         const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
         sum += p0 + p1;
         pk[8 * h + e] = Pack<BF16>::pack(p0, p1);
@@ -211,6 +212,7 @@ struct __align__(8) Ctrl {
   uint32_t tmem_base;
   int abort_flag;
   int skip;
+  int q_off;  // AttnParams::q_off
 };
 static_assert(sizeof(Ctrl) <= 256, "control block");
 
@@ -346,27 +348,47 @@ __device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
 
 // rotate_tile for the RoPE variants: the thread's chunk pair ck works only if ck < R (= rotary_dim
 // / 16); its chunks are ck and ck + R (pairs (k, k + rotary_dim/2)) or the adjacent 2 ck, 2 ck + 1
-// (pairs (2k, 2k + 1)), with frequencies 8 ck .. 8 ck + 7 either way.  Same carried cos/sin walk.
+// (pairs (2k, 2k + 1)), with frequencies 8 ck .. 8 ck + 7 either way.  With pos == nullptr the
+// rows take the carried cos/sin walk of rotate_tile; otherwise row r of the tile sits at position
+// pos[r] (rows r >= nvalid, past the end of the sequence, at 0) and its cos/sin are computed exactly.
 template <int D, bool BF16>
 __device__ __forceinline__ void rotate_tile_variant(uint32_t tile, int r0, int ck, RopeCS8& cs, const RopeCS8& step,
-                                                    int R, bool interleaved) {
+                                                    int R, bool interleaved, const int32_t* pos, int nvalid,
+                                                    const uint32_t* sfreq) {
   constexpr int PASSES = RotGeom<D>::PASSES, RS = RotGeom<D>::RS;
   if (ck >= R) return;
   const int ca = interleaved ? 2 * ck : ck, cb = interleaved ? 2 * ck + 1 : ck + R;
-#pragma unroll
-  for (int pass = 0; pass < PASSES; ++pass) {
-    const int row = r0 + pass * RS;
+  auto rotate_row = [&](int row, const RopeCS8& c8) {
     const uint32_t xo = chunk_offset(row, ca), yo = chunk_offset(row, cb);
     uint4 x = ptx::lds128(tile + xo), y = ptx::lds128(tile + yo);
     if (interleaved) {
-      rope_rotate_chunk_il_cs8<BF16>(x, cs, 0);
-      rope_rotate_chunk_il_cs8<BF16>(y, cs, 1);
+      rope_rotate_chunk_il_cs8<BF16>(x, c8, 0);
+      rope_rotate_chunk_il_cs8<BF16>(y, c8, 1);
     } else {
-      rope_rotate_chunk_cs8<BF16>(x, y, cs);
+      rope_rotate_chunk_cs8<BF16>(x, y, c8);
     }
-    rope_cs8_advance(cs, step);
     ptx::sts128(tile + xo, x);
     ptx::sts128(tile + yo, y);
+  };
+  if (pos != nullptr) {
+    int32_t m[PASSES];
+#pragma unroll
+    for (int pass = 0; pass < PASSES; ++pass) {
+      const int row = r0 + pass * RS;
+      m[pass] = row < nvalid ? __ldg(pos + row) : 0;
+    }
+#pragma unroll 1
+    for (int pass = 0; pass < PASSES; ++pass) {
+      RopeCS8 c8;
+      rope_cs8_exact_signed(m[pass], sfreq, sfreq + 64, ck * 8, c8);
+      rotate_row(r0 + pass * RS, c8);
+    }
+    return;
+  }
+#pragma unroll
+  for (int pass = 0; pass < PASSES; ++pass) {
+    rotate_row(r0 + pass * RS, cs);
+    rope_cs8_advance(cs, step);
   }
 }
 
@@ -387,11 +409,20 @@ __device__ __forceinline__ int unit_of_round(int round, int c, int G) {
   return round * G + ((round & 1) ? (G - 1 - c) : c);
 }
 
+// Key tiles a query tile starting at row r needs: its last row r' = min(r + 127, N - 1) sees keys
+// up to q_off + r'.  With q_off = 0 (GENERAL = false) that is t + 1 for the tile starting at 128 t.
+template <bool GENERAL>
+__device__ __forceinline__ int key_tiles(int r, const AttnParams& p) {
+  if constexpr (GENERAL) return (p.q_off + min(r + BM - 1, p.N - 1)) / BN + 1;
+  return r / BM + 1;
+}
+
+template <bool GENERAL>
 __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
   Unit x;
   if (p.head_pairs) {
     // Two query heads of one KV group on the same 128 rows: q0 = head 2 j, q1 = head 2 j + 1, both
-    // over key tiles 0 .. t (t = the diagonal tile).
+    // over the same key tiles.
     const int pairs = p.B * (p.Hq / 2);
     const int t = p.n_qblocks - 1 - u / pairs;
     const int bj = u - (u / pairs) * pairs;
@@ -401,7 +432,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
     x.hk = x.h0 / (p.Hq / p.Hkv);
     x.r0 = x.r1 = t * BM;
     x.active1 = true;
-    x.n0 = x.n1 = x.n_kt = t + 1;
+    x.n0 = x.n1 = x.n_kt = key_tiles<GENERAL>(x.r0, p);
     return x;
   }
   // Two consecutive 128-row tiles of one head: q0 rows 256 t.., q1 rows 256 t + 128..
@@ -414,8 +445,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
   x.r0 = t * 2 * BM;
   x.r1 = x.r0 + BM;
   x.active1 = x.r1 < p.N;
-  x.n0 = 2 * t + 1;                  // key tiles for q0 (tile 2t is its diagonal)
-  x.n1 = x.active1 ? 2 * t + 2 : 0;  // key tiles for q1
+  x.n0 = key_tiles<GENERAL>(x.r0, p);                     // key tiles for q0
+  x.n1 = x.active1 ? key_tiles<GENERAL>(x.r1, p) : 0;  // key tiles for q1
   x.n_kt = x.active1 ? x.n1 : x.n0;
   return x;
 }
@@ -424,7 +455,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
   for (int rnd_ = 0; rnd_ * (int)gridDim.x < p.total_units; ++rnd_)             \
     if (const int u_ = unit_of_round(rnd_, blockIdx.x, gridDim.x); u_ >= p.total_units) \
       break;                                                                     \
-    else if (const Unit U = decode_unit(u_, p); true)
+    else if (const Unit U = decode_unit<VARIANT>(u_, p); true)
 
 template <int D, bool ROTATE, bool BF16, bool VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -466,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(bar_addr(ctl.mma_done), 1);
     ctl.abort_flag = 0;
+    ctl.q_off = p.q_off;
     ctl.skip = (*reinterpret_cast<volatile unsigned int*>(&g_device_status)) != 0u;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
@@ -642,12 +674,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_steps = wi == 0 ? U.n0 : U.n1;
         if (n_steps == 0) continue;
         const int qt = U.row(wi) / BM;
+        // Key column c of tile j is visible to row r iff c <= q_off + qt*128 + r - j*128; tiles
+        // j >= j_mask have that limit below 127 for some row and take the per-element mask (the
+        // diagonal tile, and the one after it when q_off is not a multiple of 128).  Without extra
+        // keys (VARIANT = false: q_off = 0) that is the last tile, j = qt, with limit r.
+        const int j_mask = VARIANT ? (p.q_off + qt * BM + 1) / BN : n_steps - 1;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_steps && ok; ++j) {
           if (!(ok = wait_bar_warp(bar_addr(ctl.s_full[wi]), gs & 1, ctl, tmo))) break;
           ++gs;
           ptx::tc_fence_after();
-          const bool diag = j == n_steps - 1;  // key column c is visible to row r iff c <= r
+          const bool diag = j >= j_mask;
+          const int lim = VARIANT ? p.q_off + (qt - j) * BM + r : r;
           uint32_t sv[4][32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, sv[c]);
@@ -657,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c)
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (32 * c + e > r) sv[c][e] = __float_as_uint(-INFINITY);
+                if (32 * c + e > lim) sv[c][e] = __float_as_uint(-INFINITY);
           }
           if (j == 0) m_run = row_max128(sv) * sl2;  // the first tile of a row sets the max
           // P with the running max, kept in registers until the row sums pass the check (S stays
@@ -666,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float sum = softmax_p<BF16>(sv, sl2, m_run, pk);
           const bool need = !(sum <= kSumCap);  // also catches inf / nan
           if (__any_sync(0xFFFFFFFFu, need)) {
-            const RowState st = softmax_redo<D, BF16>(tS, tO, r, diag, need, sl2, m_run, l_run);
+            const RowState st = softmax_redo<D, BF16>(tS, tO, lim, diag, need, sl2, m_run, l_run);
             sum = st.sum;
             m_run = st.m;
             l_run = st.l;
@@ -736,7 +774,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Half-split over all d entries: the tuned path; other RoPE forms (VARIANT kernels) take
             // rotate_tile_variant.
             if constexpr (VARIANT)
-              rotate_tile_variant<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step, p.rot_chunks, p.interleaved != 0);
+              rotate_tile_variant<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step, p.rot_chunks, p.interleaved != 0,
+                                           p.kpos ? p.kpos + (size_t)U.b * p.Nk + i * BN : nullptr, p.Nk - i * BN,
+                                           sfreq);
             else
               rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
             ptx::fence_proxy_async_smem();
@@ -746,9 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++uc;
               for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
                 RopeCS8 qcs;
-                rope_cs8_exact((uint32_t)(U.row(tq) + r0), sfreq, sfreq + 64, ck * 8, qcs);
+                // Query row i sits at position q_off + i.  Calls with q_off != 0 run the VARIANT
+                // kernel: the term alone made the default kernel 1.4% slower on GB300.
+                int qpos0 = U.row(tq) + r0;
+                if constexpr (VARIANT) qpos0 += *reinterpret_cast<volatile int*>(&ctl.q_off);
+                rope_cs8_exact((uint32_t)qpos0, sfreq, sfreq + 64, ck * 8, qcs);
                 if constexpr (VARIANT)
-                  rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0);
+                  rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0,
+                                               p.qpos ? p.qpos + (size_t)U.b * p.N + U.row(tq) : nullptr,
+                                               p.N - U.row(tq), sfreq);
                 else
                   rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
               }
@@ -833,20 +879,29 @@ cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t s
 cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
                             cudaStream_t stream, const char** why) {
   if (p.total_units <= 0) return cudaSuccess;
-  const bool variant = rotate && !(p.rot_chunks == d / 16 && p.interleaved == 0);
+  // The default kernels handle N == Nk and (fused) the half-split form over all d entries at
+  // positions i and j; every other case takes the VARIANT instantiation.
+  const bool variant = p.q_off != 0 || (rotate && (!(p.rot_chunks == d / 16 && p.interleaved == 0) ||
+                                                   p.qpos != nullptr || p.kpos != nullptr));
   if (d == 128) {
-    if (variant)
+    if (variant && rotate)
       return bf16 ? launch_one<128, true, true, true>(maps, p, stream, why)
                   : launch_one<128, true, false, true>(maps, p, stream, why);
+    if (variant)
+      return bf16 ? launch_one<128, false, true, true>(maps, p, stream, why)
+                  : launch_one<128, false, false, true>(maps, p, stream, why);
     if (rotate)
       return bf16 ? launch_one<128, true, true, false>(maps, p, stream, why)
                   : launch_one<128, true, false, false>(maps, p, stream, why);
     return bf16 ? launch_one<128, false, true, false>(maps, p, stream, why)
                 : launch_one<128, false, false, false>(maps, p, stream, why);
   }
-  if (variant)
+  if (variant && rotate)
     return bf16 ? launch_one<64, true, true, true>(maps, p, stream, why)
                 : launch_one<64, true, false, true>(maps, p, stream, why);
+  if (variant)
+    return bf16 ? launch_one<64, false, true, true>(maps, p, stream, why)
+                : launch_one<64, false, false, true>(maps, p, stream, why);
   if (rotate)
     return bf16 ? launch_one<64, true, true, false>(maps, p, stream, why)
                 : launch_one<64, true, false, false>(maps, p, stream, why);

@@ -113,14 +113,31 @@ attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, i
 
 size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N * (size_t)H * (size_t)d * 2u; }
 
-// Resolves a RoPE variant: rotary dimension r (0 -> d) and pairing; checks r in [16, d], r % 16 == 0.
-attnfuse_status_t resolve_opts(const attnfuse_rope_opts_t* o, int d, int* r, int* interleaved) {
-  *r = (o && o->rotary_dim) ? o->rotary_dim : d;
-  *interleaved = o ? o->interleaved : 0;
-  if (*r < 16 || *r > d || (*r % 16) != 0)
-    return fail(ATTNFUSE_ERR_INVALID_ARG, "rotary_dim=%d must be 0 or a multiple of 16 in [16, d=%d]", *r, d);
-  if (*interleaved != 0 && *interleaved != 1)
-    return fail(ATTNFUSE_ERR_INVALID_ARG, "interleaved=%d must be 0 or 1", *interleaved);
+// The options of an _ex call with their defaults filled in.
+struct Opts {
+  int rdim;        // rotary dimension (0 -> d)
+  int interleaved;
+  int Nk;          // key/value tokens (0 -> N)
+  const int32_t* qpos;
+  const int32_t* kpos;
+};
+
+// Resolves and checks the options: r in [16, d], r % 16 == 0; interleaved 0/1; N <= Nk < 2^24;
+// position arrays 4-byte aligned.
+attnfuse_status_t resolve_opts(const attnfuse_rope_opts_t* o, int d, int N, Opts* x) {
+  x->rdim = (o && o->rotary_dim) ? o->rotary_dim : d;
+  x->interleaved = o ? o->interleaved : 0;
+  x->Nk = (o && o->kv_len) ? o->kv_len : N;
+  x->qpos = o ? o->q_positions : nullptr;
+  x->kpos = o ? o->k_positions : nullptr;
+  if (x->rdim < 16 || x->rdim > d || (x->rdim % 16) != 0)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rotary_dim=%d must be 0 or a multiple of 16 in [16, d=%d]", x->rdim, d);
+  if (x->interleaved != 0 && x->interleaved != 1)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "interleaved=%d must be 0 or 1", x->interleaved);
+  if (x->Nk < N || x->Nk >= kMaxN)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "kv_len=%d must be 0 or in [N=%d, %d]", o ? o->kv_len : 0, N, kMaxN - 1);
+  if ((x->qpos && !aligned(x->qpos, 4)) || (x->kpos && !aligned(x->kpos, 4)))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "q_positions and k_positions must be 4-byte aligned");
   return ATTNFUSE_OK;
 }
 
@@ -187,11 +204,18 @@ attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnf
 }
 
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype) {
+  return attnfuse_workspace_bytes_ex(B, Hq, Hkv, N, d, mode, dtype, nullptr);
+}
+
+size_t attnfuse_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype,
+                                   const attnfuse_rope_opts_t* opts) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return 0;
-  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, N, d, dtype);
+  const int Nk = (opts && opts->kv_len) ? opts->kv_len : N;
+  if (Nk < N) return 0;
+  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
   if (mode != ATTNFUSE_PREROTATE) return 0;
-  return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, N, Hkv, d), 256);
+  return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, Nk, Hkv, d), 256);
 }
 
 attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int H, int d, double rope_base,
@@ -213,8 +237,10 @@ attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, i
   const char* xs = static_cast<const char*>(x);
   const char* ys = static_cast<const char*>(y);
   if (xs != ys && xs < ys + bytes && ys < xs + bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "x and y overlap without being equal");
-  int rdim = 0, il = 0;
-  if ((st = resolve_opts(opts, d, &rdim, &il)) != ATTNFUSE_OK) return st;
+  Opts o;
+  if ((st = resolve_opts(opts, d, N, &o)) != ATTNFUSE_OK) return st;
+  if (o.Nk != N || o.kpos)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "attnfuse_rope_apply_ex takes q_positions only (kv_len 0, k_positions NULL)");
   if ((st = check_device()) != ATTNFUSE_OK) return st;
 
   RopeApplyParams p;
@@ -227,9 +253,11 @@ attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, i
   p.N = N;
   p.tokens = (long long)B * N;
   p.groups_total = p.job[0].groups;
-  p.rot_chunks = rdim / 16;
-  p.interleaved = il;
-  rope_freqs_host(rdim, rope_base, &p.freqs);
+  p.pos = o.qpos;
+  p.pos_off = 0;
+  p.rot_chunks = o.rdim / 16;
+  p.interleaved = o.interleaved;
+  rope_freqs_host(o.rdim, rope_base, &p.freqs);
   cudaError_t e = launch_rope_apply(p, d, dtype == ATTNFUSE_BF16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rope_apply launch");
   return ATTNFUSE_OK;
@@ -251,10 +279,11 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   g_err[0] = '\0';
   attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, mode, dtype);
   if (st != ATTNFUSE_OK) return st;
-  int rdim = 0, il = 0;
-  if ((st = resolve_opts(opts, d, &rdim, &il)) != ATTNFUSE_OK) return st;
-  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, N, d, dtype);
-  const size_t need = attnfuse_workspace_bytes(B, Hq, Hkv, N, d, mode, dtype);
+  Opts o;
+  if ((st = resolve_opts(opts, d, N, &o)) != ATTNFUSE_OK) return st;
+  const int Nk = o.Nk;
+  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
+  const size_t need = attnfuse_workspace_bytes_ex(B, Hq, Hkv, N, d, mode, dtype, opts);
   if (workspace) {
     if (workspace_bytes < need)
       return fail(ATTNFUSE_ERR_INVALID_ARG, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
@@ -269,6 +298,10 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.N = N;
+  p.Nk = Nk;
+  p.q_off = Nk - N;
+  p.qpos = o.qpos;
+  p.kpos = o.kpos;
   // GQA with an even group size pairs two query heads of a KV group on the same rows (equal key
   // ranges: no half-empty last step, finer units for the persistent schedule); otherwise a unit is
   // two consecutive 128-row tiles of one head.
@@ -279,9 +312,9 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   p.lse = lse;
   p.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
   p.timeout_ns = kTimeoutNs;
-  p.rot_chunks = rdim / 16;
-  p.interleaved = il;
-  rope_freqs_host(rdim, rope_base, &p.freqs);
+  p.rot_chunks = o.rdim / 16;
+  p.interleaved = o.interleaved;
+  rope_freqs_host(o.rdim, rope_base, &p.freqs);
 
   const void* qa = q;
   const void* ka = k;
@@ -300,16 +333,41 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
     void* kr = static_cast<char*>(ws) + round_up(tensor_bytes(B, N, Hq, d), 256);
     RopeApplyParams rp;
     std::memset(&rp, 0, sizeof rp);
-    rp.job[0] = RopeJob{q, qr, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
-    rp.job[1] = RopeJob{k, kr, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
-    rp.njobs = 2;
-    rp.N = N;
-    rp.tokens = (long long)B * N;
-    rp.groups_total = rp.job[0].groups + rp.job[1].groups;
     rp.rot_chunks = p.rot_chunks;
     rp.interleaved = p.interleaved;
     rp.freqs = p.freqs;
-    cudaError_t e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+    const RopeJob jq{q, qr, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    const RopeJob jk{k, kr, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    cudaError_t e = cudaSuccess;
+    if (Nk == N && !o.qpos && !o.kpos) {
+      // Q and K share tokens and positions: one launch over both.
+      rp.job[0] = jq;
+      rp.job[1] = jk;
+      rp.njobs = 2;
+      rp.N = N;
+      rp.tokens = (long long)B * N;
+      rp.groups_total = jq.groups + jk.groups;
+      e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+    } else {
+      // Queries at Nk - N + i (or q_positions), keys at j (or k_positions): one launch each.
+      rp.njobs = 1;
+      rp.job[0] = jq;
+      rp.N = N;
+      rp.tokens = (long long)B * N;
+      rp.groups_total = jq.groups;
+      rp.pos = o.qpos;
+      rp.pos_off = Nk - N;
+      e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+      if (e == cudaSuccess) {
+        rp.job[0] = jk;
+        rp.N = Nk;
+        rp.tokens = (long long)B * Nk;
+        rp.groups_total = jk.groups;
+        rp.pos = o.kpos;
+        rp.pos_off = 0;
+        e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+      }
+    }
     if (e != cudaSuccess) {
       if (owned) cudaFreeAsync(owned, s);
       return cuda_fail(e, "rope_apply launch");
@@ -320,8 +378,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
 
   AttnMaps maps;
   if ((st = encode_bnhd(&maps.q, qa, B, N, Hq, d, dtype, "q")) == ATTNFUSE_OK &&
-      (st = encode_bnhd(&maps.k, ka, B, N, Hkv, d, dtype, "k")) == ATTNFUSE_OK &&
-      (st = encode_bnhd(&maps.v, v, B, N, Hkv, d, dtype, "v")) == ATTNFUSE_OK) {
+      (st = encode_bnhd(&maps.k, ka, B, Nk, Hkv, d, dtype, "k")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.v, v, B, Nk, Hkv, d, dtype, "v")) == ATTNFUSE_OK) {
     const char* why = nullptr;
     cudaError_t e = launch_attn_fwd(maps, p, d, dtype == ATTNFUSE_BF16, mode == ATTNFUSE_FUSED, s, &why);
     if (e != cudaSuccess) st = why ? fail(ATTNFUSE_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "attention launch");

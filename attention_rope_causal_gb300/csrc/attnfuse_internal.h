@@ -25,6 +25,8 @@ struct RopeApplyParams {
   int njobs;
   int N;
   long long tokens;  // B * N
+  const int32_t* pos;  // [B, N] rotation position of each token (one job only), or nullptr:
+  int pos_off;         //   then the position of token (b, n) is pos_off + n
   int groups_total;  // job[0].groups + (njobs > 1 ? job[1].groups : 0)
   int rot_chunks;    // rotary_dim / 16: item ck < rot_chunks rotates (frequencies 8 ck .. 8 ck + 7)
   int interleaved;   // 0: pairs (k, k + rotary_dim/2); 1: pairs (2k, 2k + 1)
@@ -36,12 +38,16 @@ cudaError_t launch_rope_apply(const RopeApplyParams& p, int d, bool bf16, cudaSt
 // ---- attention kernel -----------------------------------------------------------------------
 
 struct AttnParams {
-  int B, Hq, Hkv, N;
+  int B, Hq, Hkv, N;  // N = query rows per batch entry
+  int Nk;             // key/value rows per batch entry (>= N)
+  int q_off;          // Nk - N: query i is token q_off + i and sees keys j <= q_off + i
+  const int32_t* qpos;  // [B, N] query rotation positions, or nullptr (q_off + i)
+  const int32_t* kpos;  // [B, Nk] key rotation positions, or nullptr (j)
   int head_pairs;    // 1: a work unit is two query heads of one KV group on the same 128 rows
                      // (Hq / Hkv even); 0: two consecutive 128-row tiles of one head
   int n_qblocks;     // query blocks per head: ceil(N / 128) with head pairs, ceil(N / 256) without
   int total_units;   // B * Hq * n_qblocks, halved with head pairs
-  void* out;         // [B, N, Hq, d]
+  void* out;         // [B, N, Hq, d]  (q is [B, N, Hq, d]; k, v are [B, Nk, Hkv, d])
   float* lse;        // [B, Hq, N] or nullptr
   float scale_log2;  // log2(e) / sqrt(d)
   int rot_chunks;    // rotary_dim / 16 (fused mode: rotation thread chunk ck < rot_chunks works)

@@ -61,6 +61,14 @@ __device__ __forceinline__ void rope_cs(uint32_t pos, uint32_t flo, uint32_t fhi
   sincos_turns(turns, c, s);
 }
 
+// The same for any signed position: the turn fraction of -m is the negated turn fraction of m
+// (within the 2^-32 turn truncation).
+__device__ __forceinline__ void rope_cs_signed(int32_t pos, uint32_t flo, uint32_t fhi, float& c, float& s) {
+  const uint32_t a = pos < 0 ? 0u - (uint32_t)pos : (uint32_t)pos;
+  const uint32_t t = __umulhi(a, flo) + a * fhi;
+  sincos_turns(pos < 0 ? 0u - t : t, c, s);
+}
+
 // (c, s) <- (c, s) * (c2, s2) as unit complex numbers: the angle advances by the angle of (c2, s2).
 __device__ __forceinline__ void rope_advance(float& c, float& s, float c2, float s2) {
   float cn = __fmaf_rn(c, c2, -__fmul_rn(s, s2));
@@ -151,6 +159,19 @@ __device__ __forceinline__ void rope_cs8_exact(uint32_t pos, const uint32_t* lo,
     float c0, s0, c1, s1;
     rope_cs(pos, lo[k0 + 2 * j], hi[k0 + 2 * j], c0, s0);
     rope_cs(pos, lo[k0 + 2 * j + 1], hi[k0 + 2 * j + 1], c1, s1);
+    o.c[j] = ptx::f2_pack(c0, c1);
+    o.s[j] = ptx::f2_pack(s0, s1);
+  }
+}
+
+// rope_cs8_exact for a signed position.
+__device__ __forceinline__ void rope_cs8_exact_signed(int32_t pos, const uint32_t* lo, const uint32_t* hi, int k0,
+                                                      RopeCS8& o) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float c0, s0, c1, s1;
+    rope_cs_signed(pos, lo[k0 + 2 * j], hi[k0 + 2 * j], c0, s0);
+    rope_cs_signed(pos, lo[k0 + 2 * j + 1], hi[k0 + 2 * j + 1], c1, s1);
     o.c[j] = ptx::f2_pack(c0, c1);
     o.s[j] = ptx::f2_pack(s0, s1);
   }

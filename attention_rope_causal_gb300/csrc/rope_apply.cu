@@ -10,7 +10,8 @@
 // each warp-wide 16-byte load or store touches whole 128-byte segments.  A thread computes the
 // cos/sin of its 8 frequencies once and applies them to every head of its group, keeping 4 heads
 // (8 loads of 16 bytes) in flight.  RoPE variants: only the first rotary_dim entries rotate (the
-// rest are copied), in half-split or interleaved pairs.
+// rest are copied), in half-split or interleaved pairs.  The rotation position of token (b, n) is
+// read from a per-token array, or is a fixed offset plus n.
 #include <cuda_runtime.h>
 
 #include "attnfuse_internal.h"
@@ -32,7 +33,7 @@ __global__ void __launch_bounds__(kThreads) rope_apply_kernel(const __grid_const
   const int rem = (int)(item - token * per_token);
   int g = rem / NCH;
   const int ck = rem - g * NCH;
-  const uint32_t pos = (uint32_t)(token % p.N);
+  const int32_t pos = p.pos ? p.pos[token] : p.pos_off + (int32_t)(token % p.N);
 
   int j = 0;
   if (g >= p.job[0].groups) {
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) rope_apply_kernel(const __grid_const
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const int k = ck * 8 + t;
-      rope_cs(pos, p.freqs.lo[k], p.freqs.hi[k], c[t], s[t]);
+      rope_cs_signed(pos, p.freqs.lo[k], p.freqs.hi[k], c[t], s[t]);
     }
   }
 

@@ -91,3 +91,27 @@ def make_inputs(w: Workload, device=None):
             x = x.to(device)
         out.append(x)
     return tuple(out)
+
+
+def make_kv_inputs(B: int, N: int, Nk: int, Hq: int, Hkv: int, d: int, dtype: str, seed: int, sigma: float = 1.0,
+                   device=None):
+    """(q, k, v) with more keys than queries: q [B, N, Hq, d], k and v [B, Nk, Hkv, d]; same recipe as
+    :func:`make_inputs` (fp32 standard normals in the order q, k, v from ``seed``, times sigma, cast)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    t = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    out = []
+    for shape in ((B, N, Hq, d), (B, Nk, Hkv, d), (B, Nk, Hkv, d)):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x.mul_(sigma)
+        x = x.to(t)
+        out.append(x if device is None else x.to(device))
+    return tuple(out)
+
+
+def make_positions(B: int, n: int, seed: int, low: int = -4096, high: int = 1 << 20) -> torch.Tensor:
+    """Random int32 rotation positions [B, n] in [low, high) (any integers are valid positions)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randint(low, high, (B, n), generator=g, dtype=torch.int64).to(torch.int32)

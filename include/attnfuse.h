@@ -96,21 +96,43 @@ attnfuse_status_t attnfuse_rope_apply(const void* x, void* y, int B, int N, int 
                                       attnfuse_dtype_t dtype, void* stream);
 
 /*
- * RoPE variants (extensions of the rotation the pages name, "AttnFuse Makes RoPE a First-Class
- * Attention Compilation Operation", paragraph 1; the pages fix no pairing or rotary dimension).
+ * RoPE variants and the general causal form (extensions of the rotation and the causality block the
+ * pages name, "AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraphs 1-2;
+ * the pages fix no pairing, rotary dimension, key length or position source).
  *   rotary_dim: only entries [0, r) of each head vector are rotated, with theta_k = base^(-2k/r),
  *               k < r/2; entries [r, d) pass through unchanged.  0 means r = d.  Otherwise
  *               16 <= r <= d and r a multiple of 16.
  *   interleaved: 0 pairs (k, k + r/2) (half-split, the default form); 1 pairs (2k, 2k + 1).
- * A NULL pointer to the struct means { 0, 0 }: the functions without _ex.
+ *   kv_len:     Nk, the number of key/value tokens per batch entry (k, v are [B, Nk, Hkv, d]); 0
+ *               means N.  Otherwise N <= Nk < 2^24.  The N queries are the last N of the Nk tokens
+ *               (a prefill that extends a cache of Nk - N earlier tokens; N = 1 is one decode
+ *               step): query i sees keys j <= Nk - N + i.
+ *   q_positions: NULL, or device int32 [B, N] (4-byte aligned): the rotation position of each
+ *               query token.  NULL means Nk - N + i.
+ *   k_positions: NULL, or device int32 [B, Nk]: the rotation position of each key token.  NULL
+ *               means j.  Positions may be any int32 values; they set the RoPE angles only, never
+ *               the mask.  The fused kernel computes exact cos/sin per row when positions are given
+ *               (slower than the default walk along consecutive positions).
+ * A NULL pointer to the struct means all zero: the functions without _ex.
  */
 typedef struct {
   int rotary_dim;
   int interleaved;
+  int kv_len;
+  const int32_t* q_positions;
+  const int32_t* k_positions;
 } attnfuse_rope_opts_t;
 
-/* attnfuse_rope_causal_fwd with a RoPE variant (opts may be NULL); same arguments otherwise.
- * Invalid opts give ATTNFUSE_ERR_INVALID_ARG. */
+/* attnfuse_workspace_bytes for attnfuse_rope_causal_fwd_ex with `opts` (may be NULL): the rotated K
+ * has kv_len tokens.  Returns 0 for invalid arguments. */
+size_t attnfuse_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype,
+                                   const attnfuse_rope_opts_t* opts);
+
+/* attnfuse_rope_causal_fwd with a RoPE variant and/or the general causal form (opts may be NULL);
+ * same arguments otherwise (N = query tokens; `lse` is [B, Hq, N]).  Invalid opts give
+ * ATTNFUSE_ERR_INVALID_ARG.  In PREROTATE mode the workspace must hold
+ * attnfuse_workspace_bytes_ex(...) bytes (rotated Q [B, N, Hq, d] and K [B, Nk, Hkv, d]); AUTO
+ * applies attnfuse_select_mode with Nk in place of N. */
 attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse,
                                               int B, int Hq, int Hkv, int N, int d, double rope_base,
                                               attnfuse_mode_t mode, attnfuse_dtype_t dtype, void* workspace,
@@ -118,7 +140,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
                                               void* stream);
 
 /* attnfuse_rope_apply with a RoPE variant (opts may be NULL).  Out of place, the entries that are
- * not rotated are copied to y; in place they are left as they are. */
+ * not rotated are copied to y; in place they are left as they are.  opts->q_positions, if not NULL,
+ * gives the position of each token of x ([B, N] int32); kv_len must be 0 and k_positions NULL. */
 attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, int H, int d, double rope_base,
                                          attnfuse_dtype_t dtype, const attnfuse_rope_opts_t* opts, void* stream);
 

@@ -109,6 +109,38 @@ def test_variant_options_are_checked_before_the_device(lib, r, il, status):
     assert b"rotary_dim" in lib.attnfuse_last_error() or b"interleaved" in lib.attnfuse_last_error()
 
 
+@pytest.mark.parametrize("kv_len,qpos,kpos,what", [(100, None, None, b"kv_len"), (1 << 24, None, None, b"kv_len"),
+                                                  (-5, None, None, b"kv_len"), (0, FAKE + 2, None, b"positions"),
+                                                  (200, None, FAKE + 1, b"positions")])
+def test_key_length_and_position_options_are_checked_before_the_device(lib, kv_len, qpos, kpos, what):
+    opts = binding.RopeOpts(0, 0, kv_len, qpos, kpos)
+    assert lib.attnfuse_rope_causal_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 128, 64, 1e4, 0, 0, None, 0,
+                                           ctypes.byref(opts), None) == 1
+    assert what in lib.attnfuse_last_error()
+
+
+def test_rope_apply_takes_query_positions_only(lib):
+    for opts in (binding.RopeOpts(0, 0, 32, None, None), binding.RopeOpts(0, 0, 0, None, FAKE)):
+        assert lib.attnfuse_rope_apply_ex(FAKE, FAKE, 1, 16, 2, 64, 1e4, 0, ctypes.byref(opts), None) == 1
+        assert b"q_positions only" in lib.attnfuse_last_error()
+
+
+def test_workspace_bytes_with_more_keys(lib):
+    opts = binding.RopeOpts(0, 0, 1000, None, None)
+    q = 1 * 300 * 4 * 128 * 2
+    k = 1 * 1000 * 2 * 128 * 2
+    assert lib.attnfuse_workspace_bytes_ex(1, 4, 2, 300, 128, 1, 0, ctypes.byref(opts)) == q + k
+    assert lib.attnfuse_workspace_bytes_ex(1, 4, 2, 300, 128, 0, 0, ctypes.byref(opts)) == 0
+    assert lib.attnfuse_workspace_bytes_ex(1, 4, 2, 300, 128, 1, 0, None) == lib.attnfuse_workspace_bytes(
+        1, 4, 2, 300, 128, 1, 0)
+    short = binding.RopeOpts(0, 0, 100, None, None)
+    assert lib.attnfuse_workspace_bytes_ex(1, 4, 2, 300, 128, 1, 0, ctypes.byref(short)) == 0
+    # AUTO judges the shape by the key length
+    long_kv = binding.RopeOpts(0, 0, 8192, None, None)
+    assert lib.attnfuse_workspace_bytes_ex(1, 32, 8, 16, 128, 2, 0, ctypes.byref(long_kv)) > 0
+    assert binding.workspace_bytes(1, 4, 2, 300, 128, "prerotate", kv_len=1000) == q + k
+
+
 def test_valid_call_without_gpu_fails_cleanly(lib):
     import torch
     if torch.cuda.is_available():
