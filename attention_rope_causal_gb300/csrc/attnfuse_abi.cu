@@ -197,9 +197,9 @@ attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnf
   (void)dtype;
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0) return ATTNFUSE_FUSED;
   // Measured on GB300 (bench.py --sweep): with 4:1 GQA, pre-rotation wins at every N in [2048,
-  // 16384] (both dtypes); with MHA d=64 the crossover is N* ~ 4000 (3980 bf16, 4030 fp16).
+  // 16384] (both dtypes); with MHA d=64 the crossover is N* ~ 3100 (3066 bf16, 3108 fp16).
   const bool gqa = Hq / Hkv >= 2;
-  const int n_star = gqa ? 2048 : 4000;
+  const int n_star = gqa ? 2048 : 3072;
   return N >= n_star ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
 }
 

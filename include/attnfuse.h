@@ -81,7 +81,7 @@ size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_m
  * crossover ("Rotation Calculus" in "AttnFuse Makes RoPE a First-Class Attention Compilation
  * Operation", paragraph 2, made a runtime choice): grouped-query attention (Hq / Hkv >= 2) with
  * N >= 2048 -> PREROTATE (measured faster at every N from 2048 to 16384); multi-head attention
- * (Hq == Hkv) with N >= 4000 -> PREROTATE (measured N* ~ 4000); everything else -> FUSED.
+ * (Hq == Hkv) with N >= 3072 -> PREROTATE (measured N* ~ 3100); everything else -> FUSED.
  * Host-only and pure: no device access; arguments it cannot judge (non-positive sizes, Hq not a
  * multiple of Hkv) give FUSED.
  */
