@@ -16,7 +16,9 @@ ctypes.  What it computes, and the passages it follows, are stated in that file'
   theta_k = base^(-2k/r), and adjacent pairs (2k, 2k+1) instead of (k, k+r/2);
 * more keys than queries (k, v with Nk >= Nq tokens: the queries are the last Nq, so query i sees
   keys j <= Nk - Nq + i) and explicit rotation positions (``q_positions``, ``k_positions``), which
-  change the angles only.
+  change the angles only;
+* the backward pass (``rope_causal_bwd``): gradients of sum(dout * out) through the softmax, the
+  products and the rotation (dq = R^T dq', dk = R^T dk').
 """
 from __future__ import annotations
 
@@ -78,6 +80,12 @@ def _load():
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.orc_rope_causal_bwd.restype = ctypes.c_int
+            lib.orc_rope_causal_bwd.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -217,3 +225,50 @@ def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None, rot
     if rc != 0:
         raise RuntimeError("orc_rope_causal_ex failed")
     return out, lse
+
+
+def _rows(rows, N: int, what: str):
+    if rows is None:
+        return None, N, None
+    sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    if sel.size and (sel.min() < 0 or sel.max() >= N):
+        raise ValueError(f"{what} out of range")
+    if np.unique(sel).size != sel.size:
+        raise ValueError(f"{what} must be distinct")
+    return sel.ctypes.data, int(sel.size), sel
+
+
+def rope_causal_bwd(q, k, v, dout, base: float, q_rows=None, k_rows=None, threads: int | None = None,
+                    rotary_dim: int | None = None, interleaved: bool = False):
+    """Backward pass of :func:`rope_causal` (N queries and keys, default positions): the gradients of
+    L = sum(dout * out) with respect to q, k and v (no lse term).
+
+    q, dout: [B, N, Hq, d]; k, v: [B, N, Hkv, d], one dtype (bf16/fp16 torch tensors, fp16 or fp64
+    arrays).  q_rows / k_rows select the query rows whose dq and the key rows whose dk, dv are
+    returned (default: all, in order).  Returns (dq [B, Rq, Hq, d], dk [B, Rk, Hkv, d],
+    dv [B, Rk, Hkv, d]) as float64.
+    """
+    qr, dq_ = _as_raw(q)
+    kr, dk_ = _as_raw(k)
+    vr, dv_ = _as_raw(v)
+    gr, dg_ = _as_raw(dout)
+    if not (dq_ == dk_ == dv_ == dg_):
+        raise TypeError("q, k, v, dout must share one dtype")
+    B, N, Hq, d = qr.shape
+    Hkv = kr.shape[2]
+    if kr.shape != (B, N, Hkv, d) or vr.shape != (B, N, Hkv, d) or gr.shape != qr.shape:
+        raise ValueError("k, v must be [B, N, Hkv, d] and dout [B, N, Hq, d]")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    qp, nq, _qs = _rows(q_rows, N, "q_rows")
+    kp, nk, _ks = _rows(k_rows, N, "k_rows")
+    dq = np.zeros((B, nq, Hq, d))
+    dk = np.zeros((B, nk, Hkv, d))
+    dv = np.zeros((B, nk, Hkv, d))
+    r = d if rotary_dim is None else int(rotary_dim)
+    rc = _load().orc_rope_causal_bwd(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, gr.ctypes.data, dq_, B, Hq, Hkv,
+                                     N, d, r, int(bool(interleaved)), float(base), qp, nq, kp, nk, dq.ctypes.data,
+                                     dk.ctypes.data, dv.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("orc_rope_causal_bwd failed")
+    return dq, dk, dv
