@@ -43,6 +43,10 @@ _SIGNATURES = {
                                               ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.POINTER(RopeOpts),
                                               ctypes.c_void_p]),
     "attnfuse_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 7),
+    "attnfuse_rope_causal_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int,
+                                                                                        ctypes.c_void_p, ctypes.c_size_t,
+                                                                                        ctypes.c_void_p]),
+    "attnfuse_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
     "attnfuse_workspace_bytes_ex": (ctypes.c_size_t, [ctypes.c_int] * 7 + [ctypes.POINTER(RopeOpts)]),
     "attnfuse_select_mode": (ctypes.c_int, [ctypes.c_int] * 6),
     "attnfuse_rope_causal_fwd_prerotate_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -186,6 +190,34 @@ def rope_apply(x, rope_base: float, out=None, stream=None, rotary_dim=None, inte
         _check(load().attnfuse_rope_apply_ex(_ptr(x), _ptr(out), B, N, H, d, float(rope_base), DTYPES[x.dtype],
                                              ctypes.byref(opts), _stream_ptr(stream)))
     return out
+
+
+def bwd_workspace_bytes(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> int:
+    return int(load().attnfuse_bwd_workspace_bytes(B, Hq, Hkv, N, d, DTYPES[dtype]))
+
+
+def rope_causal_bwd(q, k, v, out, lse, dout, rope_base: float, dq=None, dk=None, dv=None, workspace=None,
+                    stream=None):
+    """Backward pass through ``attnfuse_rope_causal_bwd``: (dq, dk, dv) for q [B, N, Hq, d], k/v
+    [B, N, Hkv, d], the forward's out [B, N, Hq, d] and lse [B, Hq, N] (float32), and dout = dL/dout.
+    All CUDA tensors, contiguous, one 16-bit dtype (lse float32)."""
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(load().attnfuse_rope_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                           _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(rope_base), DTYPES[q.dtype],
+                                           ws_ptr, ws_bytes, _stream_ptr(stream)))
+    return dq, dk, dv
 
 
 def device_status(stream=None) -> int:

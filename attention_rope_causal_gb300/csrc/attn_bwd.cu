@@ -1,0 +1,728 @@
+// Backward pass of causal softmax attention with RoPE on sm_103a: dq, dk, dv from q, k, v, the
+// forward's output O and log-sum-exp, and dO = dL/dO.
+//
+// What it computes (the chain rule through the forward of "AttnFuse Makes RoPE a First-Class
+// Attention Compilation Operation", 2026-09-13 AI papers report, paragraphs 1-2: RoPE on Q and K
+// before the product, causal mask, softmax; training needs this pass, paragraph 3): with q' = R(i) q,
+// k' = R(j) k, P_ij = exp(q'_i.k'_j / sqrt(d) - lse_i) for j <= i,
+//   dv_j  = sum_{h in the group, i >= j} P_ij dO_i
+//   dS_ij = P_ij (dO_i . v_j - D_i),   D_i = dO_i . O_i  (= sum_j P_ij dO_i . v_j)
+//   dq_i  = R(i)^T sum_j dS_ij k'_j / sqrt(d),   dk_j = R(j)^T sum_{h, i >= j} dS_ij q'_i / sqrt(d)
+// (R^T: the rotation by the negated angle).  Three steps:
+//   1. the pre-rotation kernel writes q', k' to the workspace, and bwd_prep_kernel writes D;
+//   2. bwd_dkdv_kernel: one unit = one 128-key tile of one KV head; it walks every query tile at or
+//      after the key tile, for every query head of the group, accumulating dV and dK' in tensor
+//      memory (S^T = K' Q'^T and dP^T = V dO^T by tcgen05.mma, P^T and dS^T elementwise, then
+//      dV += P^T dO and dK' += dS^T Q' with P^T, dS^T read from tensor memory);
+//   3. bwd_dq_kernel: one unit = one 128-row query tile of one head; it walks key tiles 0 .. its
+//      diagonal, accumulating dQ' (S and dP, dS elementwise, dQ' += dS K').
+// Both epilogues scale by 1/sqrt(d) and rotate back with R^T at the row's position in registers (a
+// thread holds a whole row, so each pair (e, e + d/2) is local).
+//
+// Structure of both kernels: 384 threads, one CTA per SM, persistent over units.
+//   warp 0      TMA producer (whole warp; lane 0 issues), also stages lse/D vectors for dK/dV.
+//   warp 1      tcgen05.mma issuer (whole warp, one elected lane issues); owns the tensor memory.
+//   warps 4-7   elementwise for columns 0..63 of each 128 x 128 tile, and half of the epilogue.
+//   warps 8-11  the same for columns 64..127.
+// Tensor memory (512 columns): S (0..127) | dP (128..255) | accumulators (256..).  The packed 16-bit
+// P / dS of a warpgroup's 64 columns are written over the first 32 columns of that warpgroup's own
+// 64 S / dP columns, so no warpgroup overwrites columns the other has yet to read; each K16 step of
+// the MMAs that read them addresses its 8 columns directly.
+// Every barrier wait gives up after AttnBwdParams::timeout_ns, records bit 0 in this file's device
+// status word and stops the CTA after letting its copies and MMAs land.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <type_traits>
+
+#include "attnfuse_internal.h"
+#include "ptx.cuh"
+#include "rope.cuh"
+
+namespace attnfuse {
+
+__device__ unsigned int g_bwd_status = 0;
+
+namespace {
+
+constexpr int BM = 128;                     // rows per tile (= TMEM lanes)
+constexpr int kThreads = 384;
+constexpr uint32_t kBoxBytes = 128 * 128;   // 128 rows x 64 16-bit columns, 128-byte swizzled
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int NBOX = D / 64;
+  static constexpr uint32_t TILE = NBOX * kBoxBytes;
+  // Resident pair (dK/dV: K', V; dQ: Q', dO) then a 2-stage ring of pairs (dK/dV: Q', dO; dQ: K', V).
+  static constexpr uint32_t OFF_RES = 0;
+  static constexpr uint32_t OFF_RING = 2 * TILE;
+  static constexpr uint32_t OFF_VEC = OFF_RING + 4 * TILE;  // dK/dV: per stage L[128], D[128] (fp32)
+  static constexpr uint32_t OFF_CTL = OFF_VEC + 2 * 2 * BM * 4;
+  static constexpr uint32_t SMEM = OFF_CTL + 256 + 1024;
+};
+
+struct __align__(8) BwdCtrl {
+  uint64_t res_full, res_empty;          // resident pair landed / free again
+  uint64_t ring_full[2], ring_empty[2];  // ring stage landed / free again
+  uint64_t s_full;                       // S and dP of this step are in tensor memory
+  uint64_t p_ready;                      // the elementwise warps wrote P / dS (256 arrivals)
+  uint64_t acc_full;                     // the unit's accumulators are complete
+  uint64_t acc_empty;                    // the epilogue has read them (256 arrivals)
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int skip;
+};
+static_assert(sizeof(BwdCtrl) <= 256, "control block");
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t& b) { return ptx::smem_u32(&b); }
+
+__device__ __forceinline__ void signal_abort(BwdCtrl& ctl) {
+  *reinterpret_cast<volatile int*>(&ctl.abort_flag) = 1;
+  atomicOr(&g_bwd_status, 1u);
+}
+
+// Bounded wait on an mbarrier phase; false if this CTA aborted or the wait ran out (then the
+// status word and the abort flag are set).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, BwdCtrl& ctl, unsigned long long timeout_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        signal_abort(ctl);
+        return false;
+      }
+    }
+  }
+}
+
+// Whole-warp form: every lane polls, a vote makes the outcome warp-uniform.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, BwdCtrl& ctl, unsigned long long tmo) {
+  return __all_sync(0xFFFFFFFFu, wait_bar(bar, parity, ctl, tmo));
+}
+
+// Bounded wait that ignores the abort flag: used only to let in-flight copies and MMAs land.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer_ns() - t0 > timeout_ns) return;
+}
+
+__device__ __forceinline__ int unit_of_round(int round, int c, int G) {
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return Pack<BF16>::pack(lo, hi);
+}
+
+// D[b, h, i] = dO_i . O_i in fp32: one warp per (b, i, h) row of d elements.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ AttnBwdParams p) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int PER = D / 32;  // elements per lane: 4 (d = 128) or 2 (d = 64)
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  const long long rows = (long long)p.B * p.N * p.Hq;
+  if (row >= rows) return;
+  const T* o = reinterpret_cast<const T*>(p.out) + row * D + lane * PER;
+  const T* g = reinterpret_cast<const T*>(p.dout) + row * D + lane * PER;
+  float acc = 0.f;
+  if constexpr (PER == 4) {
+    const uint2 ov = *reinterpret_cast<const uint2*>(o), gv = *reinterpret_cast<const uint2*>(g);
+    float a0, a1, b0, b1;
+    Pack<BF16>::unpack(ov.x, a0, a1);
+    Pack<BF16>::unpack(gv.x, b0, b1);
+    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
+    Pack<BF16>::unpack(ov.y, a0, a1);
+    Pack<BF16>::unpack(gv.y, b0, b1);
+    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
+  } else {
+    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o), gv = *reinterpret_cast<const uint32_t*>(g);
+    float a0, a1, b0, b1;
+    Pack<BF16>::unpack(ov, a0, a1);
+    Pack<BF16>::unpack(gv, b0, b1);
+    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) {
+    // row = (b * N + i) * Hq + h  ->  D[(b * Hq + h) * N + i]
+    const int h = (int)(row % p.Hq);
+    const long long bi = row / p.Hq;
+    const int i = (int)(bi % p.N);
+    const int b = (int)(bi / p.N);
+    p.Dvec[((long long)b * p.Hq + h) * p.N + i] = acc;
+  }
+}
+
+// R(pos)^T applied to the pair (x, y) = (row[e], row[e + d/2]) with frequency F_e.
+__device__ __forceinline__ void unrotate_pair(float& x, float& y, uint32_t pos, uint32_t flo, uint32_t fhi) {
+  float c, s;
+  rope_cs(pos, flo, fhi, c, s);
+  const float xr = __fmaf_rn(x, c, __fmul_rn(y, s));
+  const float yr = __fmaf_rn(y, c, -__fmul_rn(x, s));
+  x = xr;
+  y = yr;
+}
+
+// S-like product into tensor memory: D[dst] = A B^T with A, B 128-row tiles of d columns in shared
+// memory, both K-major (the layout TMA writes).  Consecutive K-steps add a constant to the start
+// address field (offsets stay inside the 14-bit field).
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t dst, uint32_t a, uint32_t b, uint32_t idesc) {
+  const uint64_t da = ptx::sdesc_sw128(a, 16, 1024), db = ptx::sdesc_sw128(b, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t step = (uint64_t)((kk / 4) * (kBoxBytes >> 4) + (kk % 4) * 2);
+    ptx::mma_ss_w(dst, da + step, db + step, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Accumulation D[dst] (+)= A B with A the packed 16-bit 128 x 128 matrix in tensor memory (K16 step
+// kk in the 8 columns at a + 64 (kk / 4) + 8 (kk % 4): each warpgroup's half sits over its own S /
+// dP columns) and B a 128-row tile in shared memory read MN-major (N = d columns, K = its rows).
+template <int D>
+__device__ __forceinline__ void issue_acc(uint32_t dst, uint32_t a, uint32_t b, uint32_t idesc, bool first) {
+  const uint64_t db = ptx::sdesc_sw128(b, kBoxBytes, 1024);
+#pragma unroll
+  for (int kk = 0; kk < BM / 16; ++kk)
+    ptx::mma_ts_w(dst, a + 64 * (kk / 4) + 8 * (kk % 4), db + (uint64_t)(kk * (2048 >> 4)), idesc,
+                  (!first || kk > 0) ? 1u : 0u);
+}
+
+// Common prologue of both kernels: barriers, tensor memory, skip flag.
+template <int D>
+__device__ __forceinline__ void bwd_setup(BwdCtrl& ctl, int warp) {
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_addr(ctl.res_full), 1);
+    ptx::mbar_init(bar_addr(ctl.res_empty), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar_addr(ctl.ring_full[s]), 1);
+      ptx::mbar_init(bar_addr(ctl.ring_empty[s]), 1);
+    }
+    ptx::mbar_init(bar_addr(ctl.s_full), 1);
+    ptx::mbar_init(bar_addr(ctl.p_ready), 256);
+    ptx::mbar_init(bar_addr(ctl.acc_full), 1);
+    ptx::mbar_init(bar_addr(ctl.acc_empty), 256);
+    ptx::mbar_init(bar_addr(ctl.mma_done), 1);
+    ctl.abort_flag = 0;
+    ctl.skip = (*reinterpret_cast<volatile unsigned int*>(&g_bwd_status)) != 0u;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+}
+
+__device__ __forceinline__ void bwd_teardown(BwdCtrl& ctl, int warp, uint32_t tmem) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Let every copy already issued land before shared memory is released.
+__device__ __forceinline__ void drain_copies(BwdCtrl& ctl, int res_loads, int ring_loads) {
+  const unsigned long long drain = 100000000ull;
+  if (res_loads > 0) drain_bar(bar_addr(ctl.res_full), (res_loads - 1) & 1, drain);
+  for (int s = 0; s < 2; ++s)
+    if (ring_loads > s) drain_bar(bar_addr(ctl.ring_full[s]), ((ring_loads - 1 - s) / 2) & 1, drain);
+}
+
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int head, int row,
+                                         int b) {
+#pragma unroll
+  for (int bx = 0; bx < D / 64; ++bx) ptx::tma_load_4d(dst + bx * kBoxBytes, map, bar, bx * 64, head, row, b);
+}
+
+// ================================ dK, dV ==================================================
+// Unit u: key tile kt = u / (B Hkv) (ascending, so the units with the most query tiles come first)
+// of KV head hk, batch b; steps: query head h of the group (outer), query tile t = kt .. last.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const __grid_constant__ AttnBwdParams p) {
+  using C = BwdCfg<D>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr uint32_t AB = BF16 ? 1u : 0u;
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, BM, 0, 0);
+  constexpr uint32_t IDESC_ACC = ptx::idesc_f16(AB, BM, D, 0, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  BwdCtrl& ctl = *reinterpret_cast<BwdCtrl*>(sgen + C::OFF_CTL);
+  const uint32_t sK = sbase + C::OFF_RES, sV = sK + C::TILE, sRing = sbase + C::OFF_RING;
+  float* sVec = reinterpret_cast<float*>(sgen + C::OFF_VEC);
+  const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+
+  bwd_setup<D>(ctl, warp);
+  const uint32_t tmem = ctl.tmem_base;
+  const bool skip = __shfl_sync(0xFFFFFFFFu, ctl.skip, 0) != 0;
+  const unsigned long long tmo = p.timeout_ns;
+  const int g = p.Hq / p.Hkv, nt = p.n_tiles, bh_count = p.B * p.Hkv;
+  const int total = bh_count * nt;
+
+  if (!skip && warp == 0) {
+    // ------------------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      ptx::tma_prefetch_desc(&tmO);
+    }
+    int gs = 0, uc = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
+      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+      if (u >= total) break;
+      const int kt = u / bh_count, bh = u - kt * bh_count, b = bh / p.Hkv, hk = bh - b * p.Hkv;
+      if (!(ok = wait_warp(bar_addr(ctl.res_empty), (uc & 1) ^ 1, ctl, tmo))) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar_addr(ctl.res_full), 2 * C::TILE);
+        tma_tile<D>(sK, &tmK, bar_addr(ctl.res_full), hk, kt * BM, b);
+        tma_tile<D>(sV, &tmV, bar_addr(ctl.res_full), hk, kt * BM, b);
+      }
+      ++uc;
+      const int nq = nt - kt;
+      for (int s = 0; s < g * nq; ++s) {
+        const int h = hk * g + s / nq, t = kt + s % nq, st = gs & 1;
+        if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
+        // L = lse * log2(e) and D of the tile's 128 query rows (rows past N: L = +inf, so P = 0).
+        float* vL = sVec + st * 2 * BM;
+        const size_t rbase = ((size_t)b * p.Hq + h) * p.N;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = lane * 4 + k, row = t * BM + c;
+          vL[c] = row < p.N ? p.lse[rbase + row] * kLog2e : INFINITY;
+          vL[BM + c] = row < p.N ? p.Dvec[rbase + row] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t sQ = sRing + st * 2 * C::TILE;
+          ptx::mbar_arrive_expect_tx(bar_addr(ctl.ring_full[st]), 2 * C::TILE);
+          tma_tile<D>(sQ, &tmQ, bar_addr(ctl.ring_full[st]), h, t * BM, b);
+          tma_tile<D>(sQ + C::TILE, &tmO, bar_addr(ctl.ring_full[st]), h, t * BM, b);
+        }
+        ++gs;
+      }
+    }
+    if (!ok && lane == 0) drain_copies(ctl, uc, gs);
+  } else if (!skip && warp == 1) {
+    // ------------------------------------------ MMA issuer --------------------------------
+    int gs = 0, uc = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
+      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+      if (u >= total) break;
+      const int kt = u / bh_count, nsteps = g * (nt - kt);
+      if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
+      ptx::tc_fence_after();
+      for (int s = 0; s < nsteps; ++s) {
+        const int st = gs & 1;
+        const uint32_t sQ = sRing + st * 2 * C::TILE, sO = sQ + C::TILE;
+        if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        issue_kmajor<D>(tmem + COL_S, sK, sQ, IDESC_S);    // S^T  = K' Q'^T
+        issue_kmajor<D>(tmem + COL_DP, sV, sO, IDESC_S);   // dP^T = V dO^T
+        ptx::mma_commit_w(bar_addr(ctl.s_full));
+        if (!(ok = wait_warp(bar_addr(ctl.p_ready), gs & 1, ctl, tmo))) break;
+        if (s == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sO, IDESC_ACC, s == 0);       // dV  += P^T dO
+        issue_acc<D>(tmem + COL_ACC + D, tmem + COL_DP, sQ, IDESC_ACC, s == 0);  // dK' += dS^T Q'
+        ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
+        ++gs;
+      }
+      if (!ok) break;
+      ptx::mma_commit_w(bar_addr(ctl.acc_full));
+      ptx::mma_commit_w(bar_addr(ctl.res_empty));
+      ++uc;
+    }
+    ptx::mma_commit_w(bar_addr(ctl.mma_done));
+    drain_bar(bar_addr(ctl.mma_done), 0, 100000000ull);
+  } else if (!skip && warp >= 4) {
+    // ------------------------------------------ elementwise + epilogue --------------------
+    const int wg = (warp - 4) / 4;             // query columns [64 wg, 64 wg + 64)
+    const int r = (warp & 3) * 32 + lane;      // key row in the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + COL_S, tP = tmem + lane_off + COL_DP, tA = tmem + lane_off + COL_ACC;
+    const float sl2 = p.scale_log2;
+    int gs = 0, uc = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
+      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+      if (u >= total) break;
+      const int kt = u / bh_count, bh = u - kt * bh_count, b = bh / p.Hkv, hk = bh - b * p.Hkv;
+      const int nq = nt - kt;
+      for (int s = 0; s < g * nq; ++s) {
+        const int t = kt + s % nq, st = gs & 1;
+        if (!(ok = wait_warp(bar_addr(ctl.s_full), gs & 1, ctl, tmo))) break;
+        if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        const float* vL = sVec + st * 2 * BM;
+        const bool diag = t == kt;  // query c of the tile sees key r iff c >= r
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int q0 = 64 * wg + 32 * c;
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(tS + q0, sv);
+          ptx::tmem_ld32(tP + q0, dv);
+          ptx::tmem_wait_ld();
+          uint32_t pp[16], dsp[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int q = q0 + 2 * e;
+            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -vL[q]));
+            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -vL[q + 1]));
+            if (diag) {
+              if (q < r) p0 = 0.f;
+              if (q + 1 < r) p1 = 0.f;
+            }
+            const float d0 = p0 * (__uint_as_float(dv[2 * e]) - vL[BM + q]);
+            const float d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - vL[BM + q + 1]);
+            pp[e] = pack2<BF16>(p0, p1);
+            dsp[e] = pack2<BF16>(d0, d1);
+          }
+          ptx::tmem_st16(tS + 64 * wg + 16 * c, pp);
+          ptx::tmem_st16(tP + 64 * wg + 16 * c, dsp);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(ctl.p_ready));
+        ++gs;
+      }
+      if (!ok) break;
+      // Epilogue: dV columns [wg d/2, wg d/2 + d/2); dK' pairs e in [wg d/4, wg d/4 + d/4) with e + d/2.
+      if (!(ok = wait_warp(bar_addr(ctl.acc_full), uc & 1, ctl, tmo))) break;
+      ptx::tc_fence_after();
+      constexpr int HV = D / 2, QK = D / 4;
+      uint32_t vv[HV], kx[QK], ky[QK];
+#pragma unroll
+      for (int c = 0; c < HV / 32; ++c) {
+        uint32_t tmp[32];
+        ptx::tmem_ld32(tA + wg * HV + 32 * c, tmp);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) vv[32 * c + e] = tmp[e];
+      }
+      if constexpr (QK == 32) {
+        ptx::tmem_ld32(tA + D + wg * QK, kx);
+        ptx::tmem_ld32(tA + D + HV + wg * QK, ky);
+      } else {
+        ptx::tmem_ld16(tA + D + wg * QK, kx);
+        ptx::tmem_ld16(tA + D + HV + wg * QK, ky);
+      }
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_addr(ctl.acc_empty));
+      ++uc;
+      const int j = kt * BM + r;
+      if (j < p.N) {
+        T* dvrow = reinterpret_cast<T*>(p.dv) + (((size_t)b * p.N + j) * p.Hkv + hk) * D;
+        T* dkrow = reinterpret_cast<T*>(p.dk) + (((size_t)b * p.N + j) * p.Hkv + hk) * D;
+#pragma unroll
+        for (int v = 0; v < HV / 8; ++v) {
+          uint4 w;
+          w.x = pack2<BF16>(__uint_as_float(vv[8 * v]), __uint_as_float(vv[8 * v + 1]));
+          w.y = pack2<BF16>(__uint_as_float(vv[8 * v + 2]), __uint_as_float(vv[8 * v + 3]));
+          w.z = pack2<BF16>(__uint_as_float(vv[8 * v + 4]), __uint_as_float(vv[8 * v + 5]));
+          w.w = pack2<BF16>(__uint_as_float(vv[8 * v + 6]), __uint_as_float(vv[8 * v + 7]));
+          *reinterpret_cast<uint4*>(dvrow + wg * HV + 8 * v) = w;
+        }
+        float x[QK], y[QK];
+#pragma unroll
+        for (int e = 0; e < QK; ++e) {
+          x[e] = __uint_as_float(kx[e]) * p.inv_sqrt_d;
+          y[e] = __uint_as_float(ky[e]) * p.inv_sqrt_d;
+          const int k = wg * QK + e;
+          unrotate_pair(x[e], y[e], (uint32_t)j, p.freqs.lo[k], p.freqs.hi[k]);
+        }
+#pragma unroll
+        for (int v = 0; v < QK / 8; ++v) {
+          uint4 wx, wy;
+          wx.x = pack2<BF16>(x[8 * v], x[8 * v + 1]);
+          wx.y = pack2<BF16>(x[8 * v + 2], x[8 * v + 3]);
+          wx.z = pack2<BF16>(x[8 * v + 4], x[8 * v + 5]);
+          wx.w = pack2<BF16>(x[8 * v + 6], x[8 * v + 7]);
+          wy.x = pack2<BF16>(y[8 * v], y[8 * v + 1]);
+          wy.y = pack2<BF16>(y[8 * v + 2], y[8 * v + 3]);
+          wy.z = pack2<BF16>(y[8 * v + 4], y[8 * v + 5]);
+          wy.w = pack2<BF16>(y[8 * v + 6], y[8 * v + 7]);
+          *reinterpret_cast<uint4*>(dkrow + wg * QK + 8 * v) = wx;
+          *reinterpret_cast<uint4*>(dkrow + HV + wg * QK + 8 * v) = wy;
+        }
+      }
+    }
+  }
+  bwd_teardown(ctl, warp, tmem);
+}
+
+// ================================ dQ ======================================================
+// Unit u: query tile t = nt - 1 - u / (B Hq) (descending: the longest units first) of head h, batch
+// b; steps: key tiles j = 0 .. t of KV head h / g.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ AttnBwdParams p) {
+  using C = BwdCfg<D>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr uint32_t AB = BF16 ? 1u : 0u;
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, BM, 0, 0);
+  constexpr uint32_t IDESC_ACC = ptx::idesc_f16(AB, BM, D, 0, 1);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  BwdCtrl& ctl = *reinterpret_cast<BwdCtrl*>(sgen + C::OFF_CTL);
+  const uint32_t sQ = sbase + C::OFF_RES, sO = sQ + C::TILE, sRing = sbase + C::OFF_RING;
+  const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+
+  bwd_setup<D>(ctl, warp);
+  const uint32_t tmem = ctl.tmem_base;
+  const bool skip = __shfl_sync(0xFFFFFFFFu, ctl.skip, 0) != 0;
+  const unsigned long long tmo = p.timeout_ns;
+  const int g = p.Hq / p.Hkv, nt = p.n_tiles, bh_count = p.B * p.Hq;
+  const int total = bh_count * nt;
+
+  if (!skip && warp == 0) {
+    // ------------------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      ptx::tma_prefetch_desc(&tmO);
+    }
+    int gs = 0, uc = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
+      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+      if (u >= total) break;
+      const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
+      if (!(ok = wait_warp(bar_addr(ctl.res_empty), (uc & 1) ^ 1, ctl, tmo))) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar_addr(ctl.res_full), 2 * C::TILE);
+        tma_tile<D>(sQ, &tmQ, bar_addr(ctl.res_full), h, t * BM, b);
+        tma_tile<D>(sO, &tmO, bar_addr(ctl.res_full), h, t * BM, b);
+      }
+      ++uc;
+      for (int j = 0; j <= t; ++j) {
+        const int st = gs & 1;
+        if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
+        if (lane == 0) {
+          const uint32_t sK = sRing + st * 2 * C::TILE;
+          ptx::mbar_arrive_expect_tx(bar_addr(ctl.ring_full[st]), 2 * C::TILE);
+          tma_tile<D>(sK, &tmK, bar_addr(ctl.ring_full[st]), h / g, j * BM, b);
+          tma_tile<D>(sK + C::TILE, &tmV, bar_addr(ctl.ring_full[st]), h / g, j * BM, b);
+        }
+        ++gs;
+      }
+    }
+    if (!ok && lane == 0) drain_copies(ctl, uc, gs);
+  } else if (!skip && warp == 1) {
+    // ------------------------------------------ MMA issuer --------------------------------
+    int gs = 0, uc = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
+      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+      if (u >= total) break;
+      const int t = nt - 1 - u / bh_count;
+      if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
+      ptx::tc_fence_after();
+      for (int j = 0; j <= t; ++j) {
+        const int st = gs & 1;
+        const uint32_t sK = sRing + st * 2 * C::TILE, sV = sK + C::TILE;
+        if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        issue_kmajor<D>(tmem + COL_S, sQ, sK, IDESC_S);   // S  = Q' K'^T
+        issue_kmajor<D>(tmem + COL_DP, sO, sV, IDESC_S);  // dP = dO V^T
+        ptx::mma_commit_w(bar_addr(ctl.s_full));
+        if (!(ok = wait_warp(bar_addr(ctl.p_ready), gs & 1, ctl, tmo))) break;
+        if (j == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sK, IDESC_ACC, j == 0);  // dQ' += dS K'
+        ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
+        ++gs;
+      }
+      if (!ok) break;
+      ptx::mma_commit_w(bar_addr(ctl.acc_full));
+      ptx::mma_commit_w(bar_addr(ctl.res_empty));
+      ++uc;
+    }
+    ptx::mma_commit_w(bar_addr(ctl.mma_done));
+    drain_bar(bar_addr(ctl.mma_done), 0, 100000000ull);
+  } else if (!skip && warp >= 4) {
+    // ------------------------------------------ elementwise + epilogue --------------------
+    const int wg = (warp - 4) / 4;             // key columns [64 wg, 64 wg + 64)
+    const int r = (warp & 3) * 32 + lane;      // query row in the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + COL_S, tP = tmem + lane_off + COL_DP, tA = tmem + lane_off + COL_ACC;
+    const float sl2 = p.scale_log2;
+    int gs = 0, uc = 0;
+    bool ok = true;
+    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
+      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+      if (u >= total) break;
+      const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
+      const int i = t * BM + r;
+      const size_t srow = ((size_t)b * p.Hq + h) * p.N + i;
+      const float L = i < p.N ? p.lse[srow] * kLog2e : INFINITY;  // rows past N: P = 0
+      const float Dr = i < p.N ? p.Dvec[srow] : 0.f;
+      for (int j = 0; j <= t; ++j) {
+        if (!(ok = wait_warp(bar_addr(ctl.s_full), gs & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        const bool diag = j == t;  // key c of the tile is visible to query r iff c <= r
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int k0 = 64 * wg + 32 * c;
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(tS + k0, sv);
+          ptx::tmem_ld32(tP + k0, dv);
+          ptx::tmem_wait_ld();
+          uint32_t dsp[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k = k0 + 2 * e;
+            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -L));
+            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -L));
+            if (diag) {
+              if (k > r) p0 = 0.f;
+              if (k + 1 > r) p1 = 0.f;
+            }
+            dsp[e] = pack2<BF16>(p0 * (__uint_as_float(dv[2 * e]) - Dr), p1 * (__uint_as_float(dv[2 * e + 1]) - Dr));
+          }
+          ptx::tmem_st16(tS + 64 * wg + 16 * c, dsp);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(ctl.p_ready));
+        ++gs;
+      }
+      if (!ok) break;
+      // Epilogue: dQ' pairs e in [wg d/4, wg d/4 + d/4) with e + d/2.
+      if (!(ok = wait_warp(bar_addr(ctl.acc_full), uc & 1, ctl, tmo))) break;
+      ptx::tc_fence_after();
+      constexpr int HV = D / 2, QK = D / 4;
+      uint32_t qx[QK], qy[QK];
+      if constexpr (QK == 32) {
+        ptx::tmem_ld32(tA + wg * QK, qx);
+        ptx::tmem_ld32(tA + HV + wg * QK, qy);
+      } else {
+        ptx::tmem_ld16(tA + wg * QK, qx);
+        ptx::tmem_ld16(tA + HV + wg * QK, qy);
+      }
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_addr(ctl.acc_empty));
+      ++uc;
+      if (i < p.N) {
+        T* dqrow = reinterpret_cast<T*>(p.dq) + (((size_t)b * p.N + i) * p.Hq + h) * D;
+        float x[QK], y[QK];
+#pragma unroll
+        for (int e = 0; e < QK; ++e) {
+          x[e] = __uint_as_float(qx[e]) * p.inv_sqrt_d;
+          y[e] = __uint_as_float(qy[e]) * p.inv_sqrt_d;
+          const int k = wg * QK + e;
+          unrotate_pair(x[e], y[e], (uint32_t)i, p.freqs.lo[k], p.freqs.hi[k]);
+        }
+#pragma unroll
+        for (int v = 0; v < QK / 8; ++v) {
+          uint4 wx, wy;
+          wx.x = pack2<BF16>(x[8 * v], x[8 * v + 1]);
+          wx.y = pack2<BF16>(x[8 * v + 2], x[8 * v + 3]);
+          wx.z = pack2<BF16>(x[8 * v + 4], x[8 * v + 5]);
+          wx.w = pack2<BF16>(x[8 * v + 6], x[8 * v + 7]);
+          wy.x = pack2<BF16>(y[8 * v], y[8 * v + 1]);
+          wy.y = pack2<BF16>(y[8 * v + 2], y[8 * v + 3]);
+          wy.z = pack2<BF16>(y[8 * v + 4], y[8 * v + 5]);
+          wy.w = pack2<BF16>(y[8 * v + 6], y[8 * v + 7]);
+          *reinterpret_cast<uint4*>(dqrow + wg * QK + 8 * v) = wx;
+          *reinterpret_cast<uint4*>(dqrow + HV + wg * QK + 8 * v) = wy;
+        }
+      }
+    }
+  }
+  bwd_teardown(ctl, warp, tmem);
+}
+
+// One CTA per SM (shared memory admits one), each walking its share of the units.  TAG separates
+// the per-device set-up caches of kernels that share a signature.
+template <int TAG, typename K>
+cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const AttnBwdMaps& m, const AttnBwdParams& p,
+                              cudaStream_t stream) {
+  constexpr int kMaxDevices = 64;
+  static int sm_count[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (sm_count[dev] == 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = n;
+  }
+  const int grid = units < sm_count[dev] ? units : sm_count[dev];
+  kernel<<<dim3((unsigned)grid), dim3(kThreads), smem, stream>>>(m.q, m.k, m.v, m.dout, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_impl(const AttnBwdMaps& m, const AttnBwdParams& p, cudaStream_t stream) {
+  const long long rows = (long long)p.B * p.N * p.Hq;
+  const long long blocks = (rows * 32 + 255) / 256;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  bwd_prep_kernel<D, BF16><<<dim3((unsigned)blocks), dim3(256), 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_persistent<2 * D + BF16 * 1>(bwd_dkdv_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hkv * p.n_tiles, m, p,
+                                          stream);
+  if (e != cudaSuccess) return e;
+  return launch_persistent<2 * D + BF16 * 1 + 1000>(bwd_dq_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hq * p.n_tiles,
+                                                   m, p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const AttnBwdMaps& maps, const AttnBwdParams& p, int d, bool bf16, cudaStream_t stream) {
+  if (p.n_tiles <= 0) return cudaSuccess;
+  if (d == 128) return bf16 ? launch_bwd_impl<128, true>(maps, p, stream) : launch_bwd_impl<128, false>(maps, p, stream);
+  return bf16 ? launch_bwd_impl<64, true>(maps, p, stream) : launch_bwd_impl<64, false>(maps, p, stream);
+}
+
+cudaError_t read_and_clear_bwd_status(unsigned int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_bwd_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  if (*value != 0u) {
+    const unsigned int zero = 0u;
+    e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+}  // namespace attnfuse

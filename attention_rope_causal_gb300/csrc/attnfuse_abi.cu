@@ -388,11 +388,100 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   return st;
 }
 
+size_t attnfuse_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return 0;
+  return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, N, Hkv, d), 256) +
+         round_up((size_t)B * Hq * N * sizeof(float), 256);
+}
+
+attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const void* v, const void* out,
+                                           const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                           int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, ATTNFUSE_FUSED, dtype);
+  if (st != ATTNFUSE_OK) return st;
+  if (!lse || !dout || !dq || !dk || !dv) return fail(ATTNFUSE_ERR_INVALID_ARG, "lse, dout, dq, dk and dv must be non-null");
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "dout, dq, dk and dv must be 16-byte aligned");
+  const size_t need = attnfuse_bwd_workspace_bytes(B, Hq, Hkv, N, d, dtype);
+  if (workspace) {
+    if (workspace_bytes < need)
+      return fail(ATTNFUSE_ERR_INVALID_ARG, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    if (!aligned(workspace, 256)) return fail(ATTNFUSE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  if ((st = check_device()) != ATTNFUSE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  void* owned = nullptr;
+  void* ws = workspace;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&owned, need, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(ATTNFUSE_ERR_NO_MEMORY, "cudaMallocAsync(%zu) for the backward workspace failed: %s", need,
+                  cudaGetErrorString(e));
+    }
+    ws = owned;
+  }
+  void* qr = ws;
+  void* kr = static_cast<char*>(ws) + round_up(tensor_bytes(B, N, Hq, d), 256);
+  float* Dv = reinterpret_cast<float*>(static_cast<char*>(kr) + round_up(tensor_bytes(B, N, Hkv, d), 256));
+
+  AttnBwdParams p;
+  std::memset(&p, 0, sizeof p);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.n_tiles = (N + 127) / 128;
+  p.out = out;
+  p.dout = dout;
+  p.lse = lse;
+  p.Dvec = Dv;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
+  p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  p.timeout_ns = kTimeoutNs;
+  rope_freqs_host(d, rope_base, &p.freqs);
+
+  // q' and k' (the forward's rotation, one launch over both), then D, dK/dV and dQ.
+  RopeApplyParams rp;
+  std::memset(&rp, 0, sizeof rp);
+  rp.job[0] = RopeJob{q, qr, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
+  rp.job[1] = RopeJob{k, kr, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
+  rp.njobs = 2;
+  rp.N = N;
+  rp.tokens = (long long)B * N;
+  rp.groups_total = rp.job[0].groups + rp.job[1].groups;
+  rp.rot_chunks = d / 16;
+  rp.freqs = p.freqs;
+  cudaError_t e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+  if (e != cudaSuccess) st = cuda_fail(e, "rope_apply launch");
+  AttnBwdMaps maps;
+  if (st == ATTNFUSE_OK && (st = encode_bnhd(&maps.q, qr, B, N, Hq, d, dtype, "q'")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.k, kr, B, N, Hkv, d, dtype, "k'")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.v, v, B, N, Hkv, d, dtype, "v")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.dout, dout, B, N, Hq, d, dtype, "dout")) == ATTNFUSE_OK) {
+    e = launch_attn_bwd(maps, p, d, dtype == ATTNFUSE_BF16, s);
+    if (e != cudaSuccess) st = cuda_fail(e, "backward launch");
+  }
+  if (owned) cudaFreeAsync(owned, s);
+  return st;
+}
+
 attnfuse_status_t attnfuse_device_status(void* stream) {
   g_err[0] = '\0';
   unsigned int v = 0;
   cudaError_t e = read_and_clear_device_status(&v, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "device status");
+  unsigned int vb = 0;
+  e = read_and_clear_bwd_status(&vb);
+  if (e != cudaSuccess) return cuda_fail(e, "device status (backward)");
+  v |= vb;
   if (v != 0u) return fail(ATTNFUSE_ERR_TIMEOUT, "a kernel barrier wait ran out (device status 0x%x)", v);
   return ATTNFUSE_OK;
 }

@@ -64,6 +64,34 @@ struct AttnMaps {
 cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
                             cudaStream_t stream, const char** why);
 
+// ---- backward kernels ------------------------------------------------------------------------
+
+struct AttnBwdParams {
+  int B, Hq, Hkv, N;
+  int n_tiles;            // ceil(N / 128)
+  const void* out;        // [B, N, Hq, d] forward output
+  const void* dout;       // [B, N, Hq, d] dL/dout
+  const float* lse;       // [B, Hq, N] forward log-sum-exp (natural log)
+  float* Dvec;            // [B, Hq, N] workspace: dout . out per row
+  void* dq;               // [B, N, Hq, d]
+  void* dk;               // [B, N, Hkv, d]
+  void* dv;               // [B, N, Hkv, d]
+  float scale_log2;       // log2(e) / sqrt(d)
+  float inv_sqrt_d;
+  unsigned long long timeout_ns;
+  RopeFreqs freqs;        // F_k, k < d/2 (half-split, rotary dimension d)
+};
+
+struct AttnBwdMaps {
+  CUtensorMap q, k, v, dout;  // q, k: the rotated copies
+};
+
+// Launches D = rowsum(dout * out), then the dK/dV and dQ kernels (rotated q, k already in place).
+cudaError_t launch_attn_bwd(const AttnBwdMaps& maps, const AttnBwdParams& p, int d, bool bf16, cudaStream_t stream);
+
+// Reads and clears the backward kernels' device status word (call after synchronising).
+cudaError_t read_and_clear_bwd_status(unsigned int* value);
+
 // Device status word written by kernels whose barrier waits ran out (bit 0).
 cudaError_t read_and_clear_device_status(unsigned int* value, cudaStream_t stream);
 

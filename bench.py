@@ -412,6 +412,20 @@ def run_sweep(args):
     return 0
 
 
+def bwd_fn(w, q, k, v, out, lse, stream):
+    """One backward step (attnfuse_rope_causal_bwd) on the forward's out / lse with a fixed dout and
+    preallocated gradients and workspace."""
+    import torch
+    from attention_rope_causal_gb300 import binding
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 1000)
+    dout = torch.randn(q.shape, generator=g).to(q.dtype).cuda()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, q.dtype), dtype=torch.uint8,
+                     device="cuda")
+    return lambda: binding.rope_causal_bwd(q, k, v, out, lse, dout, w.rope_base, dq=dq, dk=dk, dv=dv, workspace=ws,
+                                           stream=stream)
+
+
 def run_only(args):
     """Run one path alone (for profilers): W + K steps of `fused`, `prerotate` or `rope` with L2 flushes."""
     import torch
@@ -425,6 +439,9 @@ def run_only(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     if args.only == "rope":
         f = rope_pass_fn(w, stream)
+    elif args.only == "backward":
+        fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)()
+        f = bwd_fn(w, q, k, v, out, lse, stream)
     else:
         f = fwd_fn(w, q, k, v, out, lse, ws[args.only], args.only, stream)
     ms = time_steps(f, args.warmup + args.steps, flush, stream)[args.warmup:]
@@ -479,6 +496,11 @@ def run_ours(args):
     time_steps(rope_pass, args.warmup, flush, stream)
     rope_ms = statistics.median(time_steps(rope_pass, max(20, args.steps // 10), flush, stream))
     rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
+    # the backward pass on the forward's out / lse (a training step's second half)
+    fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)()
+    bwd = bwd_fn(w, q, k, v, out, lse, stream)
+    time_steps(bwd, args.warmup, flush, stream)
+    bwd_ms = statistics.median(time_steps(bwd, max(20, args.steps // 10), flush, stream))
     if binding.device_status() != 0:
         raise RuntimeError(f"device status: {binding.last_error()}")
 
@@ -507,6 +529,10 @@ def run_ours(args):
                       "rope_gbs": rope_bytes / (rope_ms / 1e3) / 1e9,
                       "rope_frac_of_hbm": rope_bytes / (rope_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                       "fused_over_prerotate": per_launch_ms / pre_ms},
+        "backward": {"ms": bwd_ms, "tflops": 2.5 * w.causal_flops / (bwd_ms / 1e3) / 1e12,
+                     "flops_note": "2.5 x the causal forward FLOPs (dS^T Q, dS K, P^T dO, dO V^T and the "
+                                   "recomputed Q K^T); the kernels compute Q K^T and dO V^T twice",
+                     "kernels": "rope_apply (q', k') + bwd_prep (D) + bwd_dkdv + bwd_dq"},
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
@@ -525,7 +551,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=inputs.LLAMA.name, choices=sorted(inputs.NAMED))
     ap.add_argument("--sweep", action="store_true", help="run the crossover sweep instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("fused", "prerotate", "rope"), help="time one path alone (for profilers)")
+    ap.add_argument("--only", choices=("fused", "prerotate", "rope", "backward"),
+                    help="time one path alone (for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

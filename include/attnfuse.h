@@ -146,6 +146,28 @@ attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, i
                                          attnfuse_dtype_t dtype, const attnfuse_rope_opts_t* opts, void* stream);
 
 /*
+ * Backward pass of attnfuse_rope_causal_fwd (N queries and keys, positions i and j, half-split
+ * rotation over all d entries): the gradients of a loss L with respect to q, k and v, given
+ * dout = dL/dout and the forward's out and lse ("AttnFuse Makes RoPE a First-Class Attention
+ * Compilation Operation", paragraph 3, names the training step this serves; the chain rule through
+ * paragraphs 1-2's rotation, causal mask and softmax).  With q' = R(i) q, k' = R(j) k,
+ * P = softmax(q'k'^T / sqrt(d)) causal and D_i = dout_i . out_i:
+ *     dv = P^T dout,  dS = P o (dout v^T - D),  dq = R^T (dS k' / sqrt(d)),  dk = R^T (dS^T q' / sqrt(d))
+ * (GQA: a KV head's dk, dv sum over its query heads; L's dependence on lse is not propagated).
+ * Layouts as the forward: q, out, dout, dq [B, N, Hq, d]; k, v, dk, dv [B, N, Hkv, d]; lse
+ * [B, Hq, N] float32 (required).  Outputs must not overlap the inputs.  `workspace` holds
+ * attnfuse_bwd_workspace_bytes(...) bytes (rotated q and k, and D); NULL allocates with
+ * cudaMallocAsync / cudaFreeAsync on `stream`.  Errors as for the forward.
+ */
+attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const void* v, const void* out,
+                                           const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                           int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attnfuse_rope_causal_bwd needs (0 for invalid arguments). */
+size_t attnfuse_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word.  Returns
  * ATTNFUSE_ERR_TIMEOUT if a kernel's barrier wait ran out since the last read, ATTNFUSE_ERR_CUDA if
  * synchronising failed (e.g. a device fault), ATTNFUSE_OK otherwise.

@@ -141,6 +141,31 @@ def test_workspace_bytes_with_more_keys(lib):
     assert binding.workspace_bytes(1, 4, 2, 300, 128, "prerotate", kv_len=1000) == q + k
 
 
+def bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, Hq=4, Hkv=2, N=128,
+             d=64, base=1e4, dtype=0, ws=None, wsb=0)
+    a.update(kw)
+    return lib.attnfuse_rope_causal_bwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["dout"], a["dq"], a["dk"],
+                                        a["dv"], a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["base"], a["dtype"],
+                                        a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [({"lse": None}, 1), ({"dout": None}, 1), ({"dq": None}, 1), ({"dv": FAKE + 8}, 1),
+                                        ({"d": 96}, 2), ({"Hq": 3}, 1), ({"N": 0}, 1), ({"dtype": 7}, 1),
+                                        ({"ws": FAKE, "wsb": 64}, 1), ({"base": 0.5}, 1)])
+def test_backward_arguments_are_checked_before_the_device(lib, kw, status):
+    assert bwd(lib, **kw) == status
+
+
+def test_backward_workspace_bytes(lib):
+    q = 1 * 4096 * 32 * 128 * 2
+    k = 1 * 4096 * 8 * 128 * 2
+    dvec = 32 * 4096 * 4
+    assert lib.attnfuse_bwd_workspace_bytes(1, 32, 8, 4096, 128, 0) == q + k + dvec
+    assert lib.attnfuse_bwd_workspace_bytes(1, 32, 8, 4096, 96, 0) == 0
+    assert lib.attnfuse_bwd_workspace_bytes(0, 32, 8, 4096, 128, 0) == 0
+
+
 def test_valid_call_without_gpu_fails_cleanly(lib):
     import torch
     if torch.cuda.is_available():
