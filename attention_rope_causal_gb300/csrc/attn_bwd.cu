@@ -67,8 +67,8 @@ struct BwdCfg {
 struct __align__(8) BwdCtrl {
   uint64_t res_full, res_empty;          // resident pair landed / free again
   uint64_t ring_full[2], ring_empty[2];  // ring stage landed / free again
-  uint64_t s_full;                       // S and dP of this step are in tensor memory
-  uint64_t p_ready;                      // the elementwise warps wrote P / dS (256 arrivals)
+  uint64_t s_full[2];                    // S and dP of half h of this step are in tensor memory
+  uint64_t p_ready[2];                   // warpgroup h wrote its P / dS (128 arrivals)
   uint64_t acc_full;                     // the unit's accumulators are complete
   uint64_t acc_empty;                    // the epilogue has read them (256 arrivals)
   uint64_t mma_done;
@@ -173,9 +173,10 @@ __device__ __forceinline__ void unrotate_pair(float& x, float& y, uint32_t pos, 
   y = yr;
 }
 
-// S-like product into tensor memory: D[dst] = A B^T with A, B 128-row tiles of d columns in shared
-// memory, both K-major (the layout TMA writes).  Consecutive K-steps add a constant to the start
-// address field (offsets stay inside the 14-bit field).
+// S-like product into tensor memory: D[dst] = A B^T with A a 128-row and B a 64-row slice of tiles
+// of d columns in shared memory, both K-major (the layout TMA writes; a 64-row slice starts 8 KB
+// into each 128-row box).  Consecutive K-steps add a constant to the start address field (offsets
+// stay inside the 14-bit field).
 template <int D>
 __device__ __forceinline__ void issue_kmajor(uint32_t dst, uint32_t a, uint32_t b, uint32_t idesc) {
   const uint64_t da = ptx::sdesc_sw128(a, 16, 1024), db = ptx::sdesc_sw128(b, 16, 1024);
@@ -189,14 +190,20 @@ __device__ __forceinline__ void issue_kmajor(uint32_t dst, uint32_t a, uint32_t 
 // Accumulation D[dst] (+)= A B with A the packed 16-bit 128 x 128 matrix in tensor memory (K16 step
 // kk in the 8 columns at a + 64 (kk / 4) + 8 (kk % 4): each warpgroup's half sits over its own S /
 // dP columns) and B a 128-row tile in shared memory read MN-major (N = d columns, K = its rows).
+// Only the K-steps of half `half` (K rows [64 half, 64 half + 64)) are issued.
 template <int D>
-__device__ __forceinline__ void issue_acc(uint32_t dst, uint32_t a, uint32_t b, uint32_t idesc, bool first) {
+__device__ __forceinline__ void issue_acc(uint32_t dst, uint32_t a, uint32_t b, uint32_t idesc, int half,
+                                          bool first) {
   const uint64_t db = ptx::sdesc_sw128(b, kBoxBytes, 1024);
 #pragma unroll
-  for (int kk = 0; kk < BM / 16; ++kk)
+  for (int k = 0; k < 4; ++k) {
+    const int kk = 4 * half + k;
     ptx::mma_ts_w(dst, a + 64 * (kk / 4) + 8 * (kk % 4), db + (uint64_t)(kk * (2048 >> 4)), idesc,
-                  (!first || kk > 0) ? 1u : 0u);
+                  (!first || k > 0) ? 1u : 0u);
+  }
 }
+
+constexpr uint32_t kHalfRows = 64 * 128;  // byte offset of row 64 inside a 128-row box
 
 // Common prologue of both kernels: barriers, tensor memory, skip flag.
 template <int D>
@@ -208,8 +215,10 @@ __device__ __forceinline__ void bwd_setup(BwdCtrl& ctl, int warp) {
       ptx::mbar_init(bar_addr(ctl.ring_full[s]), 1);
       ptx::mbar_init(bar_addr(ctl.ring_empty[s]), 1);
     }
-    ptx::mbar_init(bar_addr(ctl.s_full), 1);
-    ptx::mbar_init(bar_addr(ctl.p_ready), 256);
+    for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(bar_addr(ctl.s_full[h]), 1);
+      ptx::mbar_init(bar_addr(ctl.p_ready[h]), 128);
+    }
     ptx::mbar_init(bar_addr(ctl.acc_full), 1);
     ptx::mbar_init(bar_addr(ctl.acc_empty), 256);
     ptx::mbar_init(bar_addr(ctl.mma_done), 1);
@@ -263,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = BwdCfg<D>;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr uint32_t AB = BF16 ? 1u : 0u;
-  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, BM, 0, 0);
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, 64, 0, 0);  // 128 x 64 halves
   constexpr uint32_t IDESC_ACC = ptx::idesc_f16(AB, BM, D, 0, 1);
 
   extern __shared__ uint8_t smem_raw[];
@@ -330,28 +339,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) drain_copies(ctl, uc, gs);
   } else if (!skip && warp == 1) {
     // ------------------------------------------ MMA issuer --------------------------------
+    // Two halves per step (queries 0..63 -> warpgroup 0, 64..127 -> warpgroup 1), software
+    // pipelined: S^T, dP^T of one half run on the tensor cores while the other half's warpgroup
+    // computes P^T, dS^T.  Order per step g: [dV, dK of half 0 of g] [S^T, dP^T of half 0 of g+1]
+    // [dV, dK of half 1 of g] [S^T, dP^T of half 1 of g+1].
     int gs = 0, uc = 0;
     bool ok = true;
+    auto issue_s = [&](int g_step, int half) {
+      const uint32_t sQ = sRing + (g_step & 1) * 2 * C::TILE + half * kHalfRows, sO = sQ + C::TILE;
+      issue_kmajor<D>(tmem + COL_S + 64 * half, sK, sQ, IDESC_S);    // S^T  = K' Q'^T  (64 queries)
+      issue_kmajor<D>(tmem + COL_DP + 64 * half, sV, sO, IDESC_S);   // dP^T = V dO^T
+      ptx::mma_commit_w(bar_addr(ctl.s_full[half]));
+    };
     for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
       const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
       if (u >= total) break;
       const int kt = u / bh_count, nsteps = g * (nt - kt);
       if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
+      if (!(ok = wait_warp(bar_addr(ctl.ring_full[gs & 1]), (gs >> 1) & 1, ctl, tmo))) break;
       ptx::tc_fence_after();
+      issue_s(gs, 0);
+      issue_s(gs, 1);
       for (int s = 0; s < nsteps; ++s) {
         const int st = gs & 1;
         const uint32_t sQ = sRing + st * 2 * C::TILE, sO = sQ + C::TILE;
-        if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
-        ptx::tc_fence_after();
-        issue_kmajor<D>(tmem + COL_S, sK, sQ, IDESC_S);    // S^T  = K' Q'^T
-        issue_kmajor<D>(tmem + COL_DP, sV, sO, IDESC_S);   // dP^T = V dO^T
-        ptx::mma_commit_w(bar_addr(ctl.s_full));
-        if (!(ok = wait_warp(bar_addr(ctl.p_ready), gs & 1, ctl, tmo))) break;
-        if (s == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo))) break;
-        ptx::tc_fence_after();
-        issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sO, IDESC_ACC, s == 0);       // dV  += P^T dO
-        issue_acc<D>(tmem + COL_ACC + D, tmem + COL_DP, sQ, IDESC_ACC, s == 0);  // dK' += dS^T Q'
-        ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
+        const bool more = s + 1 < nsteps;
+        for (int half = 0; half < 2; ++half) {
+          if (!(ok = wait_warp(bar_addr(ctl.p_ready[half]), gs & 1, ctl, tmo))) break;
+          if (s == 0 && half == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo)))
+            break;
+          ptx::tc_fence_after();
+          const bool first = s == 0 && half == 0;
+          issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sO, IDESC_ACC, half, first);       // dV  += P^T dO
+          issue_acc<D>(tmem + COL_ACC + D, tmem + COL_DP, sQ, IDESC_ACC, half, first);  // dK' += dS^T Q'
+          if (half == 1) ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
+          if (more) {
+            if (half == 0 && !(ok = wait_warp(bar_addr(ctl.ring_full[(gs + 1) & 1]), ((gs + 1) >> 1) & 1, ctl, tmo)))
+              break;
+            ptx::tc_fence_after();
+            issue_s(gs + 1, half);
+          }
+        }
+        if (!ok) break;
         ++gs;
       }
       if (!ok) break;
@@ -377,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = nt - kt;
       for (int s = 0; s < g * nq; ++s) {
         const int t = kt + s % nq, st = gs & 1;
-        if (!(ok = wait_warp(bar_addr(ctl.s_full), gs & 1, ctl, tmo))) break;
+        if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
         if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
         ptx::tc_fence_after();
         const float* vL = sVec + st * 2 * BM;
@@ -409,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(ctl.p_ready));
+        ptx::mbar_arrive(bar_addr(ctl.p_ready[wg]));
         ++gs;
       }
       if (!ok) break;
@@ -489,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = BwdCfg<D>;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr uint32_t AB = BF16 ? 1u : 0u;
-  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, BM, 0, 0);
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(AB, BM, 64, 0, 0);  // 128 x 64 halves
   constexpr uint32_t IDESC_ACC = ptx::idesc_f16(AB, BM, D, 0, 1);
 
   extern __shared__ uint8_t smem_raw[];
@@ -544,27 +573,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) drain_copies(ctl, uc, gs);
   } else if (!skip && warp == 1) {
     // ------------------------------------------ MMA issuer --------------------------------
+    // Two halves per key tile (keys 0..63 -> warpgroup 0, 64..127 -> warpgroup 1), pipelined as in
+    // the dK/dV kernel: [dQ' += dS K' of half 0 of j] [S, dP of half 0 of j+1] [half 1 of j] ...
     int gs = 0, uc = 0;
     bool ok = true;
+    auto issue_s = [&](int g_step, int half) {
+      const uint32_t sK = sRing + (g_step & 1) * 2 * C::TILE + half * kHalfRows, sV = sK + C::TILE;
+      issue_kmajor<D>(tmem + COL_S + 64 * half, sQ, sK, IDESC_S);   // S  = Q' K'^T  (64 keys)
+      issue_kmajor<D>(tmem + COL_DP + 64 * half, sO, sV, IDESC_S);  // dP = dO V^T
+      ptx::mma_commit_w(bar_addr(ctl.s_full[half]));
+    };
     for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
       const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
       if (u >= total) break;
       const int t = nt - 1 - u / bh_count;
       if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
+      if (!(ok = wait_warp(bar_addr(ctl.ring_full[gs & 1]), (gs >> 1) & 1, ctl, tmo))) break;
       ptx::tc_fence_after();
+      issue_s(gs, 0);
+      issue_s(gs, 1);
       for (int j = 0; j <= t; ++j) {
         const int st = gs & 1;
-        const uint32_t sK = sRing + st * 2 * C::TILE, sV = sK + C::TILE;
-        if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
-        ptx::tc_fence_after();
-        issue_kmajor<D>(tmem + COL_S, sQ, sK, IDESC_S);   // S  = Q' K'^T
-        issue_kmajor<D>(tmem + COL_DP, sO, sV, IDESC_S);  // dP = dO V^T
-        ptx::mma_commit_w(bar_addr(ctl.s_full));
-        if (!(ok = wait_warp(bar_addr(ctl.p_ready), gs & 1, ctl, tmo))) break;
-        if (j == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo))) break;
-        ptx::tc_fence_after();
-        issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sK, IDESC_ACC, j == 0);  // dQ' += dS K'
-        ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
+        const uint32_t sK = sRing + st * 2 * C::TILE;
+        const bool more = j < t;
+        for (int half = 0; half < 2; ++half) {
+          if (!(ok = wait_warp(bar_addr(ctl.p_ready[half]), gs & 1, ctl, tmo))) break;
+          if (j == 0 && half == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo)))
+            break;
+          ptx::tc_fence_after();
+          issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sK, IDESC_ACC, half, j == 0 && half == 0);  // dQ' += dS K'
+          if (half == 1) ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
+          if (more) {
+            if (half == 0 && !(ok = wait_warp(bar_addr(ctl.ring_full[(gs + 1) & 1]), ((gs + 1) >> 1) & 1, ctl, tmo)))
+              break;
+            ptx::tc_fence_after();
+            issue_s(gs + 1, half);
+          }
+        }
+        if (!ok) break;
         ++gs;
       }
       if (!ok) break;
@@ -592,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float L = i < p.N ? p.lse[srow] * kLog2e : INFINITY;  // rows past N: P = 0
       const float Dr = i < p.N ? p.Dvec[srow] : 0.f;
       for (int j = 0; j <= t; ++j) {
-        if (!(ok = wait_warp(bar_addr(ctl.s_full), gs & 1, ctl, tmo))) break;
+        if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
         ptx::tc_fence_after();
         const bool diag = j == t;  // key c of the tile is visible to query r iff c <= r
 #pragma unroll
@@ -618,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(ctl.p_ready));
+        ptx::mbar_arrive(bar_addr(ctl.p_ready[wg]));
         ++gs;
       }
       if (!ok) break;
