@@ -123,37 +123,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return Pack<BF16>::pack(lo, hi);
 }
 
-// D[b, h, i] = dO_i . O_i in fp32: one warp per (b, i, h) row of d elements.
+// D[b, h, i] = dO_i . O_i in fp32.  A thread takes 8 elements (one 16-byte load of each tensor), d/8
+// consecutive threads a row, so a warp reads whole 256-byte rows with 16-byte accesses; the group
+// reduces with shuffles.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ AttnBwdParams p) {
-  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  constexpr int PER = D / 32;  // elements per lane: 4 (d = 128) or 2 (d = 64)
-  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
+  constexpr int TPR = D / 8;  // threads per row: 16 (d = 128) or 8 (d = 64)
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = tid / TPR;
+  const int part = (int)(tid % TPR);
   const long long rows = (long long)p.B * p.N * p.Hq;
-  if (row >= rows) return;
-  const T* o = reinterpret_cast<const T*>(p.out) + row * D + lane * PER;
-  const T* g = reinterpret_cast<const T*>(p.dout) + row * D + lane * PER;
   float acc = 0.f;
-  if constexpr (PER == 4) {
-    const uint2 ov = *reinterpret_cast<const uint2*>(o), gv = *reinterpret_cast<const uint2*>(g);
-    float a0, a1, b0, b1;
-    Pack<BF16>::unpack(ov.x, a0, a1);
-    Pack<BF16>::unpack(gv.x, b0, b1);
-    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
-    Pack<BF16>::unpack(ov.y, a0, a1);
-    Pack<BF16>::unpack(gv.y, b0, b1);
-    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
-  } else {
-    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o), gv = *reinterpret_cast<const uint32_t*>(g);
-    float a0, a1, b0, b1;
-    Pack<BF16>::unpack(ov, a0, a1);
-    Pack<BF16>::unpack(gv, b0, b1);
-    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
+  if (row < rows) {
+    const uint4 ov = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.out) + (row * D + part * 8) * 2);
+    const uint4 gv = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.dout) + (row * D + part * 8) * 2);
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a0, a1, b0, b1;
+      Pack<BF16>::unpack(ow[k], a0, a1);
+      Pack<BF16>::unpack(gw[k], b0, b1);
+      acc = fmaf(a0, b0, fmaf(a1, b1, acc));
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  if (lane == 0) {
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (row < rows && part == 0) {
     // row = (b * N + i) * Hq + h  ->  D[(b * Hq + h) * N + i]
     const int h = (int)(row % p.Hq);
     const long long bi = row / p.Hq;
@@ -741,7 +736,7 @@ cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const AttnBwdM
 template <int D, bool BF16>
 cudaError_t launch_bwd_impl(const AttnBwdMaps& m, const AttnBwdParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.B * p.N * p.Hq;
-  const long long blocks = (rows * 32 + 255) / 256;
+  const long long blocks = (rows * (D / 8) + 255) / 256;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   bwd_prep_kernel<D, BF16><<<dim3((unsigned)blocks), dim3(256), 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
