@@ -457,7 +457,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const AttnParams& p) {
       break;                                                                     \
     else if (const Unit U = decode_unit<VARIANT>(u_, p); true)
 
-template <int D, bool ROTATE, bool BF16, bool VARIANT>
+template <int D, bool ROTATE, bool BF16, bool VARIANT, bool ROT_K>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
@@ -569,12 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < VST; ++s)
           if (gv > s) drain_bar(bar_addr(ctl.v_full[s]), ((gv - 1 - s) / VST) & 1, drain);
       }
-    } else if (!skip && warp == 1 && (!ROTATE || lane == 0)) {
+    } else if (!skip && warp == 1 && (!(ROTATE && ROT_K) || lane == 0)) {
       // ================================ MMA issuer ============================================
       // Descriptors are built once per operand tile; consecutive K-steps only add a constant to the
       // start-address field (offsets stay inside the 14-bit field), so nothing but an add separates
       // two tcgen05.mma issues.
-      using I = Issue<!ROTATE>;
+      using I = Issue<!(ROTATE && ROT_K)>;
       auto issue_S = [&](int iq, uint32_t kbase) {
         const uint64_t dq = ptx::sdesc_sw128(sQ + iq * C::TILE, 16, 1024);
         const uint64_t dk = ptx::sdesc_sw128(kbase, 16, 1024);
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         for (int i = 0; i < U.n_kt && ok; ++i) {
           const int ks = gk % KST, kph = (gk / KST) & 1;
-          if (!(ok = I::wait(bar_addr(ROTATE ? ctl.k_ready[ks] : ctl.k_full[ks]), kph, ctl, tmo))) break;
+          if (!(ok = I::wait(bar_addr(ROTATE && ROT_K ? ctl.k_ready[ks] : ctl.k_full[ks]), kph, ctl, tmo))) break;
           ptx::tc_fence_after();
           const uint32_t kbase = sK + ks * C::TILE;
           const int vs = gv % VST, vph = (gv / VST) & 1;
@@ -764,45 +764,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
         int gk = 0, uc = 0;
         bool ok = true;
-        FOR_EACH_UNIT(U) {
-          RopeCS8 kcs;
-          for (int i = 0; i < U.n_kt && ok; ++i) {
-            if (i % kReseed == 0) rope_cs8_exact((uint32_t)(i * BN + r0), sfreq, sfreq + 64, ck * 8, kcs);
-            const int ks = gk % KST, kph = (gk / KST) & 1;
-            if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
-            ++gk;
-            // Half-split over all d entries: the tuned path; other RoPE forms (VARIANT kernels) take
-            // rotate_tile_variant.
+        // The unit's query tiles, once they have landed.
+        auto rotate_q = [&](const Unit& U) -> bool {
+          if (!wait_bar_warp(bar_addr(ctl.q_full), uc & 1, ctl, tmo)) return false;
+          ++uc;
+          for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
+            RopeCS8 qcs;
+            // Query row i sits at position q_off + i.  Calls with q_off != 0 run the VARIANT
+            // kernel: the term alone made the default kernel 1.4% slower on GB300.
+            int qpos0 = U.row(tq) + r0;
+            if constexpr (VARIANT) qpos0 += *reinterpret_cast<volatile int*>(&ctl.q_off);
+            rope_cs8_exact((uint32_t)qpos0, sfreq, sfreq + 64, ck * 8, qcs);
             if constexpr (VARIANT)
-              rotate_tile_variant<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step, p.rot_chunks, p.interleaved != 0,
-                                           p.kpos ? p.kpos + (size_t)U.b * p.Nk + i * BN : nullptr, p.Nk - i * BN,
-                                           sfreq);
+              rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0,
+                                           p.qpos ? p.qpos + (size_t)U.b * p.N + U.row(tq) : nullptr,
+                                           p.N - U.row(tq), sfreq);
             else
-              rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
-            if (i == 0) {
-              if (!(ok = wait_bar_warp(bar_addr(ctl.q_full), uc & 1, ctl, tmo))) break;
-              ++uc;
-              for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
-                RopeCS8 qcs;
-                // Query row i sits at position q_off + i.  Calls with q_off != 0 run the VARIANT
-                // kernel: the term alone made the default kernel 1.4% slower on GB300.
-                int qpos0 = U.row(tq) + r0;
-                if constexpr (VARIANT) qpos0 += *reinterpret_cast<volatile int*>(&ctl.q_off);
-                rope_cs8_exact((uint32_t)qpos0, sfreq, sfreq + 64, ck * 8, qcs);
-                if constexpr (VARIANT)
-                  rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0,
-                                               p.qpos ? p.qpos + (size_t)U.b * p.N + U.row(tq) : nullptr,
-                                               p.N - U.row(tq), sfreq);
-                else
-                  rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
-              }
-              ptx::fence_proxy_async_smem();
-              ptx::mbar_arrive(bar_addr(ctl.q_ready));
-            }
+              rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
           }
-          if (!ok) break;
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(bar_addr(ctl.q_ready));
+          return true;
+        };
+        if constexpr (!ROT_K) {
+          // Split mode: K arrives rotated (the pre-rotation pass); only the query tiles turn here.
+          FOR_EACH_UNIT(U) {
+            if (!(ok = rotate_q(U))) break;
+          }
+        } else {
+          FOR_EACH_UNIT(U) {
+            RopeCS8 kcs;
+            for (int i = 0; i < U.n_kt && ok; ++i) {
+              if (i % kReseed == 0) rope_cs8_exact((uint32_t)(i * BN + r0), sfreq, sfreq + 64, ck * 8, kcs);
+              const int ks = gk % KST, kph = (gk / KST) & 1;
+              if (!(ok = wait_bar_warp(bar_addr(ctl.k_full[ks]), kph, ctl, tmo))) break;
+              ++gk;
+              // Half-split over all d entries: the tuned path; other RoPE forms (VARIANT kernels) take
+              // rotate_tile_variant.
+              if constexpr (VARIANT)
+                rotate_tile_variant<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step, p.rot_chunks, p.interleaved != 0,
+                                             p.kpos ? p.kpos + (size_t)U.b * p.Nk + i * BN : nullptr, p.Nk - i * BN,
+                                             sfreq);
+              else
+                rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
+              ptx::fence_proxy_async_smem();
+              ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
+              if (i == 0 && !(ok = rotate_q(U))) break;
+            }
+            if (!ok) break;
+          }
         }
       }
     }
@@ -839,9 +849,9 @@ __global__ void diag_wait_timeout_kernel(unsigned long long timeout_ns) {
   __syncthreads();
 }
 
-template <int D, bool ROTATE, bool BF16, bool VARIANT>
+template <int D, bool ROTATE, bool BF16, bool VARIANT, bool ROT_K>
 cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t stream, const char** why) {
-  auto kernel = attn_fwd_kernel<D, ROTATE, BF16, VARIANT>;
+  auto kernel = attn_fwd_kernel<D, ROTATE, BF16, VARIANT, ROT_K>;
   constexpr int kMaxDevices = 64;
   static int configured[kMaxDevices] = {0};
   static int sm_count[kMaxDevices] = {0};
@@ -874,39 +884,34 @@ cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t s
   return cudaGetLastError();
 }
 
+// Rotation mode r: 0 none (pre-rotated Q and K), 1 Q and K (fused), 2 Q only (split: K pre-rotated).
+template <int D, bool BF16, bool VARIANT>
+cudaError_t launch_mode(const AttnMaps& maps, const AttnParams& p, int r, cudaStream_t stream, const char** why) {
+  if (r == 1) return launch_one<D, true, BF16, VARIANT, true>(maps, p, stream, why);
+  if (r == 2) return launch_one<D, true, BF16, VARIANT, false>(maps, p, stream, why);
+  return launch_one<D, false, BF16, VARIANT, false>(maps, p, stream, why);
+}
+
+template <int D>
+cudaError_t launch_d(const AttnMaps& maps, const AttnParams& p, bool bf16, bool variant, int r, cudaStream_t stream,
+                     const char** why) {
+  if (variant)
+    return bf16 ? launch_mode<D, true, true>(maps, p, r, stream, why) : launch_mode<D, false, true>(maps, p, r, stream, why);
+  return bf16 ? launch_mode<D, true, false>(maps, p, r, stream, why) : launch_mode<D, false, false>(maps, p, r, stream, why);
+}
+
 }  // namespace
 
-cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
-                            cudaStream_t stream, const char** why) {
+cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate_q,
+                            bool rotate_k, cudaStream_t stream, const char** why) {
   if (p.total_units <= 0) return cudaSuccess;
-  // The default kernels handle N == Nk and (fused) the half-split form over all d entries at
-  // positions i and j; every other case takes the VARIANT instantiation.
-  const bool variant = p.q_off != 0 || (rotate && (!(p.rot_chunks == d / 16 && p.interleaved == 0) ||
-                                                   p.qpos != nullptr || p.kpos != nullptr));
-  if (d == 128) {
-    if (variant && rotate)
-      return bf16 ? launch_one<128, true, true, true>(maps, p, stream, why)
-                  : launch_one<128, true, false, true>(maps, p, stream, why);
-    if (variant)
-      return bf16 ? launch_one<128, false, true, true>(maps, p, stream, why)
-                  : launch_one<128, false, false, true>(maps, p, stream, why);
-    if (rotate)
-      return bf16 ? launch_one<128, true, true, false>(maps, p, stream, why)
-                  : launch_one<128, true, false, false>(maps, p, stream, why);
-    return bf16 ? launch_one<128, false, true, false>(maps, p, stream, why)
-                : launch_one<128, false, false, false>(maps, p, stream, why);
-  }
-  if (variant && rotate)
-    return bf16 ? launch_one<64, true, true, true>(maps, p, stream, why)
-                : launch_one<64, true, false, true>(maps, p, stream, why);
-  if (variant)
-    return bf16 ? launch_one<64, false, true, true>(maps, p, stream, why)
-                : launch_one<64, false, false, true>(maps, p, stream, why);
-  if (rotate)
-    return bf16 ? launch_one<64, true, true, false>(maps, p, stream, why)
-                : launch_one<64, true, false, false>(maps, p, stream, why);
-  return bf16 ? launch_one<64, false, true, false>(maps, p, stream, why)
-              : launch_one<64, false, false, false>(maps, p, stream, why);
+  // The default kernels handle N == Nk and the half-split form over all d entries at positions i
+  // and j; every other case takes the VARIANT instantiation.
+  const bool variant = p.q_off != 0 || (rotate_q && (!(p.rot_chunks == d / 16 && p.interleaved == 0) ||
+                                                     p.qpos != nullptr || p.kpos != nullptr));
+  const int r = !rotate_q ? 0 : (rotate_k ? 1 : 2);
+  return d == 128 ? launch_d<128>(maps, p, bf16, variant, r, stream, why)
+                  : launch_d<64>(maps, p, bf16, variant, r, stream, why);
 }
 
 cudaError_t read_and_clear_device_status(unsigned int* value, cudaStream_t stream) {

@@ -148,8 +148,8 @@ attnfuse_status_t validate_fwd(const void* q, const void* k, const void* v, cons
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "B, Hq, Hkv, N must be >= 1");
   if (N >= kMaxN) return fail(ATTNFUSE_ERR_INVALID_ARG, "N=%d exceeds the supported maximum %d", N, kMaxN - 1);
   if (Hq % Hkv != 0) return fail(ATTNFUSE_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE && mode != ATTNFUSE_AUTO)
-    return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0), prerotate (1) or auto (2)", (int)mode);
+  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE && mode != ATTNFUSE_AUTO && mode != ATTNFUSE_SPLIT)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0), prerotate (1), auto (2) or split (3)", (int)mode);
   attnfuse_status_t st = check_dtype_d(d, dtype);
   if (st != ATTNFUSE_OK) return st;
   if ((st = check_base(base)) != ATTNFUSE_OK) return st;
@@ -214,6 +214,7 @@ size_t attnfuse_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfus
   const int Nk = (opts && opts->kv_len) ? opts->kv_len : N;
   if (Nk < N) return 0;
   if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
+  if (mode == ATTNFUSE_SPLIT) return round_up(tensor_bytes(B, Nk, Hkv, d), 256);
   if (mode != ATTNFUSE_PREROTATE) return 0;
   return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, Nk, Hkv, d), 256);
 }
@@ -319,7 +320,37 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   const void* qa = q;
   const void* ka = k;
   void* owned = nullptr;
-  if (mode == ATTNFUSE_PREROTATE) {
+  if (mode == ATTNFUSE_SPLIT) {
+    // K (re-read by every query tile that needs it) is rotated once into the workspace; the
+    // attention kernel rotates each query tile, which it reads once, on chip.
+    void* ws = workspace;
+    if (!ws) {
+      cudaError_t e = cudaMallocAsync(&owned, need, s);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ATTNFUSE_ERR_NO_MEMORY, "cudaMallocAsync(%zu) for the rotated K failed: %s", need, cudaGetErrorString(e));
+      }
+      ws = owned;
+    }
+    RopeApplyParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    rp.job[0] = RopeJob{k, ws, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    rp.njobs = 1;
+    rp.N = Nk;
+    rp.tokens = (long long)B * Nk;
+    rp.groups_total = rp.job[0].groups;
+    rp.pos = o.kpos;
+    rp.pos_off = 0;
+    rp.rot_chunks = p.rot_chunks;
+    rp.interleaved = p.interleaved;
+    rp.freqs = p.freqs;
+    cudaError_t e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+    if (e != cudaSuccess) {
+      if (owned) cudaFreeAsync(owned, s);
+      return cuda_fail(e, "rope_apply launch");
+    }
+    ka = ws;
+  } else if (mode == ATTNFUSE_PREROTATE) {
     void* ws = workspace;
     if (!ws) {
       cudaError_t e = cudaMallocAsync(&owned, need, s);
@@ -381,7 +412,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
       (st = encode_bnhd(&maps.k, ka, B, Nk, Hkv, d, dtype, "k")) == ATTNFUSE_OK &&
       (st = encode_bnhd(&maps.v, v, B, Nk, Hkv, d, dtype, "v")) == ATTNFUSE_OK) {
     const char* why = nullptr;
-    cudaError_t e = launch_attn_fwd(maps, p, d, dtype == ATTNFUSE_BF16, mode == ATTNFUSE_FUSED, s, &why);
+    cudaError_t e = launch_attn_fwd(maps, p, d, dtype == ATTNFUSE_BF16, mode == ATTNFUSE_FUSED || mode == ATTNFUSE_SPLIT,
+                                    mode == ATTNFUSE_FUSED, s, &why);
     if (e != cudaSuccess) st = why ? fail(ATTNFUSE_ERR_UNSUPPORTED, "%s", why) : cuda_fail(e, "attention launch");
   }
   if (owned) cudaFreeAsync(owned, s);

@@ -60,9 +60,10 @@ struct AttnMaps {
   CUtensorMap q, k, v;
 };
 
-// Launches the attention kernel.  rotate = true rotates Q and K tiles on chip (fused mode).
-cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate,
-                            cudaStream_t stream, const char** why);
+// Launches the attention kernel.  rotate_q / rotate_k rotate the Q / K tiles on chip (fused mode:
+// both; split mode: Q only, K pre-rotated; pre-rotate mode: neither).
+cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate_q,
+                            bool rotate_k, cudaStream_t stream, const char** why);
 
 // ---- backward kernels ------------------------------------------------------------------------
 

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-typedef enum { ATTNFUSE_FUSED = 0, ATTNFUSE_PREROTATE = 1, ATTNFUSE_AUTO = 2 } attnfuse_mode_t;
+typedef enum { ATTNFUSE_FUSED = 0, ATTNFUSE_PREROTATE = 1, ATTNFUSE_AUTO = 2, ATTNFUSE_SPLIT = 3 } attnfuse_mode_t;
 
 typedef enum { ATTNFUSE_BF16 = 0, ATTNFUSE_FP16 = 1 } attnfuse_dtype_t;
 
@@ -60,8 +60,12 @@ typedef enum {
  *   mode = ATTNFUSE_FUSED:     one kernel; Q and K tiles are rotated in shared memory.
  *   mode = ATTNFUSE_PREROTATE: a RoPE pass writes rotated Q', K' into `workspace`, then the same
  *                              attention kernel runs on Q', K', V without rotation.
- *   mode = ATTNFUSE_AUTO:      whichever of the two attnfuse_select_mode returns for the shape.
- * Both modes compute the function in the header comment.  `lse` may be NULL (not written).
+ *   mode = ATTNFUSE_SPLIT:     a RoPE pass writes rotated K' into `workspace` (K is re-read by every
+ *                              query tile that needs it), then the attention kernel rotates each
+ *                              query tile on chip (each is read once): rotation cost paid once per
+ *                              element for both tensors.
+ *   mode = ATTNFUSE_AUTO:      whichever mode attnfuse_select_mode returns for the shape.
+ * All modes compute the function in the header comment.  `lse` may be NULL (not written).
  * `workspace` must hold attnfuse_workspace_bytes(...) bytes (0 for FUSED); if it is NULL while
  * bytes are needed, the call allocates with cudaMallocAsync and frees with cudaFreeAsync on
  * `stream`.  Query rows never read keys beyond their own position; rows are independent.
@@ -72,8 +76,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
                                            void* stream);
 
 /* Bytes of workspace attnfuse_rope_causal_fwd needs: 0 for FUSED; for PREROTATE the rotated copies
- * of Q and K (each rounded up to 256 bytes); for AUTO those of the selected mode.  Returns 0 for
- * invalid arguments. */
+ * of Q and K (each rounded up to 256 bytes); for SPLIT the rotated K; for AUTO those of the selected
+ * mode.  Returns 0 for invalid arguments. */
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype);
 
 /*

@@ -92,6 +92,13 @@ def test_select_mode_follows_the_measured_crossover(lib, B, Hq, Hkv, N, mode):
             assert lib.attnfuse_select_mode(B, Hq, Hkv, N, d, dtype) == mode
 
 
+def test_split_mode_workspace_is_the_rotated_keys(lib):
+    assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 3, 0) == 1 * 4096 * 8 * 128 * 2
+    assert lib.attnfuse_workspace_bytes(1, 1, 1, 1, 64, 3, 1) == 256
+    assert fwd(lib, mode=3, ws=FAKE, ws_bytes=16) == 1       # workspace too small for K'
+    assert fwd(lib, mode=4) == 1
+
+
 def test_auto_mode_workspace_is_that_of_the_selected_mode(lib):
     for shape in ((1, 32, 8, 4096, 128), (2, 16, 16, 2048, 64), (1, 16, 16, 8192, 64)):
         sel = lib.attnfuse_select_mode(*shape, 0)

@@ -1,7 +1,7 @@
 """The general causal form through the C ABI: more keys than queries (k, v hold Nk >= N tokens and
 the queries are the last N of them, so query i sees keys j <= Nk - N + i: a prefill that extends a
 cache, and N = 1 a decode step) and explicit int32 rotation positions for queries and keys, in the
-pre-rotation pass and both attention modes, against the oracle's fp64 definition.
+pre-rotation pass and every attention mode, against the oracle's fp64 definition.
 """
 import numpy as np
 import pytest
@@ -67,16 +67,17 @@ def _check_both_modes(q, k, v, dt, label, **kw):
                                       k_positions=None if kp is None else kp.numpy())
     dev = {n: (t.cuda() if isinstance(t, torch.Tensor) else t) for n, t in kw.items()}
     outs = {}
-    for mode in ("fused", "prerotate"):
+    for mode in ("fused", "prerotate", "split"):
         o, l = binding.rope_causal_fwd(q.cuda(), k.cuda(), v.cuda(), 1e4, mode=mode, **dev)
         torch.cuda.synchronize()
         assert binding.device_status() == 0
         outs[mode] = (o.cpu(), l.cpu())
         assert_close(o.double().cpu().numpy(), l.double().cpu().numpy(), o_ref, l_ref, dt, f"{mode} {label}")
-    e = errors(outs["fused"][0].double().numpy(), outs["fused"][1].double().numpy(),
-               outs["prerotate"][0].double().numpy(), outs["prerotate"][1].double().numpy())
     t = TOL[dt]
-    assert e["max_abs"] <= t["max_abs"] / 4 and e["rel_l2"] <= t["rel_l2"] / 4, e
+    for m in ("fused", "split"):
+        e = errors(outs[m][0].double().numpy(), outs[m][1].double().numpy(),
+                   outs["prerotate"][0].double().numpy(), outs["prerotate"][1].double().numpy())
+        assert e["max_abs"] <= t["max_abs"] / 4 and e["rel_l2"] <= t["rel_l2"] / 4, (m, e)
     return outs
 
 
@@ -128,7 +129,7 @@ def test_explicit_default_positions_agree_with_the_defaults():
     qp = torch.arange(Nk - N, Nk, dtype=torch.int32).reshape(1, N).cuda()
     kp = torch.arange(Nk, dtype=torch.int32).reshape(1, Nk).cuda()
     qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
-    for mode in ("fused", "prerotate"):
+    for mode in ("fused", "prerotate", "split"):
         a, la = binding.rope_causal_fwd(qc, kc, vc, 1e4, mode=mode)
         b, lb = binding.rope_causal_fwd(qc, kc, vc, 1e4, mode=mode, q_positions=qp, k_positions=kp)
         torch.cuda.synchronize()
@@ -147,7 +148,7 @@ def test_prefill_rows_equal_the_tail_of_full_attention():
     B, N, Nk, Hq, Hkv, d = 1, 200, 520, 4, 2, 128
     q_full, k, v = inputs.make_kv_inputs(B, Nk, Nk, Hq, Hkv, d, "bf16", seed=31)
     qc, kc, vc = q_full.cuda(), k.cuda(), v.cuda()
-    for mode in ("fused", "prerotate"):
+    for mode in ("fused", "prerotate", "split"):
         full_o, full_l = binding.rope_causal_fwd(qc, kc, vc, 1e4, mode=mode)
         pre_o, pre_l = binding.rope_causal_fwd(qc[:, Nk - N:].contiguous(), kc, vc, 1e4, mode=mode)
         torch.cuda.synchronize()

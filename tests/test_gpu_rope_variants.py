@@ -1,6 +1,6 @@
 """RoPE variants through the C ABI (attnfuse_rope_apply_ex, attnfuse_rope_causal_fwd_ex): a rotary
 dimension r < d (only the first r entries rotated, theta_k = base^(-2k/r)) and interleaved pairs
-(2k, 2k+1), in the pre-rotation pass and in both attention modes, against the oracle's fp64
+(2k, 2k+1), in the pre-rotation pass and in every attention mode, against the oracle's fp64
 definition of each variant.
 """
 import numpy as np
@@ -101,7 +101,7 @@ def test_attention_variant_matches_oracle(B, N, Hq, Hkv, d, dt, r, il):
     q, k, v = draw(B, N, Hq, Hkv, d, dt, seed=N + r)
     o_ref, l_ref = oracle.rope_causal(q, k, v, 1e4, rotary_dim=r, interleaved=il)
     outs = {}
-    for mode in ("fused", "prerotate"):
+    for mode in ("fused", "prerotate", "split"):
         o, l = binding.rope_causal_fwd(q.cuda(), k.cuda(), v.cuda(), 1e4, mode=mode, rotary_dim=r, interleaved=il)
         torch.cuda.synchronize()
         assert binding.device_status() == 0
@@ -109,10 +109,11 @@ def test_attention_variant_matches_oracle(B, N, Hq, Hkv, d, dt, r, il):
         assert_close(o.double().cpu().numpy(), l.double().cpu().numpy(), o_ref, l_ref, dt,
                      f"{mode} r={r} interleaved={il} {B}x{N}x{Hq}/{Hkv}x{d} {dt}")
     # the two modes agree to well within the oracle tolerance (as for the default form)
-    e = errors(outs["fused"][0].double().numpy(), outs["fused"][1].double().numpy(),
-               outs["prerotate"][0].double().numpy(), outs["prerotate"][1].double().numpy())
     t = TOL[dt]
-    assert e["max_abs"] <= t["max_abs"] / 4 and e["rel_l2"] <= t["rel_l2"] / 4, e
+    for m in ("fused", "split"):
+        e = errors(outs[m][0].double().numpy(), outs[m][1].double().numpy(),
+                   outs["prerotate"][0].double().numpy(), outs["prerotate"][1].double().numpy())
+        assert e["max_abs"] <= t["max_abs"] / 4 and e["rel_l2"] <= t["rel_l2"] / 4, (m, e)
 
 
 def test_full_half_split_options_equal_the_default_call():
