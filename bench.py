@@ -367,14 +367,14 @@ def rope_pass_fn(w, stream):
 
 
 def measure_point(w, steps, warmup):
-    """Median-of-steps times (ms) for fused, pre-rotate pipeline and the RoPE pass alone."""
+    """Median-of-steps times (ms) for fused, the pre-rotate and split pipelines, and the RoPE pass alone."""
     import torch
     from attention_rope_causal_gb300 import binding
     stream = torch.cuda.current_stream()
-    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
+    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate", "split"))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     res = {}
-    for mode in ("fused", "prerotate"):
+    for mode in ("fused", "prerotate", "split"):
         f = fwd_fn(w, q, k, v, out, lse, ws[mode], mode, stream)
         time_steps(f, warmup, flush, stream)
         res[mode] = statistics.median(time_steps(f, steps, flush, stream))
@@ -395,9 +395,11 @@ def run_sweep(args):
         fl = w.causal_flops
         qk_bytes = 2 * (w.B * w.N * (w.Hq + w.Hkv) * w.d * 2)
         rec = {"workload": w.name, "N": w.N, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "dtype": w.dtype,
-               "fused_ms": t["fused"], "prerotate_ms": t["prerotate"], "rope_ms": t["rope"],
+               "fused_ms": t["fused"], "prerotate_ms": t["prerotate"], "split_ms": t["split"], "rope_ms": t["rope"],
                "fused_tflops": fl / t["fused"] / 1e9, "prerotate_tflops": fl / t["prerotate"] / 1e9,
-               "rope_gbs": qk_bytes / t["rope"] / 1e6, "fused_over_prerotate": t["fused"] / t["prerotate"]}
+               "split_tflops": fl / t["split"] / 1e9, "rope_gbs": qk_bytes / t["rope"] / 1e6,
+               "fused_over_prerotate": t["fused"] / t["prerotate"],
+               "fastest": min(("fused", "prerotate", "split"), key=lambda m: t[m])}
         rows.append(rec)
         print(json.dumps(rec), flush=True)
     summary = {}
@@ -435,7 +437,7 @@ def run_only(args):
     torch.cuda.set_device(0)
     w = inputs.NAMED[args.workload]
     stream = torch.cuda.current_stream()
-    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
+    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate", "split"))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     if args.only == "rope":
         f = rope_pass_fn(w, stream)
@@ -459,7 +461,7 @@ def run_ours(args):
     w = inputs.NAMED[args.workload]
     peaks = load_peaks()
     stream = torch.cuda.current_stream()
-    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate"))
+    q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate", "split"))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     step = fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)
 
@@ -492,6 +494,9 @@ def run_ours(args):
     pre = fwd_fn(w, q, k, v, out, lse, ws["prerotate"], "prerotate", stream)
     time_steps(pre, args.warmup, flush, stream)
     pre_ms = statistics.median(time_steps(pre, max(20, args.steps // 10), flush, stream))
+    spl = fwd_fn(w, q, k, v, out, lse, ws["split"], "split", stream)
+    time_steps(spl, args.warmup, flush, stream)
+    split_ms = statistics.median(time_steps(spl, max(20, args.steps // 10), flush, stream))
     rope_pass = rope_pass_fn(w, stream)
     time_steps(rope_pass, args.warmup, flush, stream)
     rope_ms = statistics.median(time_steps(rope_pass, max(20, args.steps // 10), flush, stream))
@@ -529,6 +534,8 @@ def run_ours(args):
                       "rope_gbs": rope_bytes / (rope_ms / 1e3) / 1e9,
                       "rope_frac_of_hbm": rope_bytes / (rope_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                       "fused_over_prerotate": per_launch_ms / pre_ms},
+        "split": {"ms": split_ms, "tflops": w.causal_flops / (split_ms / 1e3) / 1e12,
+                  "note": "K rotated by the pre-rotation pass, query tiles rotated on chip"},
         "backward": {"ms": bwd_ms, "tflops": 2.5 * w.causal_flops / (bwd_ms / 1e3) / 1e12,
                      "flops_note": "2.5 x the causal forward FLOPs (dS^T Q, dS K, P^T dO, dO V^T and the "
                                    "recomputed Q K^T); the kernels compute Q K^T and dO V^T twice",
@@ -551,7 +558,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=inputs.LLAMA.name, choices=sorted(inputs.NAMED))
     ap.add_argument("--sweep", action="store_true", help="run the crossover sweep instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("fused", "prerotate", "rope", "backward"),
+    ap.add_argument("--only", choices=("fused", "prerotate", "split", "rope", "backward"),
                     help="time one path alone (for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -81,11 +81,11 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype);
 
 /*
- * The faster of FUSED and PREROTATE for a shape on GB300, from the measured fused-vs-pre-rotate
- * crossover ("Rotation Calculus" in "AttnFuse Makes RoPE a First-Class Attention Compilation
- * Operation", paragraph 2, made a runtime choice): grouped-query attention (Hq / Hkv >= 2) with
- * N >= 2048 -> PREROTATE (measured faster at every N from 2048 to 16384); multi-head attention
- * (Hq == Hkv) with N >= 3072 -> PREROTATE (measured N* ~ 3100); everything else -> FUSED.
+ * The fastest mode for a shape on GB300, from the measured sweep of all three ("Rotation Calculus" in
+ * "AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraph 2, made a runtime
+ * choice): grouped-query attention (Hq / Hkv >= 2) with N >= 2048 -> SPLIT (fastest at 9 of 10
+ * measured points from 2048 to 16384, pre-rotation at the tenth); multi-head attention (Hq == Hkv)
+ * with N >= 3072 -> PREROTATE (measured N* ~ 3100 against FUSED); everything else -> FUSED.
  * Host-only and pure: no device access; arguments it cannot judge (non-positive sizes, Hq not a
  * multiple of Hkv) give FUSED.
  */

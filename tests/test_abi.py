@@ -81,8 +81,8 @@ def test_workspace_bytes(lib):
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,N,mode", [
-    (1, 32, 8, 4096, 1), (4, 32, 8, 2048, 1), (1, 32, 8, 16384, 1), (8, 32, 8, 1024, 0),  # GQA 4:1
-    (1, 8, 4, 3000, 1), (1, 64, 8, 2047, 0),                                           # other groups
+    (1, 32, 8, 4096, 3), (4, 32, 8, 2048, 3), (1, 32, 8, 16384, 3), (8, 32, 8, 1024, 0),  # GQA 4:1
+    (1, 8, 4, 3000, 3), (1, 64, 8, 2047, 0),                                           # other groups
     (2, 16, 16, 2048, 0), (1, 16, 16, 3071, 0), (1, 16, 16, 3072, 1), (1, 16, 16, 32768, 1),  # MHA
     (0, 16, 16, 4096, 0), (1, 6, 4, 4096, 0),                                          # not judged
 ])
@@ -103,7 +103,7 @@ def test_auto_mode_workspace_is_that_of_the_selected_mode(lib):
     for shape in ((1, 32, 8, 4096, 128), (2, 16, 16, 2048, 64), (1, 16, 16, 8192, 64)):
         sel = lib.attnfuse_select_mode(*shape, 0)
         assert lib.attnfuse_workspace_bytes(*shape, 2, 0) == lib.attnfuse_workspace_bytes(*shape, sel, 0)
-    assert binding.select_mode(1, 32, 8, 4096, 128) == "prerotate"
+    assert binding.select_mode(1, 32, 8, 4096, 128) == "split"
     assert binding.select_mode(2, 16, 16, 2048, 64) == "fused"
 
 
