@@ -35,7 +35,8 @@ METRIC = "RoPE+causal attn fwd TFLOP/s and % of GB300 bf16 peak; fused vs pre-ro
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 * 1024 * 1024
 KERNEL_SOURCES = ("attention_rope_causal_gb300/csrc/attn_fwd.cu", "attention_rope_causal_gb300/csrc/ptx.cuh",
-                  "attention_rope_causal_gb300/csrc/rope.cuh", "attention_rope_causal_gb300/csrc/rope_apply.cu")
+                  "attention_rope_causal_gb300/csrc/rope.cuh", "attention_rope_causal_gb300/csrc/rope_apply.cu",
+                  "attention_rope_causal_gb300/csrc/attn_bwd.cu")
 
 
 # ----------------------------------------------------------------------------------------------
