@@ -357,6 +357,7 @@ typedef struct {
   rope_form_t form;
   const double *theta;
   const double *qrot, *krot; /* [B, N, Hq, d], [B, N, Hkv, d] */
+  const double *qpos;        /* [B, N] rotation positions of the queries, or NULL: i */
   const int64_t *qslot;      /* [N]: output slot of query row i, or -1 if its dq is not reported */
   int64_t nq;                /* reported query rows per batch entry */
   double *dq;                /* [B, nq, Hq, d] */
@@ -409,7 +410,8 @@ static void bwd_q_item(void *vctx, int64_t item, double *scratch) {
     for (int e = 0; e < d; ++e) dqr[e] += dS * kj[e] * scale;
   }
   double *out = c->dq + (((size_t)b * (size_t)c->nq + (size_t)slot) * c->Hq + h) * d;
-  rope_rotate_vec(dqr, out, c->form, -(double)i, c->theta); /* R(i)^T */
+  double qp = c->qpos ? c->qpos[(size_t)b * N + (size_t)i] : (double)i;
+  rope_rotate_vec(dqr, out, c->form, -qp, c->theta); /* R(p_i)^T */
 }
 
 typedef struct {
@@ -419,6 +421,7 @@ typedef struct {
   rope_form_t form;
   const double *theta;
   const double *qrot, *krot;
+  const double *kpos;        /* [B, N] rotation positions of the keys, or NULL: j */
   const int64_t *ksel;
   int64_t nk;
   const double *m, *l, *D;
@@ -459,7 +462,8 @@ static void bwd_k_item(void *vctx, int64_t item, double *scratch) {
     }
   }
   size_t obase = (((size_t)b * c->nk + (size_t)sl) * c->Hkv + hk) * d;
-  rope_rotate_vec(dkr, c->dk + obase, c->form, -(double)j, c->theta); /* R(j)^T */
+  double kp = c->kpos ? c->kpos[(size_t)b * N + (size_t)j] : (double)j;
+  rope_rotate_vec(dkr, c->dk + obase, c->form, -kp, c->theta); /* R(p_j)^T */
   for (int e = 0; e < d; ++e) c->dv[obase + e] = dvj[e];
 }
 
@@ -469,24 +473,27 @@ typedef struct {
   int H, N;
   rope_form_t form;
   const double *theta;
+  const double *pos; /* [B, N] positions, or NULL: n */
   double *out;
 } rot_all_ctx_t;
 
-/* One item = one token (b, n): rotate its H head vectors at position n. */
+/* One item = one token (b, n): rotate its H head vectors at its position. */
 static void rot_all_item(void *vctx, int64_t bn, double *scratch) {
   rot_all_ctx_t *c = (rot_all_ctx_t *)vctx;
   int d = c->form.d;
+  double pos = c->pos ? c->pos[bn] : (double)(bn % c->N);
   for (int h = 0; h < c->H; ++h) {
     size_t base = ((size_t)bn * c->H + h) * d;
     for (int e = 0; e < d; ++e) scratch[e] = load_elem(c->x, c->dtype, base + e);
-    rope_rotate_vec(scratch, c->out + base, c->form, (double)(bn % c->N), c->theta);
+    rope_rotate_vec(scratch, c->out + base, c->form, pos, c->theta);
   }
 }
 
-int orc_rope_causal_bwd(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,
-                        int Hkv, int N, int d, int rotary_dim, int interleaved, double base, const int64_t *q_rows,
-                        int64_t nq, const int64_t *k_rows, int64_t nk, double *dq, double *dk, double *dv,
-                        int nthreads) {
+/* q_pos, k_pos: [B, N] rotation positions (NULL: the token index), as for entry 3. */
+int orc_rope_causal_bwd_ex(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,
+                           int Hkv, int N, int d, int rotary_dim, int interleaved, double base, const double *q_pos,
+                           const double *k_pos, const int64_t *q_rows, int64_t nq, const int64_t *k_rows, int64_t nk,
+                           double *dq, double *dk, double *dv, int nthreads) {
   rope_form_t f = {d, rotary_dim, interleaved};
   if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 1 || Hq < 1 || Hkv < 1 || N < 1 || !form_ok(f) ||
       (Hq % Hkv) != 0)
@@ -510,20 +517,20 @@ int orc_rope_causal_bwd(const void *q, const void *k, const void *v, const void 
     rope_frequencies(f.r, base, theta);
     for (int64_t i = 0; i < N; ++i) qslot[i] = q_rows ? -1 : i;
     for (int64_t s = 0; q_rows && s < nq; ++s) qslot[q_rows[s]] = s;
-    rot_all_ctx_t rq = {q, dtype, Hq, N, f, theta, qrot};
+    rot_all_ctx_t rq = {q, dtype, Hq, N, f, theta, q_pos, qrot};
     orc_pool_t p1 = {rot_all_item, &rq, (int64_t)B * N, 0, (size_t)d, 0};
-    rot_all_ctx_t rk = {k, dtype, Hkv, N, f, theta, krot};
+    rot_all_ctx_t rk = {k, dtype, Hkv, N, f, theta, k_pos, krot};
     orc_pool_t p2 = {rot_all_item, &rk, (int64_t)B * N, 0, (size_t)d, 0};
     rc = orc_run(&p1, nthreads);
     if (rc == 0) rc = orc_run(&p2, nthreads);
     if (rc == 0) {
-      bwd_q_ctx_t qc = {v, dout, dtype, B, Hq, Hkv, N, d, f, theta, qrot, krot, qslot, nq, dq,
+      bwd_q_ctx_t qc = {v, dout, dtype, B, Hq, Hkv, N, d, f, theta, qrot, krot, q_pos, qslot, nq, dq,
                         stats, stats + nst, stats + 2 * nst};
       orc_pool_t p3 = {bwd_q_item, &qc, (int64_t)B * Hq * N, 0, (size_t)(2 * d + 2 * N), 0};
       rc = orc_run(&p3, nthreads);
     }
     if (rc == 0 && nk > 0) {
-      bwd_k_ctx_t kc = {v, dout, dtype, B, Hq, Hkv, N, d, f, theta, qrot, krot, k_rows, nk,
+      bwd_k_ctx_t kc = {v, dout, dtype, B, Hq, Hkv, N, d, f, theta, qrot, krot, k_pos, k_rows, nk,
                         stats, stats + nst, stats + 2 * nst, dk, dv};
       orc_pool_t p4 = {bwd_k_item, &kc, (int64_t)B * Hkv * nk, 0, (size_t)(4 * d), 0};
       rc = orc_run(&p4, nthreads);
@@ -535,4 +542,12 @@ int orc_rope_causal_bwd(const void *q, const void *k, const void *v, const void 
   free(stats);
   free(qslot);
   return rc;
+}
+
+int orc_rope_causal_bwd(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,
+                        int Hkv, int N, int d, int rotary_dim, int interleaved, double base, const int64_t *q_rows,
+                        int64_t nq, const int64_t *k_rows, int64_t nk, double *dq, double *dk, double *dv,
+                        int nthreads) {
+  return orc_rope_causal_bwd_ex(q, k, v, dout, dtype, B, Hq, Hkv, N, d, rotary_dim, interleaved, base, NULL, NULL,
+                                q_rows, nq, k_rows, nk, dq, dk, dv, nthreads);
 }

@@ -23,12 +23,17 @@ def _loss(q, k, v, dout, base, **kw):
     return float((out * dout).sum())
 
 
-@pytest.mark.parametrize("Hq,Hkv,d,r,il", [(2, 1, 8, None, False), (4, 2, 16, None, False), (2, 2, 16, 8, True)])
-def test_gradients_match_finite_differences_of_the_forward(Hq, Hkv, d, r, il):
+@pytest.mark.parametrize("Hq,Hkv,d,r,il,pos", [(2, 1, 8, None, False, False), (4, 2, 16, None, False, False),
+                                               (2, 2, 16, 8, True, False), (2, 1, 8, None, False, True),
+                                               (2, 2, 16, 8, False, True)])
+def test_gradients_match_finite_differences_of_the_forward(Hq, Hkv, d, r, il, pos):
     B, N, base = 2, 7, 100.0
     q, k, v = _rand((B, N, Hq, d), 1), _rand((B, N, Hkv, d), 2), _rand((B, N, Hkv, d), 3)
     dout = _rand((B, N, Hq, d), 4)
     kw = dict(rotary_dim=r, interleaved=il)
+    if pos:  # explicit rotation positions (any integers), different per batch entry
+        rng0 = np.random.default_rng(30)
+        kw.update(q_positions=rng0.integers(-50, 300, size=(B, N)), k_positions=rng0.integers(-50, 300, size=(B, N)))
     dq, dk, dv = oracle.rope_causal_bwd(q, k, v, dout, base, **kw)
     eps = 1e-6
     rng = np.random.default_rng(5)
