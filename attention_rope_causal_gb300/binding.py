@@ -46,6 +46,9 @@ _SIGNATURES = {
     "attnfuse_rope_causal_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int,
                                                                                         ctypes.c_void_p, ctypes.c_size_t,
                                                                                         ctypes.c_void_p]),
+    "attnfuse_rope_causal_bwd_ex": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5 +
+                                    [ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                     ctypes.POINTER(RopeOpts), ctypes.c_void_p]),
     "attnfuse_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
     "attnfuse_workspace_bytes_ex": (ctypes.c_size_t, [ctypes.c_int] * 7 + [ctypes.POINTER(RopeOpts)]),
     "attnfuse_select_mode": (ctypes.c_int, [ctypes.c_int] * 6),
@@ -197,10 +200,11 @@ def bwd_workspace_bytes(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> int:
 
 
 def rope_causal_bwd(q, k, v, out, lse, dout, rope_base: float, dq=None, dk=None, dv=None, workspace=None,
-                    stream=None):
-    """Backward pass through ``attnfuse_rope_causal_bwd``: (dq, dk, dv) for q [B, N, Hq, d], k/v
-    [B, N, Hkv, d], the forward's out [B, N, Hq, d] and lse [B, Hq, N] (float32), and dout = dL/dout.
-    All CUDA tensors, contiguous, one 16-bit dtype (lse float32)."""
+                    stream=None, rotary_dim=None, interleaved: bool = False, q_positions=None, k_positions=None):
+    """Backward pass through ``attnfuse_rope_causal_bwd`` (``_ex`` with a RoPE variant or positions):
+    (dq, dk, dv) for q [B, N, Hq, d], k/v [B, N, Hkv, d], the forward's out [B, N, Hq, d] and lse
+    [B, Hq, N] (float32), and dout = dL/dout.  All CUDA tensors, contiguous, one 16-bit dtype (lse
+    float32); positions [B, N] CUDA int32."""
     B, N, Hq, d = q.shape
     Hkv = k.shape[2]
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout)):
@@ -214,9 +218,17 @@ def rope_causal_bwd(q, k, v, out, lse, dout, rope_base: float, dq=None, dk=None,
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    _check(load().attnfuse_rope_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
-                                           _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(rope_base), DTYPES[q.dtype],
-                                           ws_ptr, ws_bytes, _stream_ptr(stream)))
+    opts = _opts(rotary_dim, interleaved, 0, _positions(q_positions, B * N, "q_positions"),
+                 _positions(k_positions, B * N, "k_positions"))
+    if opts is None:
+        _check(load().attnfuse_rope_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                               _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(rope_base), DTYPES[q.dtype],
+                                               ws_ptr, ws_bytes, _stream_ptr(stream)))
+    else:
+        _check(load().attnfuse_rope_causal_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(rope_base),
+                                                  DTYPES[q.dtype], ws_ptr, ws_bytes, ctypes.byref(opts),
+                                                  _stream_ptr(stream)))
     return dq, dk, dv
 
 

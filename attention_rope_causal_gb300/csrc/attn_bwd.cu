@@ -16,8 +16,10 @@
 //      dV += P^T dO and dK' += dS^T Q' with P^T, dS^T read from tensor memory);
 //   3. bwd_dq_kernel: one unit = one 128-row query tile of one head; it walks key tiles 0 .. its
 //      diagonal, accumulating dQ' (S and dP, dS elementwise, dQ' += dS K').
-// Both epilogues scale by 1/sqrt(d) and rotate back with R^T at the row's position in registers (a
-// thread holds a whole row, so each pair (e, e + d/2) is local).
+// Both epilogues scale by 1/sqrt(d) and, for the half-split form at positions i and j, rotate back
+// with R^T at the row's position in registers (a thread holds a whole row, so each pair (e, e + d/2)
+// is local); other RoPE forms and explicit positions leave that to a pre-rotation pass run with the
+// negated positions.
 //
 // Structure of both kernels: 384 threads, one CTA per SM, persistent over units.
 //   warp 0      TMA producer (whole warp; lane 0 issues), also stages lse/D vectors for dK/dV.
@@ -480,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[e] = __uint_as_float(kx[e]) * p.inv_sqrt_d;
           y[e] = __uint_as_float(ky[e]) * p.inv_sqrt_d;
           const int k = wg * QK + e;
-          unrotate_pair(x[e], y[e], (uint32_t)j, p.freqs.lo[k], p.freqs.hi[k]);
+          if (p.unrotate) unrotate_pair(x[e], y[e], (uint32_t)j, p.freqs.lo[k], p.freqs.hi[k]);
         }
 #pragma unroll
         for (int v = 0; v < QK / 8; ++v) {
@@ -687,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[e] = __uint_as_float(qx[e]) * p.inv_sqrt_d;
           y[e] = __uint_as_float(qy[e]) * p.inv_sqrt_d;
           const int k = wg * QK + e;
-          unrotate_pair(x[e], y[e], (uint32_t)i, p.freqs.lo[k], p.freqs.hi[k]);
+          if (p.unrotate) unrotate_pair(x[e], y[e], (uint32_t)i, p.freqs.lo[k], p.freqs.hi[k]);
         }
 #pragma unroll
         for (int v = 0; v < QK / 8; ++v) {

@@ -432,9 +432,24 @@ attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const v
                                            const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                                            int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
                                            void* workspace, size_t workspace_bytes, void* stream) {
+  return attnfuse_rope_causal_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, rope_base, dtype, workspace,
+                                     workspace_bytes, nullptr, stream);
+}
+
+attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                                              const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                              int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
+                                              void* workspace, size_t workspace_bytes,
+                                              const attnfuse_rope_opts_t* opts, void* stream) {
   g_err[0] = '\0';
   attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, ATTNFUSE_FUSED, dtype);
   if (st != ATTNFUSE_OK) return st;
+  Opts o;
+  if ((st = resolve_opts(opts, d, N, &o)) != ATTNFUSE_OK) return st;
+  if (o.Nk != N) return fail(ATTNFUSE_ERR_INVALID_ARG, "the backward pass takes kv_len 0 (= N) only");
+  // The half-split form over all d at positions i and j is rotated back in the kernels' epilogues;
+  // any other form runs a pre-rotation pass with the negated positions over dq and dk afterwards.
+  const bool plain_form = o.rdim == d && o.interleaved == 0 && !o.qpos && !o.kpos;
   if (!lse || !dout || !dq || !dk || !dv) return fail(ATTNFUSE_ERR_INVALID_ARG, "lse, dout, dq, dk and dv must be non-null");
   if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
     return fail(ATTNFUSE_ERR_INVALID_ARG, "dout, dq, dk and dv must be 16-byte aligned");
@@ -478,21 +493,43 @@ attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const v
   p.dv = dv;
   p.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
   p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
+  p.unrotate = plain_form ? 1 : 0;
   p.timeout_ns = kTimeoutNs;
   rope_freqs_host(d, rope_base, &p.freqs);
 
-  // q' and k' (the forward's rotation, one launch over both), then D, dK/dV and dQ.
+  // One pre-rotation launch per (tensor, position source); both tensors in one launch when they share
+  // positions i, j.  sign = 1: q', k' before the kernels; -1: dq, dk rotated back after them.
   RopeApplyParams rp;
   std::memset(&rp, 0, sizeof rp);
-  rp.job[0] = RopeJob{q, qr, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
-  rp.job[1] = RopeJob{k, kr, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
-  rp.njobs = 2;
-  rp.N = N;
-  rp.tokens = (long long)B * N;
-  rp.groups_total = rp.job[0].groups + rp.job[1].groups;
-  rp.rot_chunks = d / 16;
-  rp.freqs = p.freqs;
-  cudaError_t e = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+  rp.rot_chunks = o.rdim / 16;
+  rp.interleaved = o.interleaved;
+  rope_freqs_host(o.rdim, rope_base, &rp.freqs);
+  auto rotate = [&](const void* xq, void* yq, const void* xk, void* yk, int neg) -> cudaError_t {
+    rp.pos_neg = neg;
+    rp.N = N;
+    rp.tokens = (long long)B * N;
+    const RopeJob jq{xq, yq, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    const RopeJob jk{xk, yk, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
+    if (!o.qpos && !o.kpos) {
+      rp.job[0] = jq;
+      rp.job[1] = jk;
+      rp.njobs = 2;
+      rp.groups_total = jq.groups + jk.groups;
+      rp.pos = nullptr;
+      return launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+    }
+    rp.njobs = 1;
+    rp.job[0] = jq;
+    rp.groups_total = jq.groups;
+    rp.pos = o.qpos;
+    cudaError_t err = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+    if (err != cudaSuccess) return err;
+    rp.job[0] = jk;
+    rp.groups_total = jk.groups;
+    rp.pos = o.kpos;
+    return launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
+  };
+  cudaError_t e = rotate(q, qr, k, kr, 0);
   if (e != cudaSuccess) st = cuda_fail(e, "rope_apply launch");
   AttnBwdMaps maps;
   if (st == ATTNFUSE_OK && (st = encode_bnhd(&maps.q, qr, B, N, Hq, d, dtype, "q'")) == ATTNFUSE_OK &&
@@ -501,6 +538,8 @@ attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const v
       (st = encode_bnhd(&maps.dout, dout, B, N, Hq, d, dtype, "dout")) == ATTNFUSE_OK) {
     e = launch_attn_bwd(maps, p, d, dtype == ATTNFUSE_BF16, s);
     if (e != cudaSuccess) st = cuda_fail(e, "backward launch");
+    if (st == ATTNFUSE_OK && !plain_form && (e = rotate(dq, dq, dk, dk, 1)) != cudaSuccess)
+      st = cuda_fail(e, "rope_apply launch (rotating the gradients back)");
   }
   if (owned) cudaFreeAsync(owned, s);
   return st;

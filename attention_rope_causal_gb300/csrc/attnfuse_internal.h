@@ -27,6 +27,7 @@ struct RopeApplyParams {
   long long tokens;  // B * N
   const int32_t* pos;  // [B, N] rotation position of each token (one job only), or nullptr:
   int pos_off;         //   then the position of token (b, n) is pos_off + n
+  int pos_neg;         // 1: rotate by the negated position (R^T, the transpose of the rotation)
   int groups_total;  // job[0].groups + (njobs > 1 ? job[1].groups : 0)
   int rot_chunks;    // rotary_dim / 16: item ck < rot_chunks rotates (frequencies 8 ck .. 8 ck + 7)
   int interleaved;   // 0: pairs (k, k + rotary_dim/2); 1: pairs (2k, 2k + 1)
@@ -79,6 +80,8 @@ struct AttnBwdParams {
   void* dv;               // [B, N, Hkv, d]
   float scale_log2;       // log2(e) / sqrt(d)
   float inv_sqrt_d;
+  int unrotate;           // 1: the epilogues apply R^T (half-split over all d, positions i and j);
+                          // 0: they write the gradients in the rotated frame (a pass rotates back)
   unsigned long long timeout_ns;
   RopeFreqs freqs;        // F_k, k < d/2 (half-split, rotary dimension d)
 };

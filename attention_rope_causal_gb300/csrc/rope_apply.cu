@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(kThreads) rope_apply_kernel(const __grid_const
   const int rem = (int)(item - token * per_token);
   int g = rem / NCH;
   const int ck = rem - g * NCH;
-  const int32_t pos = p.pos ? p.pos[token] : p.pos_off + (int32_t)(token % p.N);
+  const int32_t pos0 = p.pos ? p.pos[token] : p.pos_off + (int32_t)(token % p.N);
+  const int32_t pos = p.pos_neg ? -pos0 : pos0;
 
   int j = 0;
   if (g >= p.job[0].groups) {

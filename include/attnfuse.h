@@ -168,6 +168,16 @@ attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const v
                                            int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
                                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* attnfuse_rope_causal_bwd for the RoPE variants and explicit positions of attnfuse_rope_opts_t
+ * (rotary_dim, interleaved, q_positions [B, N], k_positions [B, N]; kv_len must be 0 or N).  The
+ * kernels produce the gradients in the rotated frame and a pre-rotation pass with the negated
+ * positions rotates dq and dk back (R^T). */
+attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                                              const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                              int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
+                                              void* workspace, size_t workspace_bytes,
+                                              const attnfuse_rope_opts_t* opts, void* stream);
+
 /* Bytes of workspace attnfuse_rope_causal_bwd needs (0 for invalid arguments). */
 size_t attnfuse_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype);
 

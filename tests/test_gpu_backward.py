@@ -112,3 +112,50 @@ def test_backward_workspace_and_no_workspace_agree():
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+VARIANTS = [
+    # B, N, Hq, Hkv, d, dtype, rotary_dim, interleaved, explicit positions
+    (1, 300, 4, 2, 128, "bf16", 64, False, False),
+    (1, 257, 2, 2, 64, "fp16", None, True, False),
+    (2, 200, 4, 1, 128, "bf16", None, False, True),
+    (1, 390, 6, 3, 64, "fp16", 32, True, True),
+]
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,d,dt,r,il,pos", VARIANTS)
+def test_backward_variants_and_positions_match_oracle(B, N, Hq, Hkv, d, dt, r, il, pos):
+    # Other RoPE forms: the kernels return the gradients in the rotated frame and a pre-rotation
+    # pass with the negated positions (R^T) rotates dq and dk back.
+    q, k, v, dout = _case(B, N, Hq, Hkv, d, dt, seed=5 * N + d)
+    qp = inputs.make_positions(B, N, seed=N) if pos else None
+    kp = inputs.make_positions(B, N, seed=N + 1) if pos else None
+    kw = dict(rotary_dim=r, interleaved=il)
+    dev = dict(kw, q_positions=None if qp is None else qp.cuda(), k_positions=None if kp is None else kp.cuda())
+    qc, kc, vc, dc = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    o, l = binding.rope_causal_fwd(qc, kc, vc, 1e4, mode="prerotate", **dev)
+    dq, dk, dv = binding.rope_causal_bwd(qc, kc, vc, o, l, dc, 1e4, **dev)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    rq, rk, rv = oracle.rope_causal_bwd(q, k, v, dout, 1e4, q_positions=None if qp is None else qp.numpy(),
+                                        k_positions=None if kp is None else kp.numpy(), **kw)
+    label = f"{B}x{N}x{Hq}/{Hkv}x{d} {dt} r={r} il={il} pos={pos}"
+    assert_grad_close(dq.cpu(), rq, dt, "dq " + label)
+    assert_grad_close(dk.cpu(), rk, dt, "dk " + label)
+    assert_grad_close(dv.cpu(), rv, dt, "dv " + label)
+
+
+def test_backward_explicit_index_positions_agree_with_the_default():
+    # Same function, two routes: epilogue rotation (default) and the negated-position pass.  The pass
+    # route rounds the rotated-frame gradient to bf16 once more before rotating it back, so the two
+    # differ by about one bf16 rounding: within 2^-7 (one bf16 ulp, relative) in relative L2.
+    q, k, v, dout = _case(1, 256, 4, 2, 128, "bf16", seed=77)
+    qc, kc, vc, dc = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    pos = torch.arange(256, dtype=torch.int32).reshape(1, 256).cuda()
+    o, l = binding.rope_causal_fwd(qc, kc, vc, 1e4)
+    a = binding.rope_causal_bwd(qc, kc, vc, o, l, dc, 1e4)
+    b = binding.rope_causal_bwd(qc, kc, vc, o, l, dc, 1e4, q_positions=pos, k_positions=pos)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        err = (x.double() - y.double()).norm() / y.double().norm()
+        assert float(err) <= 2.0 ** -7, float(err)
