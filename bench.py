@@ -34,9 +34,15 @@ if ROOT not in sys.path:
 METRIC = "RoPE+causal attn fwd TFLOP/s and % of GB300 bf16 peak; fused vs pre-rotate N*"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 * 1024 * 1024
-KERNEL_SOURCES = ("attention_rope_causal_gb300/csrc/attn_fwd.cu", "attention_rope_causal_gb300/csrc/ptx.cuh",
-                  "attention_rope_causal_gb300/csrc/rope.cuh", "attention_rope_causal_gb300/csrc/rope_apply.cu",
-                  "attention_rope_causal_gb300/csrc/attn_bwd.cu")
+_CSRC = "attention_rope_causal_gb300/csrc/"
+# The sources each profiled kernel is compiled from (the kernel code; not the host-side launch code).
+KERNEL_SOURCES = {
+    "attn_fwd": tuple(_CSRC + f for f in ("attn_fwd.cu", "ptx.cuh", "rope.cuh")),
+    "rope_apply": tuple(_CSRC + f for f in ("rope_apply.cu", "rope.cuh")),
+    "attn_bwd": tuple(_CSRC + f for f in ("attn_bwd.cu", "ptx.cuh", "rope.cuh")),
+}
+TRAFFIC_KINDS = {"attn_fwd_fused": "attn_fwd", "attn_fwd_plain": "attn_fwd", "attn_fwd_split": "attn_fwd",
+                 "rope_apply_qk": "rope_apply", "bwd_dkdv": "attn_bwd", "bwd_dq": "attn_bwd"}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -55,9 +61,10 @@ def load_peaks(path=None):
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(group: str = "attn_fwd") -> str:
+    """Hash of the sources one kernel group is compiled from (`KERNEL_SOURCES`)."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[group]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -71,7 +78,7 @@ def load_traffic(kind: str, workload: str):
             rec = json.load(f)[kind][workload]
     except (OSError, KeyError, ValueError):
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(TRAFFIC_KINDS.get(kind, "attn_fwd")):
         return None
     return float(rec["dram_bytes_per_launch"])
 
