@@ -86,7 +86,7 @@ size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_m
  * choice): grouped-query attention (Hq / Hkv >= 2) with N >= 2048 -> SPLIT (fastest at 9 of 10
  * measured points from 2048 to 16384, pre-rotation at the tenth); multi-head attention (Hq == Hkv)
  * with N >= 3072 -> PREROTATE (measured N* ~ 3100 against FUSED); everything else -> FUSED.
- * Host-only and pure: no device access; arguments it cannot judge (non-positive sizes, Hq not a
+ * Host-only and pure: no device access; arguments it cannot classify (non-positive sizes, Hq not a
  * multiple of Hkv) give FUSED.
  */
 attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype);
