@@ -1,14 +1,15 @@
 /*
- * libattnfuse — causal softmax attention with Rotary Position Embedding (RoPE), forward, for
- * NVIDIA GB300 (sm_103a).  C ABI: plain pointers and sizes, no framework types.
+ * libattnfuse — causal softmax attention with Rotary Position Embedding (RoPE), forward and
+ * backward, for NVIDIA GB300 (sm_103a).  C ABI: plain pointers and sizes, no framework types.
  *
  * The operation.  "AttnFuse Makes RoPE a First-Class Attention Compilation Operation" (2026-09-13
  * AI papers report), paragraphs 1-2, and the AttnFuse abstract (arxivdaily 2609.13612): RoPE is a
  * transformation of Q and K applied before the QK^T product, composed with the causality and
  * softmax building blocks into one fused kernel.  Paragraphs 3-5 of the same report weigh that
  * fused form against rotating Q and K in a separate pass first ("pre-rotation"), whose cost is
- * memory bandwidth where the fused form's is compute; both forms are offered here.  The pages print
- * no formula; this library fixes:
+ * memory bandwidth where the fused form's is compute; both forms are offered here, and a third that
+ * the GB300 measurements favour for grouped-query attention (K rotated in a pass, Q on chip: see
+ * ATTNFUSE_SPLIT).  The pages print no formula; this library fixes:
  *     theta_k = rope_base^(-2k/d), k = 0 .. d/2-1, pairs (k, k + d/2), position = token index,
  *     x'[k] = x[k] cos(p theta_k) - x[k+d/2] sin(p theta_k),
  *     x'[k+d/2] = x[k+d/2] cos(p theta_k) + x[k] sin(p theta_k)       (Q and K; V is not rotated)
