@@ -528,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tmQ);
       ptx::tma_prefetch_desc(&tmK);
       ptx::tma_prefetch_desc(&tmV);
+      // After a pre-rotation pass (pre-rotate and split modes) this launch may start early; nothing
+      // that pass writes is read before this point.
+      if constexpr (!(ROTATE && ROT_K)) ptx::grid_dep_wait();
       int gk = 0, gv = 0, uc = 0;
       bool ok = true;
       FOR_EACH_UNIT(U) {
@@ -880,7 +883,21 @@ cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t s
   // Persistent: one CTA per SM (shared memory and registers admit only one), each walking its share
   // of the work units.
   const int grid = p.total_units < sm_count[dev] ? p.total_units : sm_count[dev];
-  kernel<<<dim3((unsigned)grid), dim3(kThreads), Cfg<D>::SMEM, stream>>>(maps.q, maps.k, maps.v, p);
+  // After this library's pre-rotation pass the kernel is launched as a programmatic dependent: its
+  // prologue (barriers, tensor memory, descriptor prefetch) overlaps the end of the pass, and the
+  // TMA producer waits for the pass before its first load.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.after_rope_pass ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kernel, maps.q, maps.k, maps.v, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

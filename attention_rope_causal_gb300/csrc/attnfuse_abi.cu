@@ -351,6 +351,7 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
       return cuda_fail(e, "rope_apply launch");
     }
     ka = ws;
+    p.after_rope_pass = 1;
   } else if (mode == ATTNFUSE_PREROTATE) {
     void* ws = workspace;
     if (!ws) {
@@ -406,6 +407,7 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
     }
     qa = qr;
     ka = kr;
+    p.after_rope_pass = 1;
   }
 
   AttnMaps maps;

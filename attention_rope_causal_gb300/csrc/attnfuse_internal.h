@@ -52,6 +52,7 @@ struct AttnParams {
   float* lse;        // [B, Hq, N] or nullptr
   float scale_log2;  // log2(e) / sqrt(d)
   int rot_chunks;    // rotary_dim / 16 (fused mode: rotation thread chunk ck < rot_chunks works)
+  int after_rope_pass;  // 1: launched right after this library's pre-rotation pass on the same stream
   int interleaved;   // 0: pairs (k, k + rotary_dim/2); 1: pairs (2k, 2k + 1)
   unsigned long long timeout_ns;  // limit on any single barrier wait
   RopeFreqs freqs;

@@ -54,6 +54,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
+// before the previous kernel in the stream has finished; it must wait here before reading what that
+// kernel wrote.  The previous kernel lets it launch early by signalling (no effect without a
+// dependent launch).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // Proxy fences
 
 // Generic-proxy writes to shared memory -> later reads by the async proxy (tcgen05.mma, TMA store).

@@ -26,6 +26,7 @@ constexpr int kThreads = 256;
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads) rope_apply_kernel(const __grid_constant__ RopeApplyParams p) {
   constexpr int NCH = D / 16;  // work items per head row; each covers two 16-byte chunks
+  ptx::grid_dep_launch_dependents();  // the attention kernel after this pass may start its prologue
   const long long item = (long long)blockIdx.x * kThreads + threadIdx.x;
   const long long per_token = (long long)p.groups_total * NCH;
   const long long token = item / per_token;
