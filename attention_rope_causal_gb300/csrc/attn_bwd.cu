@@ -131,6 +131,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ AttnBwdParams p) {
   constexpr int TPR = D / 8;  // threads per row: 16 (d = 128) or 8 (d = 64)
+  ptx::grid_dep_launch_dependents();
+  ptx::grid_dep_wait();  // launched as a dependent of the pre-rotation pass
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = tid / TPR;
   const int part = (int)(tid % TPR);
@@ -231,6 +233,10 @@ __device__ __forceinline__ void bwd_setup(BwdCtrl& ctl, int warp) {
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // Launched as a programmatic dependent of the previous kernel in the chain: the set-up above
+  // overlaps its end; nothing it wrote is read before this wait.
+  ptx::grid_dep_launch_dependents();
+  ptx::grid_dep_wait();
 }
 
 __device__ __forceinline__ void bwd_teardown(BwdCtrl& ctl, int warp, uint32_t tmem) {
@@ -711,6 +717,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   bwd_teardown(ctl, warp, tmem);
 }
 
+// Launch as a programmatic dependent of the previous kernel on the stream (it waits in-kernel).
+template <typename K, typename... Args>
+cudaError_t launch_dependent(K kernel, dim3 grid, dim3 block, uint32_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // One CTA per SM (shared memory admits one), each walking its share of the units.  TAG separates
 // the per-device set-up caches of kernels that share a signature.
 template <int TAG, typename K>
@@ -731,8 +755,7 @@ cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const AttnBwdM
     sm_count[dev] = n;
   }
   const int grid = units < sm_count[dev] ? units : sm_count[dev];
-  kernel<<<dim3((unsigned)grid), dim3(kThreads), smem, stream>>>(m.q, m.k, m.v, m.dout, p);
-  return cudaGetLastError();
+  return launch_dependent(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, m.q, m.k, m.v, m.dout, p);
 }
 
 template <int D, bool BF16>
@@ -740,8 +763,7 @@ cudaError_t launch_bwd_impl(const AttnBwdMaps& m, const AttnBwdParams& p, cudaSt
   const long long rows = (long long)p.B * p.N * p.Hq;
   const long long blocks = (rows * (D / 8) + 255) / 256;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  bwd_prep_kernel<D, BF16><<<dim3((unsigned)blocks), dim3(256), 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(bwd_prep_kernel<D, BF16>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_persistent<2 * D + BF16 * 1>(bwd_dkdv_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hkv * p.n_tiles, m, p,
                                           stream);
