@@ -197,11 +197,11 @@ attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnf
   (void)dtype;
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0) return ATTNFUSE_FUSED;
   // Measured on GB300 (bench.py --sweep): with 4:1 GQA, rotating K in a pass and Q on chip (split)
-  // is fastest at 9 of the 10 points in N in [2048, 16384] (pre-rotation at the tenth, within 3%),
-  // fused slowest everywhere; with MHA d=64 fused wins below N* ~ 3100 (3117 bf16, 3238 fp16) and
-  // pre-rotation above (split within 1% of it).
+  // is fastest at 8 of the 10 points in N in [2048, 16384] (pre-rotation at N = 8192, within 2%),
+  // fused slowest everywhere; with MHA d=64 fused ties pre-rotation at N = 2048 (N* ~ 2060) and
+  // pre-rotation wins above (split within 1% of it).
   if (Hq / Hkv >= 2) return N >= 2048 ? ATTNFUSE_SPLIT : ATTNFUSE_FUSED;
-  return N >= 3072 ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
+  return N >= 2064 ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
 }
 
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype) {

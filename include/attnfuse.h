@@ -84,9 +84,9 @@ size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_m
 /*
  * The fastest mode for a shape on GB300, from the measured sweep of all three ("Rotation Calculus" in
  * "AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraph 2, made a runtime
- * choice): grouped-query attention (Hq / Hkv >= 2) with N >= 2048 -> SPLIT (fastest at 9 of 10
- * measured points from 2048 to 16384, pre-rotation at the tenth); multi-head attention (Hq == Hkv)
- * with N >= 3072 -> PREROTATE (measured N* ~ 3100 against FUSED); everything else -> FUSED.
+ * choice): grouped-query attention (Hq / Hkv >= 2) with N >= 2048 -> SPLIT (fastest at 8 of 10
+ * measured points from 2048 to 16384, pre-rotation at the other two); multi-head attention
+ * (Hq == Hkv) with N >= 2064 -> PREROTATE (measured N* ~ 2060 against FUSED); else -> FUSED.
  * Host-only and pure: no device access; arguments it cannot classify (non-positive sizes, Hq not a
  * multiple of Hkv) give FUSED.
  */

@@ -83,7 +83,7 @@ def test_workspace_bytes(lib):
 @pytest.mark.parametrize("B,Hq,Hkv,N,mode", [
     (1, 32, 8, 4096, 3), (4, 32, 8, 2048, 3), (1, 32, 8, 16384, 3), (8, 32, 8, 1024, 0),  # GQA 4:1
     (1, 8, 4, 3000, 3), (1, 64, 8, 2047, 0),                                           # other groups
-    (2, 16, 16, 2048, 0), (1, 16, 16, 3071, 0), (1, 16, 16, 3072, 1), (1, 16, 16, 32768, 1),  # MHA
+    (2, 16, 16, 2048, 0), (1, 16, 16, 2063, 0), (1, 16, 16, 2064, 1), (1, 16, 16, 32768, 1),  # MHA
     (0, 16, 16, 4096, 0), (1, 6, 4, 4096, 0),                                          # not classified
 ])
 def test_select_mode_follows_the_measured_crossover(lib, B, Hq, Hkv, N, mode):
