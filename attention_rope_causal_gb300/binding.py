@@ -243,3 +243,30 @@ def diag_wait_timeout(timeout_ns: int, stream=None):
 
 def last_error() -> str:
     return load().attnfuse_last_error().decode(errors="replace")
+
+
+class RopeCausalAttention(torch.autograd.Function):
+    """torch.autograd wrapper: forward through ``attnfuse_rope_causal_fwd``, backward through
+    ``attnfuse_rope_causal_bwd`` (gradients for q, k, v; the lse output carries none)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, rope_base: float, mode: str = "auto", rotary_dim=None, interleaved: bool = False):
+        out, lse = rope_causal_fwd(q, k, v, rope_base, mode=mode, rotary_dim=rotary_dim, interleaved=interleaved)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.rope = (rope_base, rotary_dim, interleaved)
+        ctx.mark_non_differentiable(lse)
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, dlse):
+        q, k, v, out, lse = ctx.saved_tensors
+        rope_base, rotary_dim, interleaved = ctx.rope
+        dq, dk, dv = rope_causal_bwd(q, k, v, out, lse, dout.contiguous(), rope_base, rotary_dim=rotary_dim,
+                                     interleaved=interleaved)
+        return dq, dk, dv, None, None, None, None
+
+
+def rope_causal_attention(q, k, v, rope_base: float, mode: str = "auto", rotary_dim=None, interleaved: bool = False):
+    """Differentiable causal RoPE attention: returns out [B, N, Hq, d] (lse is kept for the backward)."""
+    out, _ = RopeCausalAttention.apply(q, k, v, rope_base, mode, rotary_dim, interleaved)
+    return out
