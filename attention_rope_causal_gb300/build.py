@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libattnfuse.so")
 
-UNITS = ("attnfuse_abi.cu", "attn_fwd.cu", "attn_bwd.cu", "rope_apply.cu", "noalloc.cu")
+UNITS = ("attnfuse_abi.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu", "rope_apply.cu", "noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -113,6 +113,32 @@ attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, i
 
 size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N * (size_t)H * (size_t)d * 2u; }
 
+// Few queries per KV head (decode, a short prefill after a cache): the split-KV decode kernels
+// serve FUSED and AUTO calls with N <= 16 and (Hq / Hkv) N <= 64 query rows per KV head.
+constexpr int kDecodeMaxN = 16;
+
+bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
+  return (mode == ATTNFUSE_FUSED || mode == ATTNFUSE_AUTO) && N <= kDecodeMaxN && (Hq / Hkv) * N <= kDecodeMaxRows &&
+         B <= 65535 && Hkv <= 65535;  // grid y and z
+}
+
+// Splits of the keys: enough CTAs for ~2 waves over 152 SMs, 64-key multiples.
+void decode_plan(int B, int Hkv, int Nk, int* keys_per_split, int* n_splits) {
+  const int chunks = (Nk + 63) / 64;
+  const int want = (304 + B * Hkv - 1) / (B * Hkv);
+  const int splits = want < 1 ? 1 : (want > chunks ? chunks : want);
+  const int per = (chunks + splits - 1) / splits;  // chunks per split
+  *keys_per_split = 64 * per;
+  *n_splits = (Nk + *keys_per_split - 1) / *keys_per_split;
+}
+
+size_t decode_workspace_bytes(int B, int Hkv, int Nk, int d) {
+  int kps = 0, ns = 0;
+  decode_plan(B, Hkv, Nk, &kps, &ns);
+  const size_t slots = (size_t)B * Hkv * ns * kDecodeMaxRows;
+  return round_up(slots * d * sizeof(float), 256) + round_up(slots * 2 * sizeof(float), 256);
+}
+
 // The options of an _ex call with their defaults filled in.
 struct Opts {
   int rdim;        // rotary dimension (0 -> d)
@@ -214,6 +240,8 @@ size_t attnfuse_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfus
   if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return 0;
   const int Nk = (opts && opts->kv_len) ? opts->kv_len : N;
   if (Nk < N) return 0;
+  if (Hq % Hkv != 0) return 0;
+  if (decode_eligible(B, Hq, Hkv, N, mode)) return decode_workspace_bytes(B, Hkv, Nk, d);
   if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
   if (mode == ATTNFUSE_SPLIT) return round_up(tensor_bytes(B, Nk, Hkv, d), 256);
   if (mode != ATTNFUSE_PREROTATE) return 0;
@@ -284,7 +312,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   Opts o;
   if ((st = resolve_opts(opts, d, N, &o)) != ATTNFUSE_OK) return st;
   const int Nk = o.Nk;
-  if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
+  const bool decode = decode_eligible(B, Hq, Hkv, N, mode);
+  if (mode == ATTNFUSE_AUTO && !decode) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
   const size_t need = attnfuse_workspace_bytes_ex(B, Hq, Hkv, N, d, mode, dtype, opts);
   if (workspace) {
     if (workspace_bytes < need)
@@ -293,6 +322,47 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   }
   if ((st = check_device()) != ATTNFUSE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (decode) {
+    DecodeParams dp;
+    std::memset(&dp, 0, sizeof dp);
+    dp.q = q;
+    dp.k = k;
+    dp.v = v;
+    dp.out = out;
+    dp.lse = lse;
+    dp.B = B;
+    dp.Hq = Hq;
+    dp.Hkv = Hkv;
+    dp.N = N;
+    dp.Nk = Nk;
+    dp.q_off = Nk - N;
+    dp.qpos = o.qpos;
+    dp.kpos = o.kpos;
+    dp.rot_chunks = o.rdim / 16;
+    dp.interleaved = o.interleaved;
+    decode_plan(B, Hkv, Nk, &dp.keys_per_split, &dp.n_splits);
+    dp.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
+    rope_freqs_host(o.rdim, rope_base, &dp.freqs);
+    void* owned = nullptr;
+    void* ws = workspace;
+    if (!ws) {
+      cudaError_t e = cudaMallocAsync(&owned, need, s);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ATTNFUSE_ERR_NO_MEMORY, "cudaMallocAsync(%zu) for the decode partials failed: %s", need,
+                    cudaGetErrorString(e));
+      }
+      ws = owned;
+    }
+    const size_t slots = (size_t)B * Hkv * dp.n_splits * kDecodeMaxRows;
+    dp.part_o = static_cast<float*>(ws);
+    dp.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(slots * d * sizeof(float), 256));
+    cudaError_t e = launch_attn_decode(dp, d, dtype == ATTNFUSE_BF16, s);
+    if (owned) cudaFreeAsync(owned, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ATTNFUSE_OK;
+  }
 
   AttnParams p;
   std::memset(&p, 0, sizeof p);

@@ -67,6 +67,32 @@ struct AttnMaps {
 cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bool bf16, bool rotate_q,
                             bool rotate_k, cudaStream_t stream, const char** why);
 
+// ---- decode kernels (few queries, many keys) ---------------------------------------------------
+
+constexpr int kDecodeMaxRows = 64;  // query rows per KV head: (Hq / Hkv) * N
+
+struct DecodeParams {
+  const void* q;          // [B, N, Hq, d]
+  const void* k;          // [B, Nk, Hkv, d]
+  const void* v;          // [B, Nk, Hkv, d]
+  void* out;              // [B, N, Hq, d]
+  float* lse;             // [B, Hq, N] or nullptr
+  int B, Hq, Hkv, N, Nk, q_off;
+  const int32_t* qpos;    // [B, N] or nullptr (q_off + i)
+  const int32_t* kpos;    // [B, Nk] or nullptr (j)
+  int rot_chunks;         // rotary_dim / 16
+  int interleaved;
+  int keys_per_split;     // multiple of 64
+  int n_splits;
+  float scale_log2;       // log2(e) / sqrt(d)
+  float* part_o;          // [B, Hkv, n_splits, rows, d] unnormalised partial outputs
+  float* part_ml;         // [B, Hkv, n_splits, rows, 2]: running max (log2 units) and sum
+  RopeFreqs freqs;
+};
+
+// Split-KV decode: one CTA per (split, KV head, batch) writes partials, a second kernel merges them.
+cudaError_t launch_attn_decode(const DecodeParams& p, int d, bool bf16, cudaStream_t stream);
+
 // ---- backward kernels ------------------------------------------------------------------------
 
 struct AttnBwdParams {

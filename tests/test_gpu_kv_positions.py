@@ -74,10 +74,16 @@ def _check_both_modes(q, k, v, dt, label, **kw):
         outs[mode] = (o.cpu(), l.cpu())
         assert_close(o.double().cpu().numpy(), l.double().cpu().numpy(), o_ref, l_ref, dt, f"{mode} {label}")
     t = TOL[dt]
+    N, Hq, Hkv = q.shape[1], q.shape[2], k.shape[2]
     for m in ("fused", "split"):
         e = errors(outs[m][0].double().numpy(), outs[m][1].double().numpy(),
                    outs["prerotate"][0].double().numpy(), outs["prerotate"][1].double().numpy())
-        assert e["max_abs"] <= t["max_abs"] / 4 and e["rel_l2"] <= t["rel_l2"] / 4, (m, e)
+        rel = t["rel_l2"] / 4
+        if m == "fused" and N <= 16 and (Hq // Hkv) * N <= 64:
+            # the fused call runs the split-KV decode kernels: they keep P in fp32 and sum in another
+            # order, so the outputs differ by about one rounding of the output type
+            rel = max(rel, 2.0 ** -7 if dt == "bf16" else 2.0 ** -10)
+        assert e["max_abs"] <= t["max_abs"] / 4 and e["rel_l2"] <= rel, (m, e)
     return outs
 
 
