@@ -1,5 +1,5 @@
 // Causal RoPE attention for a few queries against many keys (decode, short prefill after a cache):
-// split-KV on the CUDA cores.  With N queries and rows = (Hq / Hkv) N <= 64 query rows per KV head
+// split-KV on the CUDA cores.  With N queries and rows = (Hq / Hkv) N <= 16 query rows per KV head
 // the tensor-core tile kernels keep one useful row in 128 and take ~25x the HBM time of reading K
 // and V; this path reads every K and V row once.
 //
@@ -39,12 +39,13 @@ template <int D>
 struct DecCfg {
   static constexpr int KSTRIDE = D + 8;  // bf16/fp16 elements per K row in shared memory (padding
                                          // spreads consecutive rows over the banks)
-  static constexpr uint32_t OFF_Q = 0;                                            // fp32 [64][D]
+  static constexpr uint32_t OFF_Q = 0;                                            // fp32 [rows][D]
   static constexpr uint32_t OFF_K = OFF_Q + kDecodeMaxRows * D * 4;               // 16-bit [64][KSTRIDE]
   static constexpr uint32_t OFF_V = OFF_K + kChunk * KSTRIDE * 2;                 // 16-bit [64][D]
-  static constexpr uint32_t OFF_S = OFF_V + kChunk * D * 2;                       // fp32 [64 rows][64 keys]
-  static constexpr uint32_t OFF_ROW = OFF_S + kDecodeMaxRows * kChunk * 4;        // fp32 [64] m, l, alpha
-  static constexpr uint32_t SMEM = OFF_ROW + 3 * kDecodeMaxRows * 4;
+  static constexpr uint32_t OFF_S = OFF_V + kChunk * D * 2;                       // fp32 [rows][64 keys]
+  static constexpr uint32_t OFF_ROW = OFF_S + kDecodeMaxRows * kChunk * 4;        // fp32 [rows] m, l, alpha
+  static constexpr uint32_t OFF_FREQ = OFF_ROW + 3 * kDecodeMaxRows * 4;         // u32 F_k lo[64], hi[64]
+  static constexpr uint32_t SMEM = OFF_FREQ + 2 * 64 * 4;
 };
 
 // Offsets, inside a head vector, of the 8 rotation pairs of frequency group fg (frequencies
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
   float* sM = reinterpret_cast<float*>(smem + C::OFF_ROW);
   float* sL = sM + kDecodeMaxRows;
   float* sA = sL + kDecodeMaxRows;
+  uint32_t* sF = reinterpret_cast<uint32_t*>(smem + C::OFF_FREQ);  // lo[64] then hi[64]
 
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
@@ -101,6 +103,9 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
     sM[tid] = -INFINITY;
     sL[tid] = 0.f;
   }
+  // F_k in shared memory: per-lane frequency indices would serialise constant-bank loads.
+  if (tid < 64) sF[tid] = p.freqs.lo[tid];
+  else if (tid < 128) sF[tid] = p.freqs.hi[tid - 64];
   __syncthreads();
   for (int idx = tid; idx < rows * p.rot_chunks; idx += kThreads) {
     const int row = idx / p.rot_chunks, fg = idx % p.rot_chunks;
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       float c, s;
-      rope_cs_signed(pos, p.freqs.lo[8 * fg + t], p.freqs.hi[8 * fg + t], c, s);
+      rope_cs_signed(pos, sF[8 * fg + t], sF[64 + 8 * fg + t], c, s);
       int ia, ib;
       pair_index(fg, t, r, il, ia, ib);
       const float x = sQ[row * D + ia], y = sQ[row * D + ib];
@@ -125,46 +130,84 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
   // Rows past the rotary dimension and unrotated entries were already exact copies.
 
   // O accumulators: thread owns items (row, column pair) it = tid + kThreads * n.
-  constexpr int kMaxItems = kDecodeMaxRows * (D / 2) / kThreads;  // 16 (d = 128) or 8 (d = 64)
+  constexpr int kMaxItems = kDecodeMaxRows * (D / 2) / kThreads;  // 4 (d = 128) or 2 (d = 64)
   float oacc[kMaxItems][2];
 #pragma unroll
   for (int n = 0; n < kMaxItems; ++n) oacc[n][0] = oacc[n][1] = 0.f;
   const int n_items = rows * (D / 2);
 
-  for (int kc = key0; kc < key_end; kc += kChunk) {
-    __syncthreads();  // previous chunk's K, V, S no longer read
-    // ---- K and V rows of the chunk (zero past the split or the sequence) --------------------
-    for (int idx = tid; idx < kChunk * (D / 8); idx += kThreads) {
-      const int kr = idx / (D / 8), c8 = idx % (D / 8);
+  // K and V rows of a chunk: LPT 16-byte pieces per thread, all loads issued before any is used;
+  // the next chunk's are in flight while the current one is computed on.
+  constexpr int LPT = kChunk * (D / 8) / kThreads;  // 4 (d = 128) or 2 (d = 64)
+  uint4 kpre[LPT], vpre[LPT];
+  auto load_chunk = [&](int kc) {
+#pragma unroll
+    for (int n = 0; n < LPT; ++n) {
+      const int idx = tid + kThreads * n, kr = idx / (D / 8), c8 = idx % (D / 8);
       const int j = kc + kr;
-      uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
+      kpre[n] = vpre[n] = make_uint4(0, 0, 0, 0);  // zero past the split or the sequence
       if (j < key_end) {
         const size_t off = (((size_t)b * p.Nk + j) * p.Hkv + hk) * D + 8 * c8;
-        kw = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k) + off);
-        vw = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v) + off);
+        kpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k) + off));
+        vpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v) + off));
       }
-      *reinterpret_cast<uint4*>(sK + kr * C::KSTRIDE + 8 * c8) = kw;
-      *reinterpret_cast<uint4*>(sV + kr * D + 8 * c8) = vw;
     }
+  };
+  if (key0 < key_end) load_chunk(key0);
+  // cos/sin of the thread's key-rotation items (see below) and their advance by 64 positions.
+  constexpr int KIT = (kChunk * (D / 16) + kThreads - 1) / kThreads;  // 2 (d = 128) or 1 (d = 64)
+  RopeCS8 kcs[KIT], kstep[KIT];
+#pragma unroll
+  for (int n = 0; n < KIT; ++n) {
+    const int idx = tid + kThreads * n;
+    const int fg = p.rot_chunks > 0 ? idx % p.rot_chunks : 0;
+    rope_cs8_exact((uint32_t)kChunk, sF, sF + 64, 8 * fg, kstep[n]);
+  }
+
+  for (int kc = key0; kc < key_end; kc += kChunk) {
+    __syncthreads();  // previous chunk's K, V, S no longer read
+#pragma unroll
+    for (int n = 0; n < LPT; ++n) {
+      const int idx = tid + kThreads * n, kr = idx / (D / 8), c8 = idx % (D / 8);
+      *reinterpret_cast<uint4*>(sK + kr * C::KSTRIDE + 8 * c8) = kpre[n];
+      *reinterpret_cast<uint4*>(sV + kr * D + 8 * c8) = vpre[n];
+    }
+    if (kc + kChunk < key_end) load_chunk(kc + kChunk);
     __syncthreads();
-    // ---- rotate the chunk's keys in place (exact cos/sin at each key's position) ------------
-    for (int idx = tid; idx < kChunk * p.rot_chunks; idx += kThreads) {
+    // ---- rotate the chunk's keys in place ------------------------------------------------------
+    // Thread item n: key row kr, frequency group fg (8 frequencies, two 16-byte pieces).  Positions
+    // j: cos/sin carried from chunk to chunk by the exact rotation of 64 positions, exact again every
+    // 16 chunks; explicit positions: exact per key.
+#pragma unroll
+    for (int n = 0; n < KIT; ++n) {
+      const int idx = tid + kThreads * n;
+      if (idx >= kChunk * p.rot_chunks) break;
       const int kr = idx / p.rot_chunks, fg = idx % p.rot_chunks;
       const int j = kc + kr;
-      if (j >= key_end) continue;
-      const int32_t pos = p.kpos ? p.kpos[(size_t)b * p.Nk + j] : j;
-      T* row = sK + kr * C::KSTRIDE;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        float c, s;
-        rope_cs_signed(pos, p.freqs.lo[8 * fg + t], p.freqs.hi[8 * fg + t], c, s);
-        int ia, ib;
-        pair_index(fg, t, r, il, ia, ib);
-        float xr, yr;
-        rope_pair(static_cast<float>(row[ia]), static_cast<float>(row[ib]), c, s, xr, yr);
-        row[ia] = static_cast<T>(xr);
-        row[ib] = static_cast<T>(yr);
+      if (p.kpos != nullptr) {
+        if (j < key_end) rope_cs8_exact_signed(p.kpos[(size_t)b * p.Nk + j], sF, sF + 64, 8 * fg, kcs[n]);
+      } else if (((kc - key0) / kChunk) % 16 == 0) {
+        rope_cs8_exact((uint32_t)j, sF, sF + 64, 8 * fg, kcs[n]);
       }
+      if (j < key_end) {
+        T* row = sK + kr * C::KSTRIDE;
+        if (il) {
+          uint4* a = reinterpret_cast<uint4*>(row + 16 * fg);
+          uint4 x = a[0], y = a[1];
+          rope_rotate_chunk_il_cs8<BF16>(x, kcs[n], 0);
+          rope_rotate_chunk_il_cs8<BF16>(y, kcs[n], 1);
+          a[0] = x;
+          a[1] = y;
+        } else {
+          uint4* xa = reinterpret_cast<uint4*>(row + 8 * fg);
+          uint4* ya = reinterpret_cast<uint4*>(row + r / 2 + 8 * fg);
+          uint4 x = *xa, y = *ya;
+          rope_rotate_chunk_cs8<BF16>(x, y, kcs[n]);
+          *xa = x;
+          *ya = y;
+        }
+      }
+      if (p.kpos == nullptr) rope_cs8_advance(kcs[n], kstep[n]);
     }
     __syncthreads();
     // ---- scores (log2 units): thread = key kr, rows rg, rg + 4, ... --------------------------
@@ -174,15 +217,23 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
       const T* krow = sK + kr * C::KSTRIDE;
       for (int row = rg; row < rows; row += kThreads / kChunk) {
         const int i = row % p.N;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int e = 0; e < D; e += 2) {
-          float k0, k1;
-          Pack<BF16>::unpack(*reinterpret_cast<const uint32_t*>(krow + e), k0, k1);
-          acc = fmaf(sQ[row * D + e], k0, fmaf(sQ[row * D + e + 1], k1, acc));
+        const float* qrow = sQ + row * D;
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+        for (int e = 0; e < D; e += 8) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(krow + e);
+          const float4 qa = *reinterpret_cast<const float4*>(qrow + e);
+          const float4 qb = *reinterpret_cast<const float4*>(qrow + e + 4);
+          float k0, k1, k2, k3, k4, k5, k6, k7;
+          Pack<BF16>::unpack(kv.x, k0, k1);
+          Pack<BF16>::unpack(kv.y, k2, k3);
+          Pack<BF16>::unpack(kv.z, k4, k5);
+          Pack<BF16>::unpack(kv.w, k6, k7);
+          acc0 = fmaf(qa.x, k0, fmaf(qa.y, k1, fmaf(qa.z, k2, fmaf(qa.w, k3, acc0))));
+          acc1 = fmaf(qb.x, k4, fmaf(qb.y, k5, fmaf(qb.z, k6, fmaf(qb.w, k7, acc1))));
         }
         const bool visible = j < key_end && j <= p.q_off + i;
-        sS[row * kChunk + kr] = visible ? acc * p.scale_log2 : -INFINITY;
+        sS[row * kChunk + kr] = visible ? (acc0 + acc1) * p.scale_log2 : -INFINITY;
       }
     }
     __syncthreads();

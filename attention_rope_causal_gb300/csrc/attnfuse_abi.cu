@@ -113,16 +113,24 @@ attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, i
 
 size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N * (size_t)H * (size_t)d * 2u; }
 
-// Few queries per KV head (decode, a short prefill after a cache): the split-KV decode kernels
-// serve FUSED and AUTO calls with N <= 16 and (Hq / Hkv) N <= 64 query rows per KV head.
-constexpr int kDecodeMaxN = 16;
+// Few queries per KV head (decode, speculative decode): the split-KV decode kernels serve FUSED and
+// AUTO calls with at most 16 query rows (rows = (Hq / Hkv) N) per KV head, B Hkv <= 32 KV heads in
+// the batch and B Hkv rows <= 128.  Their cost grows with B Hkv (every KV head's keys are rotated
+// and dotted on the CUDA cores), the tile kernels' hardly does until their units fill the SMs.
+// Measured on GB300 (d = 128, bf16, Nk = 4096 and 32768): with 4 rows the decode kernels win up
+// to B Hkv = 32 (65 vs 72 us at 4096 keys) and lose at 64 (126 vs 83 us); with 16 rows they win at
+// B Hkv = 8 (54 vs 64 us) and lose at 16 (76 vs 67 us).
+constexpr int kDecodeMaxKvHeads = 32;
+constexpr int kDecodeMaxKvHeadRows = 128;
 
 bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
-  return (mode == ATTNFUSE_FUSED || mode == ATTNFUSE_AUTO) && N <= kDecodeMaxN && (Hq / Hkv) * N <= kDecodeMaxRows &&
-         B <= 65535 && Hkv <= 65535;  // grid y and z
+  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_AUTO) return false;
+  const long long rows = (long long)(Hq / Hkv) * N, heads = (long long)B * Hkv;
+  return rows <= kDecodeMaxRows && heads <= kDecodeMaxKvHeads && heads * rows <= kDecodeMaxKvHeadRows;
 }
 
-// Splits of the keys: enough CTAs for ~2 waves over 152 SMs, 64-key multiples.
+// Splits of the keys: about two CTAs per SM over 152 SMs, in 64-key multiples (three per SM measured
+// slower over 32K keys: more partials to merge).
 void decode_plan(int B, int Hkv, int Nk, int* keys_per_split, int* n_splits) {
   const int chunks = (Nk + 63) / 64;
   const int want = (304 + B * Hkv - 1) / (B * Hkv);

@@ -69,7 +69,7 @@ cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bo
 
 // ---- decode kernels (few queries, many keys) ---------------------------------------------------
 
-constexpr int kDecodeMaxRows = 64;  // query rows per KV head: (Hq / Hkv) * N
+constexpr int kDecodeMaxRows = 16;  // query rows per KV head: (Hq / Hkv) * N
 
 struct DecodeParams {
   const void* q;          // [B, N, Hq, d]
