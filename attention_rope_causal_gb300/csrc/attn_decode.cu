@@ -1,7 +1,7 @@
-// Causal RoPE attention for a few queries against many keys (decode, short prefill after a cache):
-// split-KV on the CUDA cores.  With N queries and rows = (Hq / Hkv) N <= 16 query rows per KV head
-// the tensor-core tile kernels keep one useful row in 128 and take ~25x the HBM time of reading K
-// and V; this path reads every K and V row once.
+// Causal RoPE attention for a few queries against many keys (decode, speculative decode): split-KV.
+// With N queries and rows = (Hq / Hkv) N <= 16 query rows per KV head the 128-row tile kernels keep
+// at most one useful row in eight and walk each KV head's keys in one CTA; here the keys of every
+// KV head are split over many CTAs and the products run as 16-row tensor-core tiles.
 //
 // What it computes: the function of attnfuse_rope_causal_fwd (header of include/attnfuse.h) in
 // its general form -- the N queries are the last N of the Nk tokens, query i sees keys j <= Nk - N
@@ -9,15 +9,21 @@
 // ("AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraphs 1-2: RoPE on Q
 // and K before the product, causal mask, softmax).
 //
-// attn_decode_kernel: one CTA per (split of keys_per_split keys, KV head, batch), 256 threads.  The
-// CTA rotates its query rows once (exact cos/sin per row) into fp32 shared memory, then walks its
-// keys 64 at a time: K and V rows to shared memory (16-byte loads), K rotated there at each key's
-// position (exact cos/sin, rounded to the input type like the other paths), scores for every (row,
-// key), online softmax per row (exp2, fp32 max and sum), O += P V in registers.  It writes the
-// unnormalised O, the running max (log2 units) and the sum of its split.
+// attn_decode_kernel: one CTA per (split of keys_per_split keys, KV head, batch), 256 threads, two
+// CTAs per SM.  The CTA rotates its query rows once (exact cos/sin per row) into fp32 shared
+// memory, then walks its keys 64 at a time: the next chunk's K and V rows are loaded into registers
+// (16-byte loads) while the current chunk is processed; K is rotated in shared memory by cos/sin
+// carried from chunk to chunk (advanced by the exact rotation of 64 positions, recomputed exactly
+// every 16 chunks; exact per key with explicit positions) and rounded to the input type like the
+// other paths; S = Q K^T by m16n8k16 MMAs (warp w: keys 8w .. 8w + 7), online softmax per row (exp2,
+// fp32 max and sum, P rounded to the input type), O += P V by MMAs (warp w: 8 d / 64 columns) with
+// the accumulators in registers.  It writes the unnormalised O, the running max (log2 units) and the
+// sum of its split.
 // attn_decode_combine_kernel: one warp per (batch, KV head, row) merges the splits (rescaling each
-// by 2^(m_s - m)) into out and lse.
-// No barrier waits, so nothing here can time out.
+// by 2^(m_s - m)) into out and lse; launched as a programmatic dependent of the first kernel, it
+// waits (griddepcontrol.wait) for that grid to complete before reading the partials.
+// No spin-waits: the first kernel synchronises only with __syncthreads, so the second one's wait
+// ends when the first grid does.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -37,15 +43,22 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct DecCfg {
-  static constexpr int KSTRIDE = D + 8;  // bf16/fp16 elements per K row in shared memory (padding
-                                         // spreads consecutive rows over the banks)
-  static constexpr uint32_t OFF_Q = 0;                                            // fp32 [rows][D]
-  static constexpr uint32_t OFF_K = OFF_Q + kDecodeMaxRows * D * 4;               // 16-bit [64][KSTRIDE]
-  static constexpr uint32_t OFF_V = OFF_K + kChunk * KSTRIDE * 2;                 // 16-bit [64][D]
-  static constexpr uint32_t OFF_S = OFF_V + kChunk * D * 2;                       // fp32 [rows][64 keys]
-  static constexpr uint32_t OFF_ROW = OFF_S + kDecodeMaxRows * kChunk * 4;        // fp32 [rows] m, l, alpha
-  static constexpr uint32_t OFF_FREQ = OFF_ROW + 3 * kDecodeMaxRows * 4;         // u32 F_k lo[64], hi[64]
-  static constexpr uint32_t SMEM = OFF_FREQ + 2 * 64 * 4;
+  // 16-bit elements per row of the Q, K and V tiles in shared memory: consecutive rows 16 bytes apart
+  // modulo 128, so the eight row addresses of an ldmatrix fall in distinct banks.
+  static constexpr int KSTRIDE = D + 8;
+  static constexpr int PSTRIDE = kChunk + 8;  // the same for P
+  static constexpr uint32_t OFF_Q = 0;                                          // fp32 [16][D]
+  static constexpr uint32_t OFF_QH = OFF_Q + kDecodeMaxRows * D * 4;            // 16-bit [16][KSTRIDE]
+  static constexpr uint32_t OFF_K = OFF_QH + kDecodeMaxRows * KSTRIDE * 2;      // 16-bit [64][KSTRIDE]
+  static constexpr uint32_t OFF_V = OFF_K + kChunk * KSTRIDE * 2;               // 16-bit [64][KSTRIDE]
+  static constexpr uint32_t OFF_S = OFF_V + kChunk * KSTRIDE * 2;               // fp32 [16][64 keys]
+  static constexpr uint32_t OFF_P = OFF_S + kDecodeMaxRows * kChunk * 4;        // 16-bit [16][PSTRIDE]
+  static constexpr uint32_t OFF_ROW = OFF_P + kDecodeMaxRows * PSTRIDE * 2;     // fp32 [16] m, l, alpha
+  static constexpr uint32_t OFF_FREQ = OFF_ROW + 3 * kDecodeMaxRows * 4;        // u32 F_k lo[64], hi[64]
+  static constexpr uint32_t OFF_STEP = OFF_FREQ + 2 * 64 * 4;                   // RopeCS8 [8]: 64 positions
+  static constexpr uint32_t SMEM = OFF_STEP + 8 * sizeof(RopeCS8);
+  static_assert(OFF_QH % 16 == 0 && OFF_K % 16 == 0 && OFF_V % 16 == 0 && OFF_P % 16 == 0 && OFF_STEP % 16 == 0,
+                "ldmatrix rows and 16-byte stores need 16-byte aligned regions");
 };
 
 // Offsets, inside a head vector, of the 8 rotation pairs of frequency group fg (frequencies
@@ -61,22 +74,76 @@ __device__ __forceinline__ void pair_index(int fg, int t, int r, bool interleave
   }
 }
 
+// Warp-level tensor-core products for the (<= 16)-row tiles: ldmatrix fragments and the
+// m16n8k16 MMA (fp32 accumulators).  tcgen05's smallest M (64) would leave three quarters of
+// every product empty here.
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr)
+               : "memory");
+}
+
+// c += a b: a the 16x16 row-major fragment, (b0, b1) the 16x8 column-major fragment.
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   using C = DecCfg<D>;
+  constexpr int KS = C::KSTRIDE;
+  constexpr int NT = D / 64;  // 8-column output tiles per warp in P V (8 warps cover d columns)
   extern __shared__ __align__(16) uint8_t smem[];
   float* sQ = reinterpret_cast<float*>(smem + C::OFF_Q);
+  T* sQh = reinterpret_cast<T*>(smem + C::OFF_QH);
   T* sK = reinterpret_cast<T*>(smem + C::OFF_K);
   T* sV = reinterpret_cast<T*>(smem + C::OFF_V);
   float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
+  T* sP = reinterpret_cast<T*>(smem + C::OFF_P);
   float* sM = reinterpret_cast<float*>(smem + C::OFF_ROW);
   float* sL = sM + kDecodeMaxRows;
   float* sA = sL + kDecodeMaxRows;
   uint32_t* sF = reinterpret_cast<uint32_t*>(smem + C::OFF_FREQ);  // lo[64] then hi[64]
+  RopeCS8* sStep = reinterpret_cast<RopeCS8*>(smem + C::OFF_STEP);  // per frequency group
 
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int g8 = lane / 4, t4 = lane % 4;  // MMA fragment row and column-pair of this lane
+  // the combine kernel may launch now; it waits for this grid's completion before reading
+  ptx::grid_dep_launch_dependents();
   const int g = p.Hq / p.Hkv;
   const int rows = g * p.N;  // row = local head * N + query index
   const int r = 2 * p.rot_chunks * 8;  // rotary dimension
@@ -84,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
   const int key0 = split * p.keys_per_split;
   const int key_end = min(p.Nk, key0 + p.keys_per_split);
 
-  // ---- query rows, rotated (exact cos/sin per row), scaled into fp32 shared memory ----------
+  // ---- query rows into fp32 shared memory; row state; P's padding rows stay zero ----------------
   for (int idx = tid; idx < rows * (D / 8); idx += kThreads) {
     const int row = idx / (D / 8), c8 = idx % (D / 8);
     const int hl = row / p.N, i = row % p.N;
@@ -102,11 +169,14 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
   if (tid < kDecodeMaxRows) {
     sM[tid] = -INFINITY;
     sL[tid] = 0.f;
+    sA[tid] = 0.f;
   }
+  for (int idx = tid; idx < kDecodeMaxRows * C::PSTRIDE / 2; idx += kThreads) reinterpret_cast<uint32_t*>(sP)[idx] = 0u;
   // F_k in shared memory: per-lane frequency indices would serialise constant-bank loads.
   if (tid < 64) sF[tid] = p.freqs.lo[tid];
   else if (tid < 128) sF[tid] = p.freqs.hi[tid - 64];
   __syncthreads();
+  // ---- rotate the query rows (exact cos/sin per row), rounded to the input type once --------------
   for (int idx = tid; idx < rows * p.rot_chunks; idx += kThreads) {
     const int row = idx / p.rot_chunks, fg = idx % p.rot_chunks;
     const int i = row % p.N;
@@ -120,21 +190,27 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
       const float x = sQ[row * D + ia], y = sQ[row * D + ib];
       float xr, yr;
       rope_pair(x, y, c, s, xr, yr);
-      // rotated query rounded to the input type once, as in the other paths
       float2 rr;
       Pack<BF16>::unpack(Pack<BF16>::pack(xr, yr), rr.x, rr.y);
       sQ[row * D + ia] = rr.x;
       sQ[row * D + ib] = rr.y;
     }
   }
-  // Rows past the rotary dimension and unrotated entries were already exact copies.
+  if (tid < p.rot_chunks) rope_cs8_exact((uint32_t)kChunk, sF, sF + 64, 8 * tid, sStep[tid]);
+  __syncthreads();
+  // 16-bit copy for the MMA (exact: every entry is a value of the input type); rows >= rows zero.
+  for (int idx = tid; idx < kDecodeMaxRows * (D / 2); idx += kThreads) {
+    const int row = idx / (D / 2), e = 2 * (idx % (D / 2));
+    const uint32_t w = row < rows ? Pack<BF16>::pack(sQ[row * D + e], sQ[row * D + e + 1]) : 0u;
+    *reinterpret_cast<uint32_t*>(sQh + row * KS + e) = w;
+  }
+  // (read by every warp as A fragments in each chunk's score product: sQh is stable from here on)
 
-  // O accumulators: thread owns items (row, column pair) it = tid + kThreads * n.
-  constexpr int kMaxItems = kDecodeMaxRows * (D / 2) / kThreads;  // 4 (d = 128) or 2 (d = 64)
-  float oacc[kMaxItems][2];
+  // O accumulators of this warp: rows g8 and g8 + 8, columns n0 + 8 nt + 2 t4 (+1).
+  const int n0 = warp * 8 * NT;
+  float o[NT][4];
 #pragma unroll
-  for (int n = 0; n < kMaxItems; ++n) oacc[n][0] = oacc[n][1] = 0.f;
-  const int n_items = rows * (D / 2);
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
   // K and V rows of a chunk: LPT 16-byte pieces per thread, all loads issued before any is used;
   // the next chunk's are in flight while the current one is computed on.
@@ -154,23 +230,18 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
     }
   };
   if (key0 < key_end) load_chunk(key0);
-  // cos/sin of the thread's key-rotation items (see below) and their advance by 64 positions.
+  // cos/sin of the thread's key-rotation items (see below); their advance by 64 positions is shared
+  // per frequency group (sStep).
   constexpr int KIT = (kChunk * (D / 16) + kThreads - 1) / kThreads;  // 2 (d = 128) or 1 (d = 64)
-  RopeCS8 kcs[KIT], kstep[KIT];
-#pragma unroll
-  for (int n = 0; n < KIT; ++n) {
-    const int idx = tid + kThreads * n;
-    const int fg = p.rot_chunks > 0 ? idx % p.rot_chunks : 0;
-    rope_cs8_exact((uint32_t)kChunk, sF, sF + 64, 8 * fg, kstep[n]);
-  }
+  RopeCS8 kcs[KIT];
 
   for (int kc = key0; kc < key_end; kc += kChunk) {
-    __syncthreads();  // previous chunk's K, V, S no longer read
+    __syncthreads();  // previous chunk's K, V, S and P no longer read
 #pragma unroll
     for (int n = 0; n < LPT; ++n) {
       const int idx = tid + kThreads * n, kr = idx / (D / 8), c8 = idx % (D / 8);
-      *reinterpret_cast<uint4*>(sK + kr * C::KSTRIDE + 8 * c8) = kpre[n];
-      *reinterpret_cast<uint4*>(sV + kr * D + 8 * c8) = vpre[n];
+      *reinterpret_cast<uint4*>(sK + kr * KS + 8 * c8) = kpre[n];
+      *reinterpret_cast<uint4*>(sV + kr * KS + 8 * c8) = vpre[n];
     }
     if (kc + kChunk < key_end) load_chunk(kc + kChunk);
     __syncthreads();
@@ -190,7 +261,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
         rope_cs8_exact((uint32_t)j, sF, sF + 64, 8 * fg, kcs[n]);
       }
       if (j < key_end) {
-        T* row = sK + kr * C::KSTRIDE;
+        T* row = sK + kr * KS;
         if (il) {
           uint4* a = reinterpret_cast<uint4*>(row + 16 * fg);
           uint4 x = a[0], y = a[1];
@@ -207,93 +278,101 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
           *ya = y;
         }
       }
-      if (p.kpos == nullptr) rope_cs8_advance(kcs[n], kstep[n]);
+      if (p.kpos == nullptr) rope_cs8_advance(kcs[n], sStep[fg]);
     }
     __syncthreads();
-    // ---- scores (log2 units): thread = key kr, rows rg, rg + 4, ... --------------------------
+    // ---- scores (log2 units) S = Q K^T: warp w takes keys 8w .. 8w + 7 -------------------------
     {
-      const int kr = tid % kChunk, rg = tid / kChunk;
-      const int j = kc + kr;
-      const T* krow = sK + kr * C::KSTRIDE;
-      for (int row = rg; row < rows; row += kThreads / kChunk) {
-        const int i = row % p.N;
-        const float* qrow = sQ + row * D;
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-        for (int e = 0; e < D; e += 8) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(krow + e);
-          const float4 qa = *reinterpret_cast<const float4*>(qrow + e);
-          const float4 qb = *reinterpret_cast<const float4*>(qrow + e + 4);
-          float k0, k1, k2, k3, k4, k5, k6, k7;
-          Pack<BF16>::unpack(kv.x, k0, k1);
-          Pack<BF16>::unpack(kv.y, k2, k3);
-          Pack<BF16>::unpack(kv.z, k4, k5);
-          Pack<BF16>::unpack(kv.w, k6, k7);
-          acc0 = fmaf(qa.x, k0, fmaf(qa.y, k1, fmaf(qa.z, k2, fmaf(qa.w, k3, acc0))));
-          acc1 = fmaf(qb.x, k4, fmaf(qb.y, k5, fmaf(qb.z, k6, fmaf(qb.w, k7, acc1))));
-        }
-        const bool visible = j < key_end && j <= p.q_off + i;
-        sS[row * kChunk + kr] = visible ? (acc0 + acc1) * p.scale_log2 : -INFINITY;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks += 2) {
+        uint32_t qa0[4], qa1[4], bk[4];  // query k-steps ks, ks + 1; the keys' 16x8 fragments of both
+        ldsm_x4(smem_u32(sQh + (lane % 16) * KS + 16 * ks + 8 * (lane / 16)), qa0);
+        ldsm_x4(smem_u32(sQh + (lane % 16) * KS + 16 * (ks + 1) + 8 * (lane / 16)), qa1);
+        ldsm_x4(smem_u32(sK + (8 * warp + lane % 8) * KS + 16 * ks + 8 * (lane / 8)), bk);
+        mma_16816<BF16>(c, qa0, bk[0], bk[1]);
+        mma_16816<BF16>(c, qa1, bk[2], bk[3]);
       }
-    }
-    __syncthreads();
-    // ---- online softmax per row: warp w takes rows w, w + 8, ... -----------------------------
-    {
-      const int warp = tid / 32, lane = tid % 32;
-      for (int row = warp; row < rows; row += kThreads / 32) {
-        const float s0 = sS[row * kChunk + lane], s1 = sS[row * kChunk + lane + 32];
-        float mx = fmaxf(s0, s1);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        const float m_old = sM[row];
-        const float m_new = fmaxf(m_old, mx);
-        // a row that has seen no visible key yet keeps m = -inf, P = 0
-        const float p0 = m_new == -INFINITY ? 0.f : ptx::ex2_approx(s0 - m_new);
-        const float p1 = m_new == -INFINITY ? 0.f : ptx::ex2_approx(s1 - m_new);
-        float sum = p0 + p1;
+      for (int h = 0; h < 2; ++h) {
+        const int row = g8 + 8 * h;
+        if (row < rows) {
+          const int i = row % p.N;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        sS[row * kChunk + lane] = p0;
-        sS[row * kChunk + lane + 32] = p1;
-        __syncwarp();
-        if (lane == 0) {
-          const float alpha = m_old == -INFINITY ? 0.f : ptx::ex2_approx(m_old - m_new);
-          sA[row] = alpha;
-          sL[row] = sL[row] * alpha + sum;
-          sM[row] = m_new;
+          for (int u = 0; u < 2; ++u) {
+            const int kr = 8 * warp + 2 * t4 + u, j = kc + kr;
+            const bool visible = j < key_end && j <= p.q_off + i;
+            sS[row * kChunk + kr] = visible ? c[2 * h + u] * p.scale_log2 : -INFINITY;
+          }
         }
       }
     }
     __syncthreads();
-    // ---- O = O alpha + P V: thread items (row, column pair) --------------------------------
+    // ---- online softmax per row: warp w takes rows w, w + 8 -----------------------------------
+    for (int row = warp; row < rows; row += kThreads / 32) {
+      const float s0 = sS[row * kChunk + lane], s1 = sS[row * kChunk + lane + 32];
+      float mx = fmaxf(s0, s1);
 #pragma unroll
-    for (int n = 0; n < kMaxItems; ++n) {
-      const int it = tid + kThreads * n;
-      if (it >= n_items) break;
-      const int row = it / (D / 2), e = 2 * (it % (D / 2));
-      const float alpha = sA[row];
-      float a0 = oacc[n][0] * alpha, a1 = oacc[n][1] * alpha;
-      const float* prow = sS + row * kChunk;
-#pragma unroll 8
-      for (int kr = 0; kr < kChunk; ++kr) {
-        float v0, v1;
-        Pack<BF16>::unpack(*reinterpret_cast<const uint32_t*>(sV + kr * D + e), v0, v1);
-        const float pw = prow[kr];
-        a0 = fmaf(pw, v0, a0);
-        a1 = fmaf(pw, v1, a1);
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+      const float m_old = sM[row];
+      const float m_new = fmaxf(m_old, mx);
+      // a row that has seen no visible key yet keeps m = -inf, P = 0
+      const float p0 = m_new == -INFINITY ? 0.f : ptx::ex2_approx(s0 - m_new);
+      const float p1 = m_new == -INFINITY ? 0.f : ptx::ex2_approx(s1 - m_new);
+      float sum = p0 + p1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+      // P rounded to the input type for the product, like the tile kernels
+      sP[row * C::PSTRIDE + lane] = static_cast<T>(p0);
+      sP[row * C::PSTRIDE + lane + 32] = static_cast<T>(p1);
+      if (lane == 0) {
+        const float alpha = m_old == -INFINITY ? 0.f : ptx::ex2_approx(m_old - m_new);
+        sA[row] = alpha;
+        sL[row] = sL[row] * alpha + sum;
+        sM[row] = m_new;
       }
-      oacc[n][0] = a0;
-      oacc[n][1] = a1;
+    }
+    __syncthreads();
+    // ---- O = O alpha + P V: warp w takes columns n0 .. n0 + 8 NT - 1 ---------------------------
+    {
+      const float a_lo = sA[g8], a_hi = sA[g8 + 8];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= a_lo;
+        o[nt][1] *= a_lo;
+        o[nt][2] *= a_hi;
+        o[nt][3] *= a_hi;
+      }
+#pragma unroll
+      for (int kk = 0; kk < kChunk / 16; ++kk) {
+        uint32_t pa[4];
+        ldsm_x4(smem_u32(sP + (lane % 16) * C::PSTRIDE + 16 * kk + 8 * (lane / 16)), pa);
+        const int mi = lane / 8;
+        if constexpr (NT == 2) {
+          uint32_t bv[4];  // keys 16 kk .. +15 of columns n0 .. n0 + 7 and n0 + 8 .. n0 + 15
+          ldsm_x4_trans(smem_u32(sV + (16 * kk + lane % 8 + 8 * (mi % 2)) * KS + n0 + 8 * (mi / 2)), bv);
+          mma_16816<BF16>(o[0], pa, bv[0], bv[1]);
+          mma_16816<BF16>(o[1], pa, bv[2], bv[3]);
+        } else {
+          uint32_t bv[2];
+          ldsm_x2_trans(smem_u32(sV + (16 * kk + lane % 8 + 8 * (mi % 2)) * KS + n0), bv);
+          mma_16816<BF16>(o[0], pa, bv[0], bv[1]);
+        }
+      }
     }
   }
   // ---- partials of this split ------------------------------------------------------------------
   const size_t base = (((size_t)b * p.Hkv + hk) * p.n_splits + split) * kDecodeMaxRows;
 #pragma unroll
-  for (int n = 0; n < kMaxItems; ++n) {
-    const int it = tid + kThreads * n;
-    if (it >= n_items) break;
-    const int row = it / (D / 2), e = 2 * (it % (D / 2));
-    *reinterpret_cast<float2*>(p.part_o + (base + row) * D + e) = make_float2(oacc[n][0], oacc[n][1]);
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = g8 + 8 * h;
+      if (row < rows) {
+        const int col = n0 + 8 * nt + 2 * t4;
+        *reinterpret_cast<float2*>(p.part_o + (base + row) * D + col) = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+      }
+    }
   }
   __syncthreads();
   if (tid < rows) {
@@ -303,7 +382,9 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const __grid_cons
 }
 
 // One warp per (batch, KV head, row): m = max_s m_s, l = sum_s l_s 2^(m_s - m),
-// out = sum_s O_s 2^(m_s - m) / l, lse = ln 2 (m + log2 l).
+// out = sum_s O_s 2^(m_s - m) / l, lse = ln 2 (m + log2 l).  The lanes read the splits' (m, l)
+// pairs in parallel and pass each split's weight to the others by shuffle, so the O loads of
+// consecutive splits are independent and overlap.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
@@ -316,23 +397,47 @@ __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const __grid_c
   const int b = (int)(w / ((long long)rows * p.Hkv));
   const int hl = row / p.N, i = row % p.N, h = hk * g + hl;
   const size_t base = ((size_t)b * p.Hkv + hk) * p.n_splits * kDecodeMaxRows + row;
+  const int S = p.n_splits;
+  ptx::grid_dep_wait();  // the partials of every split are complete and visible
   float m = -INFINITY;
-  for (int s = 0; s < p.n_splits; ++s) m = fmaxf(m, p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2]);
+  for (int s = lane; s < S; s += 32) m = fmaxf(m, p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
   constexpr int PER = D / 32;  // columns per lane
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float l = 0.f;
-  for (int s = 0; s < p.n_splits; ++s) {
-    const size_t slot = base + (size_t)s * kDecodeMaxRows;
-    const float ms = p.part_ml[slot * 2];
-    if (ms == -INFINITY) continue;  // no visible key of this row in split s
-    const float wgt = ptx::ex2_approx(ms - m);
-    l = fmaf(p.part_ml[slot * 2 + 1], wgt, l);
-    const float* o = p.part_o + slot * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = fmaf(o[e], wgt, acc[e]);
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    float wgt = 0.f;  // 0 for a split with no visible key of this row (its O is 0 too)
+    if (s0 + lane < S) {
+      const size_t slot = base + (size_t)(s0 + lane) * kDecodeMaxRows;
+      const float ms = p.part_ml[slot * 2];
+      if (ms != -INFINITY) {
+        wgt = ptx::ex2_approx(ms - m);
+        l = fmaf(p.part_ml[slot * 2 + 1], wgt, l);
+      }
+    }
+    const int cnt = min(32, S - s0);
+#pragma unroll 4
+    for (int u = 0; u < cnt; ++u) {
+      const float wu = __shfl_sync(0xFFFFFFFFu, wgt, u);
+      const float* o = p.part_o + (base + (size_t)(s0 + u) * kDecodeMaxRows) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(o);
+        acc[0] = fmaf(v.x, wu, acc[0]);
+        acc[1] = fmaf(v.y, wu, acc[1]);
+        acc[2] = fmaf(v.z, wu, acc[2]);
+        acc[3] = fmaf(v.w, wu, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(o);
+        acc[0] = fmaf(v.x, wu, acc[0]);
+        acc[1] = fmaf(v.y, wu, acc[1]);
+      }
+    }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
   const float inv = 1.f / l;
   T* dst = reinterpret_cast<T*>(p.out) + (((size_t)b * p.N + i) * p.Hq + h) * D + lane * PER;
 #pragma unroll
@@ -363,7 +468,19 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long warps = (long long)p.B * p.Hkv * (p.Hq / p.Hkv) * p.N;
   const long long blocks = (warps * 32 + 255) / 256;
-  attn_decode_combine_kernel<D, BF16><<<dim3((unsigned)blocks), dim3(256), 0, stream>>>(p);
+  // Programmatic dependent launch: the combine grid's launch overlaps the decode grid's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel<D, BF16>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -114,29 +114,38 @@ attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, i
 size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N * (size_t)H * (size_t)d * 2u; }
 
 // Few queries per KV head (decode, speculative decode): the split-KV decode kernels serve FUSED and
-// AUTO calls with at most 16 query rows (rows = (Hq / Hkv) N) per KV head, B Hkv <= 32 KV heads in
-// the batch and B Hkv rows <= 128.  Their cost grows with B Hkv (every KV head's keys are rotated
-// and dotted on the CUDA cores), the tile kernels' hardly does until their units fill the SMs.
-// Measured on GB300 (d = 128, bf16, Nk = 4096 and 32768): with 4 rows the decode kernels win up
-// to B Hkv = 32 (65 vs 72 us at 4096 keys) and lose at 64 (126 vs 83 us); with 16 rows they win at
-// B Hkv = 8 (54 vs 64 us) and lose at 16 (76 vs 67 us).
-constexpr int kDecodeMaxKvHeads = 32;
-constexpr int kDecodeMaxKvHeadRows = 128;
-
+// AUTO calls with at most 16 query rows (rows = (Hq / Hkv) N) per KV head, one MMA tile of rows.
+// Measured on GB300 (d = 128, bf16, Llama heads 32/8): faster than the tile kernels at every
+// batch tried, from B = 1 (26 vs 62 us over 4096 keys, 68 vs 386 us over 32768) to B = 64 (405 vs
+// 488 us), and with 16 rows up to B Hkv = 128 (142 vs 150 us).
 bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
   if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_AUTO) return false;
-  const long long rows = (long long)(Hq / Hkv) * N, heads = (long long)B * Hkv;
-  return rows <= kDecodeMaxRows && heads <= kDecodeMaxKvHeads && heads * rows <= kDecodeMaxKvHeadRows;
+  const long long rows = (long long)(Hq / Hkv) * N;
+  return rows <= kDecodeMaxRows && B <= 65535 && Hkv <= 65535;  // grid z and y
 }
 
-// Splits of the keys: about two CTAs per SM over 152 SMs, in 64-key multiples (three per SM measured
-// slower over 32K keys: more partials to merge).
+// Splits of the keys, in 64-key chunks: the number of slices that minimises (waves of CTAs) x (chunks
+// per slice + a CTA's fixed work, about two chunks' time measured) with two CTAs resident per SM on
+// 152 SMs (304 slots), fewest slices among equals (each slice adds a partial to merge).  A slice
+// count rounded up past a whole wave would double the time.
 void decode_plan(int B, int Hkv, int Nk, int* keys_per_split, int* n_splits) {
+  constexpr long long kSlots = 304, kFixedChunks = 2;
   const int chunks = (Nk + 63) / 64;
-  const int want = (304 + B * Hkv - 1) / (B * Hkv);
-  const int splits = want < 1 ? 1 : (want > chunks ? chunks : want);
-  const int per = (chunks + splits - 1) / splits;  // chunks per split
-  *keys_per_split = 64 * per;
+  const long long heads = (long long)B * Hkv;
+  long long best_cost = -1;
+  int best_per = chunks;
+  const int max_splits = chunks < 1024 ? chunks : 1024;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int per = (chunks + s - 1) / s;
+    const long long n = (chunks + per - 1) / per;  // slices actually needed
+    const long long waves = (heads * n + kSlots - 1) / kSlots;
+    const long long cost = waves * (per + kFixedChunks);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_per = per;
+    }
+  }
+  *keys_per_split = 64 * best_per;
   *n_splits = (Nk + *keys_per_split - 1) / *keys_per_split;
 }
 

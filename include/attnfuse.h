@@ -66,8 +66,13 @@ typedef enum {
  *                              query tile on chip (each is read once): rotation cost paid once per
  *                              element for both tensors.
  *   mode = ATTNFUSE_AUTO:      whichever mode attnfuse_select_mode returns for the shape.
+ * FUSED and AUTO calls with few queries per KV head -- (Hq / Hkv) N <= 16 query rows (a decode
+ * step, a speculative-decode step) -- run split-KV decode kernels instead: each CTA rotates one
+ * slice of one KV head's keys and the head's query rows on chip and runs the two products as
+ * 16-row tensor-core tiles; a second kernel merges the slices' partial softmax sums.
  * All modes compute the function in the header comment.  `lse` may be NULL (not written).
- * `workspace` must hold attnfuse_workspace_bytes(...) bytes (0 for FUSED); if it is NULL while
+ * `workspace` must hold attnfuse_workspace_bytes(...) bytes (0 for FUSED outside the decode
+ * shapes); if it is NULL while
  * bytes are needed, the call allocates with cudaMallocAsync and frees with cudaFreeAsync on
  * `stream`.  Query rows never read keys beyond their own position; rows are independent.
  */
@@ -78,7 +83,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
 
 /* Bytes of workspace attnfuse_rope_causal_fwd needs: 0 for FUSED; for PREROTATE the rotated copies
  * of Q and K (each rounded up to 256 bytes); for SPLIT the rotated K; for AUTO those of the selected
- * mode.  Returns 0 for invalid arguments. */
+ * mode; for FUSED and AUTO at the decode shapes the decode kernels' partial results (per key
+ * slice and KV head, 16 query-row slots of d + 2 floats).  Returns 0 for invalid arguments. */
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype);
 
 /*

@@ -58,7 +58,6 @@ def sample_rows(N: int, n_random: int, seed: int, tile: int = 128):
 
 
 def decode_path(B: int, Hq: int, Hkv: int, N: int) -> bool:
-    """Whether fused and auto calls run the split-KV decode kernels: at most 16 query rows per KV
-    head, at most 32 KV heads in the batch and at most 128 (KV head, row) pairs."""
-    rows, heads = (Hq // Hkv) * N, B * Hkv
-    return rows <= 16 and heads <= 32 and heads * rows <= 128
+    """Whether fused and auto calls run the split-KV decode kernels: at most 16 query rows
+    ((Hq / Hkv) N) per KV head."""
+    return (Hq // Hkv) * N <= 16

@@ -1,7 +1,6 @@
 """Few queries against many keys (decode, speculative decode): fused and auto calls with at most 16
-query rows ((Hq / Hkv) N) per KV head and few KV heads in the batch run the split-KV decode kernels;
-every element is compared with the oracle, and with the tile kernels (pre-rotate mode) on the same
-inputs."""
+query rows ((Hq / Hkv) N) per KV head run the split-KV decode kernels; every element is compared with
+the oracle, and with the tile kernels (pre-rotate mode) on the same inputs."""
 import pytest
 import torch
 
@@ -21,8 +20,8 @@ def _lib():
 CASES = [
     # B, N, Nk, Hq, Hkv, d, dtype, rotary_dim, interleaved, positions
     (1, 1, 4096, 32, 8, 128, "bf16", None, False, False),   # one decode step, Llama-3-8B heads
-    (4, 1, 1000, 32, 8, 128, "fp16", None, False, False),   # ragged split tail, 32 KV heads (the maximum)
-    (16, 1, 300, 8, 4, 128, "bf16", None, False, False),    # 64 KV heads: the tile kernels
+    (4, 1, 1000, 32, 8, 128, "fp16", None, False, False),   # ragged split tail, 32 KV heads
+    (16, 1, 300, 8, 4, 128, "bf16", None, False, False),    # 64 KV heads, one 64-key chunk per slice
     (2, 4, 777, 8, 2, 64, "bf16", None, False, False),      # speculative decode, 16 rows (the maximum)
     (1, 16, 2048, 16, 4, 128, "bf16", None, False, False),  # 64 rows per KV head: the tile kernels
     (1, 8, 300, 8, 8, 64, "fp16", None, False, False),      # MHA
