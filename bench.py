@@ -436,6 +436,20 @@ def bwd_fn(w, q, k, v, out, lse, stream):
                                            stream=stream)
 
 
+def decode_fn(w, mode, stream):
+    """One decode step of the workload's heads: B queries (N = 1), each against w.N cached keys,
+    through attnfuse_rope_causal_fwd_ex in `mode` ("fused" runs the split-KV decode kernels)."""
+    import torch
+    from attention_rope_causal_gb300 import binding, inputs
+    q, k, v = (t.cuda() for t in inputs.make_kv_inputs(w.B, 1, w.N, w.Hq, w.Hkv, w.d, w.dtype, seed=w.seed + 7))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(256, binding.workspace_bytes(w.B, w.Hq, w.Hkv, 1, w.d, mode, q.dtype, kv_len=w.N)),
+                     dtype=torch.uint8, device="cuda")
+    return lambda: binding.rope_causal_fwd(q, k, v, w.rope_base, mode=mode, out=out, lse=lse, workspace=ws,
+                                           stream=stream)
+
+
 def run_only(args):
     """Run one path alone (for profilers): W + K steps of `fused`, `prerotate` or `rope` with L2 flushes."""
     import torch
@@ -452,6 +466,8 @@ def run_only(args):
     elif args.only == "backward":
         fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)()
         f = bwd_fn(w, q, k, v, out, lse, stream)
+    elif args.only == "decode":
+        f = decode_fn(w, "fused", stream)
     else:
         f = fwd_fn(w, q, k, v, out, lse, ws[args.only], args.only, stream)
     ms = time_steps(f, args.warmup + args.steps, flush, stream)[args.warmup:]
@@ -514,6 +530,13 @@ def run_ours(args):
     bwd = bwd_fn(w, q, k, v, out, lse, stream)
     time_steps(bwd, args.warmup, flush, stream)
     bwd_ms = statistics.median(time_steps(bwd, max(20, args.steps // 10), flush, stream))
+    # one decode step against w.N cached keys: the decode kernels (fused mode) and the tile kernels
+    dec_ms = {}
+    for mode in ("fused", "split"):
+        dec = decode_fn(w, mode, stream)
+        time_steps(dec, args.warmup, flush, stream)
+        dec_ms[mode] = statistics.median(time_steps(dec, max(20, args.steps // 10), flush, stream))
+    kv_bytes = 2 * k.numel() * k.element_size()
     if binding.device_status() != 0:
         raise RuntimeError(f"device status: {binding.last_error()}")
 
@@ -548,6 +571,11 @@ def run_ours(args):
                      "flops_note": "2.5 x the causal forward FLOPs (dS^T Q, dS K, P^T dO, dO V^T and the "
                                    "recomputed Q K^T); the kernels compute Q K^T and dO V^T twice",
                      "kernels": "rope_apply (q', k') + bwd_prep (D) + bwd_dkdv + bwd_dq"},
+        "decode": {"workload": f"{w.B} x 1 query per head against {w.N} cached keys, Hq/Hkv = {w.Hq}/{w.Hkv}, d = {w.d}",
+                   "ms": dec_ms["fused"], "tile_kernels_ms": dec_ms["split"],
+                   "kv_gbs": kv_bytes / (dec_ms["fused"] / 1e3) / 1e9,
+                   "kv_frac_of_hbm": kv_bytes / (dec_ms["fused"] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                   "kernels": "attn_decode_kernel + attn_decode_combine_kernel (split-KV, 16-row MMA tiles)"},
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
@@ -566,7 +594,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=inputs.LLAMA.name, choices=sorted(inputs.NAMED))
     ap.add_argument("--sweep", action="store_true", help="run the crossover sweep instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("fused", "prerotate", "split", "rope", "backward"),
+    ap.add_argument("--only", choices=("fused", "prerotate", "split", "rope", "backward", "decode"),
                     help="time one path alone (for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
