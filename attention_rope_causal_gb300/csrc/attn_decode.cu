@@ -9,7 +9,7 @@
 // ("AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraphs 1-2: RoPE on Q
 // and K before the product, causal mask, softmax).
 //
-// attn_decode_kernel: one CTA per (split of keys_per_split keys, KV head, batch), 256 threads, two
+// attn_decode_kernel: one CTA per (KV head, split of keys_per_split keys, batch), 256 threads, two
 // CTAs per SM.  The CTA rotates its query rows once (exact cos/sin per row) into fp32 shared
 // memory, then walks its keys 64 at a time: the next chunk's K and V rows are loaded into registers
 // (16-byte loads) while the current chunk is processed; K is rotated in shared memory by cos/sin
@@ -51,11 +51,13 @@ struct DecCfg {
   static constexpr uint32_t OFF_QH = OFF_Q + kDecodeMaxRows * D * 4;            // 16-bit [16][KSTRIDE]
   static constexpr uint32_t OFF_K = OFF_QH + kDecodeMaxRows * KSTRIDE * 2;      // 16-bit [64][KSTRIDE]
   static constexpr uint32_t OFF_V = OFF_K + kChunk * KSTRIDE * 2;               // 16-bit [64][KSTRIDE]
-  static constexpr uint32_t OFF_S = OFF_V + kChunk * KSTRIDE * 2;               // fp32 [16][64 keys]
-  static constexpr uint32_t OFF_P = OFF_S + kDecodeMaxRows * kChunk * 4;        // 16-bit [16][PSTRIDE]
+  static constexpr int SSTRIDE = kChunk + 8;  // fp32 scores per row: the eight rows of an MMA
+                                              // fragment's store fall in distinct banks
+  static constexpr uint32_t OFF_S = OFF_V + kChunk * KSTRIDE * 2;               // fp32 [16][SSTRIDE]
+  static constexpr uint32_t OFF_P = OFF_S + kDecodeMaxRows * SSTRIDE * 4;       // 16-bit [16][PSTRIDE]
   static constexpr uint32_t OFF_ROW = OFF_P + kDecodeMaxRows * PSTRIDE * 2;     // fp32 [16] m, l, alpha
   static constexpr uint32_t OFF_FREQ = OFF_ROW + 3 * kDecodeMaxRows * 4;        // u32 F_k lo[64], hi[64]
-  static constexpr uint32_t OFF_STEP = OFF_FREQ + 2 * 64 * 4;                   // RopeCS8 [8]: 64 positions
+  static constexpr uint32_t OFF_STEP = OFF_FREQ + 2 * 64 * 4;                   // u64 c[4][8], s[4][8]
   static constexpr uint32_t SMEM = OFF_STEP + 8 * sizeof(RopeCS8);
   static_assert(OFF_QH % 16 == 0 && OFF_K % 16 == 0 && OFF_V % 16 == 0 && OFF_P % 16 == 0 && OFF_STEP % 16 == 0,
                 "ldmatrix rows and 16-byte stores need 16-byte aligned regions");
@@ -137,9 +139,13 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_c
   float* sL = sM + kDecodeMaxRows;
   float* sA = sL + kDecodeMaxRows;
   uint32_t* sF = reinterpret_cast<uint32_t*>(smem + C::OFF_FREQ);  // lo[64] then hi[64]
-  RopeCS8* sStep = reinterpret_cast<RopeCS8*>(smem + C::OFF_STEP);  // per frequency group
+  // cos/sin of 64 positions per frequency group, field-major ([j][group]) so that the lanes of a
+  // warp, which hold consecutive groups, read consecutive words
+  uint64_t* sStepC = reinterpret_cast<uint64_t*>(smem + C::OFF_STEP);
+  uint64_t* sStepS = sStepC + 4 * 8;
 
-  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  // KV head fastest: CTAs launched together read the same key rows of all heads (whole DRAM pages)
+  const int hk = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g8 = lane / 4, t4 = lane % 4;  // MMA fragment row and column-pair of this lane
   // the combine kernel may launch now; it waits for this grid's completion before reading
@@ -150,6 +156,32 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_c
   const bool il = p.interleaved != 0;
   const int key0 = split * p.keys_per_split;
   const int key_end = min(p.Nk, key0 + p.keys_per_split);
+
+  // K and V rows of a chunk: warp w loads rows 8w .. 8w + 7 (LPT 16-byte pieces per lane, 16 or 8
+  // lanes per row), all loads issued before any is used; the next chunk's are in flight while the
+  // current one is computed on, the first chunk's while the query rows are prepared.
+  constexpr int LPT = D / 32;  // 4 (d = 128) or 2 (d = 64)
+  uint4 kpre[LPT], vpre[LPT];
+  auto piece = [&](int n, int& kr, int& c8) {
+    const int local = 32 * n + lane;
+    kr = 8 * warp + local / (D / 8);
+    c8 = local % (D / 8);
+  };
+  auto load_chunk = [&](int kc) {
+#pragma unroll
+    for (int n = 0; n < LPT; ++n) {
+      int kr, c8;
+      piece(n, kr, c8);
+      const int j = kc + kr;
+      kpre[n] = vpre[n] = make_uint4(0, 0, 0, 0);  // zero past the split or the sequence
+      if (j < key_end) {
+        const size_t off = (((size_t)b * p.Nk + j) * p.Hkv + hk) * D + 8 * c8;
+        kpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k) + off));
+        vpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v) + off));
+      }
+    }
+  };
+  if (key0 < key_end) load_chunk(key0);
 
   // ---- query rows into fp32 shared memory; row state; P's padding rows stay zero ----------------
   for (int idx = tid; idx < rows * (D / 8); idx += kThreads) {
@@ -196,7 +228,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_c
       sQ[row * D + ib] = rr.y;
     }
   }
-  if (tid < p.rot_chunks) rope_cs8_exact((uint32_t)kChunk, sF, sF + 64, 8 * tid, sStep[tid]);
+  if (tid < p.rot_chunks) {
+    RopeCS8 st;
+    rope_cs8_exact((uint32_t)kChunk, sF, sF + 64, 8 * tid, st);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      sStepC[8 * j + tid] = st.c[j];
+      sStepS[8 * j + tid] = st.s[j];
+    }
+  }
   __syncthreads();
   // 16-bit copy for the MMA (exact: every entry is a value of the input type); rows >= rows zero.
   for (int idx = tid; idx < kDecodeMaxRows * (D / 2); idx += kThreads) {
@@ -212,48 +252,33 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_c
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-  // K and V rows of a chunk: LPT 16-byte pieces per thread, all loads issued before any is used;
-  // the next chunk's are in flight while the current one is computed on.
-  constexpr int LPT = kChunk * (D / 8) / kThreads;  // 4 (d = 128) or 2 (d = 64)
-  uint4 kpre[LPT], vpre[LPT];
-  auto load_chunk = [&](int kc) {
-#pragma unroll
-    for (int n = 0; n < LPT; ++n) {
-      const int idx = tid + kThreads * n, kr = idx / (D / 8), c8 = idx % (D / 8);
-      const int j = kc + kr;
-      kpre[n] = vpre[n] = make_uint4(0, 0, 0, 0);  // zero past the split or the sequence
-      if (j < key_end) {
-        const size_t off = (((size_t)b * p.Nk + j) * p.Hkv + hk) * D + 8 * c8;
-        kpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k) + off));
-        vpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v) + off));
-      }
-    }
-  };
-  if (key0 < key_end) load_chunk(key0);
   // cos/sin of the thread's key-rotation items (see below); their advance by 64 positions is shared
-  // per frequency group (sStep).
-  constexpr int KIT = (kChunk * (D / 16) + kThreads - 1) / kThreads;  // 2 (d = 128) or 1 (d = 64)
+  // per frequency group (sStepC, sStepS).
+  constexpr int KIT = D / 64;  // rotation items per lane: 8 keys x at most D/16 groups per warp
   RopeCS8 kcs[KIT];
 
   for (int kc = key0; kc < key_end; kc += kChunk) {
-    __syncthreads();  // previous chunk's K, V, S and P no longer read
+    __syncthreads();  // every warp is done with the previous chunk's V and P
+    // Warp w owns K rows 8w .. 8w + 7 from the store through the rotation to the score product, so
+    // only V (read by every warp) needs the CTA-wide barriers.
 #pragma unroll
     for (int n = 0; n < LPT; ++n) {
-      const int idx = tid + kThreads * n, kr = idx / (D / 8), c8 = idx % (D / 8);
+      int kr, c8;
+      piece(n, kr, c8);
       *reinterpret_cast<uint4*>(sK + kr * KS + 8 * c8) = kpre[n];
       *reinterpret_cast<uint4*>(sV + kr * KS + 8 * c8) = vpre[n];
     }
     if (kc + kChunk < key_end) load_chunk(kc + kChunk);
-    __syncthreads();
-    // ---- rotate the chunk's keys in place ------------------------------------------------------
-    // Thread item n: key row kr, frequency group fg (8 frequencies, two 16-byte pieces).  Positions
+    __syncwarp();
+    // ---- rotate the warp's keys in place -------------------------------------------------------
+    // Lane item n: key row kr, frequency group fg (8 frequencies, two 16-byte pieces).  Positions
     // j: cos/sin carried from chunk to chunk by the exact rotation of 64 positions, exact again every
     // 16 chunks; explicit positions: exact per key.
 #pragma unroll
     for (int n = 0; n < KIT; ++n) {
-      const int idx = tid + kThreads * n;
-      if (idx >= kChunk * p.rot_chunks) break;
-      const int kr = idx / p.rot_chunks, fg = idx % p.rot_chunks;
+      const int local = 32 * n + lane;
+      if (local >= 8 * p.rot_chunks) break;
+      const int kr = 8 * warp + local / p.rot_chunks, fg = local % p.rot_chunks;
       const int j = kc + kr;
       if (p.kpos != nullptr) {
         if (j < key_end) rope_cs8_exact_signed(p.kpos[(size_t)b * p.Nk + j], sF, sF + 64, 8 * fg, kcs[n]);
@@ -278,9 +303,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_c
           *ya = y;
         }
       }
-      if (p.kpos == nullptr) rope_cs8_advance(kcs[n], sStep[fg]);
+      if (p.kpos == nullptr) {
+        RopeCS8 st;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          st.c[jj] = sStepC[8 * jj + fg];
+          st.s[jj] = sStepS[8 * jj + fg];
+        }
+        rope_cs8_advance(kcs[n], st);
+      }
     }
-    __syncthreads();
+    __syncwarp();
     // ---- scores (log2 units) S = Q K^T: warp w takes keys 8w .. 8w + 7 -------------------------
     {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -298,19 +331,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_c
         const int row = g8 + 8 * h;
         if (row < rows) {
           const int i = row % p.N;
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int kr = 8 * warp + 2 * t4 + u, j = kc + kr;
-            const bool visible = j < key_end && j <= p.q_off + i;
-            sS[row * kChunk + kr] = visible ? c[2 * h + u] * p.scale_log2 : -INFINITY;
-          }
+          const int kr = 8 * warp + 2 * t4, j = kc + kr;
+          const int lim = min(key_end - 1, p.q_off + i);  // last visible key
+          *reinterpret_cast<float2*>(sS + row * C::SSTRIDE + kr) =
+              make_float2(j <= lim ? c[2 * h] * p.scale_log2 : -INFINITY,
+                          j + 1 <= lim ? c[2 * h + 1] * p.scale_log2 : -INFINITY);
         }
       }
     }
     __syncthreads();
     // ---- online softmax per row: warp w takes rows w, w + 8 -----------------------------------
     for (int row = warp; row < rows; row += kThreads / 32) {
-      const float s0 = sS[row * kChunk + lane], s1 = sS[row * kChunk + lane + 32];
+      const float s0 = sS[row * C::SSTRIDE + lane], s1 = sS[row * C::SSTRIDE + lane + 32];
       float mx = fmaxf(s0, s1);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
@@ -462,7 +494,7 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  attn_decode_kernel<D, BF16><<<dim3((unsigned)p.n_splits, (unsigned)p.Hkv, (unsigned)p.B), dim3(kThreads),
+  attn_decode_kernel<D, BF16><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(kThreads),
                                 DecCfg<D>::SMEM, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

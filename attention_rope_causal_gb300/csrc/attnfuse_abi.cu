@@ -121,7 +121,7 @@ size_t tensor_bytes(int B, int N, int H, int d) { return (size_t)B * (size_t)N *
 bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
   if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_AUTO) return false;
   const long long rows = (long long)(Hq / Hkv) * N;
-  return rows <= kDecodeMaxRows && B <= 65535 && Hkv <= 65535;  // grid z and y
+  return rows <= kDecodeMaxRows && B <= 65535 && Hkv <= 65535;  // grid limits
 }
 
 // Splits of the keys, in 64-key chunks: the number of slices that minimises (waves of CTAs) x (chunks
