@@ -22,6 +22,9 @@ CASES = [
     (1, 1, 4096, 32, 8, 128, "bf16", None, False, False),   # one decode step, Llama-3-8B heads
     (4, 1, 1000, 32, 8, 128, "fp16", None, False, False),   # ragged split tail, 32 KV heads
     (16, 1, 300, 8, 4, 128, "bf16", None, False, False),    # 64 KV heads, one 64-key chunk per slice
+    (32, 1, 1024, 16, 4, 128, "bf16", None, False, False),  # 128 KV heads, two slices of 8 chunks
+    (304, 1, 2048, 1, 1, 64, "bf16", None, False, False),   # one slice of 32 chunks: the key cos/sin
+                                                            # walk is recomputed exactly at chunk 16
     (2, 4, 777, 8, 2, 64, "bf16", None, False, False),      # speculative decode, 16 rows (the maximum)
     (1, 16, 2048, 16, 4, 128, "bf16", None, False, False),  # 64 rows per KV head: the tile kernels
     (1, 8, 300, 8, 8, 64, "fp16", None, False, False),      # MHA
