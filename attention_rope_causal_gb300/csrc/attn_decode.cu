@@ -10,7 +10,7 @@
 // and K before the product, causal mask, softmax).
 //
 // attn_decode_kernel: one CTA per (KV head, split of keys_per_split keys, batch), 256 threads, two
-// CTAs per SM.  The CTA rotates its query rows once (exact cos/sin per row) into fp32 shared
+// (d = 128) or three (d = 64) CTAs per SM.  The CTA rotates its query rows once (exact cos/sin per row) into fp32 shared
 // memory, then walks its keys 64 at a time: the next chunk's K and V rows are loaded into registers
 // (16-byte loads) while the current chunk is processed; K is rotated in shared memory by cos/sin
 // carried from chunk to chunk (advanced by the exact rotation of 64 positions, recomputed exactly
@@ -123,7 +123,7 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D)) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   using C = DecCfg<D>;
   constexpr int KS = C::KSTRIDE;

@@ -125,11 +125,12 @@ bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
 }
 
 // Splits of the keys, in 64-key chunks: the number of slices that minimises (waves of CTAs) x (chunks
-// per slice + a CTA's fixed work, about two chunks' time measured) with two CTAs resident per SM on
-// 152 SMs (304 slots), fewest slices among equals (each slice adds a partial to merge).  A slice
-// count rounded up past a whole wave would double the time.
-void decode_plan(int B, int Hkv, int Nk, int* keys_per_split, int* n_splits) {
-  constexpr long long kSlots = 304, kFixedChunks = 2;
+// per slice + a CTA's fixed work, about two chunks' time measured) with decode_ctas_per_sm(d) CTAs
+// resident per SM on 152 SMs, fewest slices among equals (each slice adds a partial to merge).  A
+// slice count rounded up past a whole wave would double the time.
+void decode_plan(int B, int Hkv, int Nk, int d, int* keys_per_split, int* n_splits) {
+  const long long kSlots = 152LL * decode_ctas_per_sm(d);
+  constexpr long long kFixedChunks = 2;
   const int chunks = (Nk + 63) / 64;
   const long long heads = (long long)B * Hkv;
   long long best_cost = -1;
@@ -151,7 +152,7 @@ void decode_plan(int B, int Hkv, int Nk, int* keys_per_split, int* n_splits) {
 
 size_t decode_workspace_bytes(int B, int Hkv, int Nk, int d) {
   int kps = 0, ns = 0;
-  decode_plan(B, Hkv, Nk, &kps, &ns);
+  decode_plan(B, Hkv, Nk, d, &kps, &ns);
   const size_t slots = (size_t)B * Hkv * ns * kDecodeMaxRows;
   return round_up(slots * d * sizeof(float), 256) + round_up(slots * 2 * sizeof(float), 256);
 }
@@ -358,7 +359,7 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
     dp.kpos = o.kpos;
     dp.rot_chunks = o.rdim / 16;
     dp.interleaved = o.interleaved;
-    decode_plan(B, Hkv, Nk, &dp.keys_per_split, &dp.n_splits);
+    decode_plan(B, Hkv, Nk, d, &dp.keys_per_split, &dp.n_splits);
     dp.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
     rope_freqs_host(o.rdim, rope_base, &dp.freqs);
     void* owned = nullptr;

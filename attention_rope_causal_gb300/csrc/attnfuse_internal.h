@@ -71,6 +71,11 @@ cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bo
 
 constexpr int kDecodeMaxRows = 16;  // query rows per KV head: (Hq / Hkv) * N
 
+// Decode CTAs (256 threads) resident per SM: the kernel's register cap and the key-slice planner
+// both follow it.  d = 64 fits three (80 registers, no spills); d = 128 two (three would spill
+// the carried cos/sin).
+constexpr int decode_ctas_per_sm(int d) { return d == 64 ? 3 : 2; }
+
 struct DecodeParams {
   const void* q;          // [B, N, Hq, d]
   const void* k;          // [B, Nk, Hkv, d]
