@@ -222,6 +222,11 @@ def oracle_sample_rows(w, target_s: float, q, k, v):
     return stride
 
 
+def rows_phrase(stride: int) -> str:
+    """'every query row' or 'one query row in <stride>'."""
+    return "every query row" if stride == 1 else f"one query row in {stride}"
+
+
 def run_cpu_baseline(w, target_s=12.0):
     import numpy as np
     import oracle
@@ -234,7 +239,7 @@ def run_cpu_baseline(w, target_s=12.0):
     dt = time.perf_counter() - t
     fl = oracle_rows_flops(w, rows)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.default_threads(), "kind": "oracle",
-            "sample": f"{w.name}: every {stride}th query row ({len(rows)} rows x {w.Hq} heads), fp64 C oracle, "
+            "sample": f"{w.name}: {rows_phrase(stride)} ({len(rows)} rows x {w.Hq} heads), fp64 C oracle, "
                       f"{dt:.1f} s, {fl / 1e9:.1f} GFLOP causal-equivalent"}
 
 
@@ -260,7 +265,7 @@ def run_reference_arm(args):
             fl_total += oracle_rows_flops(w, rows)
             t_total += dt
     value = fl_total / t_total / 1e12
-    sample = (f"{w.name}: each step every {stride}th query row (offset rotating) x {w.Hq} heads, fp64 C oracle "
+    sample = (f"{w.name}: each step {rows_phrase(stride)} (offset rotating) x {w.Hq} heads, fp64 C oracle "
               f"on {oracle.default_threads()} host threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / max(1, args.steps) * 1e3,
