@@ -196,3 +196,18 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
 def test_diag_rejects_bad_timeout(lib):
     assert lib.attnfuse_diag_wait_timeout(0, None) == 1
     assert lib.attnfuse_diag_wait_timeout(2_000_000_000, None) == 1
+
+
+def test_binding_rejects_host_tensors_before_the_library():
+    # The binding marshals device pointers only: host tensors are refused with ValueError (no CPU
+    # path exists to fall back on).
+    import torch
+    q = torch.zeros((1, 8, 2, 64), dtype=torch.bfloat16)
+    kv = torch.zeros((1, 8, 1, 64), dtype=torch.bfloat16)
+    lse = torch.zeros((1, 2, 8), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        binding.rope_causal_fwd(q, kv, kv, 1e4)
+    with pytest.raises(ValueError):
+        binding.rope_apply(q, 1e4)
+    with pytest.raises(ValueError):
+        binding.rope_causal_bwd(q, kv, kv, q, lse, q, 1e4)
