@@ -29,6 +29,8 @@ CASES = [
     (1, 16, 2048, 16, 4, 128, "bf16", None, False, False),  # 64 rows per KV head: the tile kernels
     (1, 8, 300, 8, 8, 64, "fp16", None, False, False),      # MHA
     (1, 1, 1, 4, 1, 128, "bf16", None, False, False),       # a single key
+    (1, 4, 770, 8, 2, 128, "bf16", None, False, False),     # last slice [768, 770): queries 0 and 1
+                                                            # see none of its keys (empty partials)
     (2, 3, 500, 8, 2, 128, "bf16", 64, True, False),        # RoPE variant
     (2, 2, 640, 4, 2, 64, "fp16", None, False, True),       # explicit positions
 ]
