@@ -740,21 +740,18 @@ cudaError_t launch_dependent(K kernel, dim3 grid, dim3 block, uint32_t smem, cud
 template <int TAG, typename K>
 cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const AttnBwdMaps& m, const AttnBwdParams& p,
                               cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static int sm_count[kMaxDevices] = {0};
+  static DeviceOnce once;  // attributes set and SM count kept per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (sm_count[dev] == 0) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = n;
-  }
-  const int grid = units < sm_count[dev] ? units : sm_count[dev];
+  int sms = 0;
+  e = once.get(dev, [&](int* out) -> cudaError_t {
+    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r != cudaSuccess) return r;
+    return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  }, &sms);
+  if (e != cudaSuccess) return e;
+  const int grid = units < sms ? units : sms;
   return launch_dependent(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, m.q, m.k, m.v, m.dout, p);
 }
 

@@ -482,18 +482,16 @@ __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const __grid_c
 
 template <int D, bool BF16>
 cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static int configured[kMaxDevices] = {0};
+  static DeviceOnce once;  // shared-memory attribute set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_decode_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)DecCfg<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  int unused = 0;
+  e = once.get(dev, [](int*) -> cudaError_t {
+    return cudaFuncSetAttribute(attn_decode_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)DecCfg<D>::SMEM);
+  }, &unused);
+  if (e != cudaSuccess) return e;
   attn_decode_kernel<D, BF16><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(kThreads),
                                 DecCfg<D>::SMEM, stream>>>(p);
   e = cudaGetLastError();

@@ -40,7 +40,6 @@
 #include <type_traits>
 
 #include "attnfuse_internal.h"
-#include "exp2_poly.cuh"
 #include "ptx.cuh"
 #include "rope.cuh"
 
@@ -62,10 +61,6 @@ constexpr float kLn2 = 0.6931471805599453f;
 // of P sums past this bound (some score exceeded m by more than ~15 in log2 units, so P could leave
 // the range of the 16-bit operand type) is the tile redone with its own max.
 constexpr float kSumCap = 32768.0f;
-
-// Which 32-column chunks of a score row take their exponentials from the FMA-pipe polynomial
-// (exp2_poly.cuh) instead of the MUFU unit (bit c set = chunk c).
-constexpr uint32_t kPolyChunkMask = 0u;
 
 // Register split after setmaxnreg (control warps / softmax warps / rotation warps).  The total,
 // 128 x (ctrl + rotate) + 256 x softmax, must not exceed the 512 x 128 registers the CTA is launched
@@ -111,15 +106,9 @@ __device__ __forceinline__ float softmax_p(const uint32_t (&sv)[4][32], float sl
     for (int e = 0; e < 16; ++e) {
       const uint64_t x2 =
           ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), SL2, NM);
-      float p0, p1;
-      if ((kPolyChunkMask >> c) & 1u) {
-        exp2_poly_pair(x2, p0, p1);
-      } else {
-        float x0, x1;
-        ptx::f2_unpack(x2, x0, x1);
-        p0 = ptx::ex2_approx(x0);
-        p1 = ptx::ex2_approx(x1);
-      }
+      float x0, x1;
+      ptx::f2_unpack(x2, x0, x1);
+      const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
       part[e & 3] = ptx::f2_add(part[e & 3], ptx::f2_pack(p0, p1));
       pk[16 * c + e] = Pack<BF16>::pack(p0, p1);
     }
@@ -855,34 +844,33 @@ __global__ void diag_wait_timeout_kernel(unsigned long long timeout_ns) {
 template <int D, bool ROTATE, bool BF16, bool VARIANT, bool ROT_K>
 cudaError_t launch_one(const AttnMaps& maps, const AttnParams& p, cudaStream_t stream, const char** why) {
   auto kernel = attn_fwd_kernel<D, ROTATE, BF16, VARIANT, ROT_K>;
-  constexpr int kMaxDevices = 64;
-  static int configured[kMaxDevices] = {0};
-  static int sm_count[kMaxDevices] = {0};
+  static DeviceOnce once;  // per instantiation: attributes set and SM count kept per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::SMEM);
-    if (e != cudaSuccess) return e;
+  bool regs_ok = true;
+  int sms = 0;
+  e = once.get(dev, [&](int* out) -> cudaError_t {
+    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<D>::SMEM);
+    if (r != cudaSuccess) return r;
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, kernel);
-    if (e != cudaSuccess) return e;
+    r = cudaFuncGetAttributes(&attr, kernel);
+    if (r != cudaSuccess) return r;
     // The warp-role register split (setmaxnreg) hands out exactly 512 x 128 registers: launching
     // with fewer per thread would leave the softmax warps waiting for registers forever.
     if (attr.numRegs != 128) {
-      if (why) *why = "attention kernel was not compiled with 128 registers per thread (setmaxnreg split)";
+      regs_ok = false;
       return cudaErrorInvalidConfiguration;
     }
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = sms;
-    configured[dev] = 1;
+    return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  }, &sms);
+  if (e != cudaSuccess) {
+    if (!regs_ok && why) *why = "attention kernel was not compiled with 128 registers per thread (setmaxnreg split)";
+    return e;
   }
   // Persistent: one CTA per SM (shared memory and registers admit only one), each walking its share
   // of the work units.
-  const int grid = p.total_units < sm_count[dev] ? p.total_units : sm_count[dev];
+  const int grid = p.total_units < sms ? p.total_units : sms;
   // After this library's pre-rotation pass the kernel is launched as a programmatic dependent: its
   // prologue (barriers, tensor memory, descriptor prefetch) overlaps the end of the pass, and the
   // TMA producer waits for the pass before its first load.

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -15,9 +16,11 @@
 
 namespace attnfuse {
 
+namespace {
+
 // F_k = round(theta_k / (2 pi) * 2^64): frequency of pair k in turns per position, as a 64-bit
 // fixed-point fraction (theta_k <= 1, so F_k < 2^61.4).  theta_k = base^(-2k/d) in double.
-void rope_freqs_host(int r, double base, RopeFreqs* f) {
+void compute_freqs(int r, double base, RopeFreqs* f) {
   std::memset(f, 0, sizeof(*f));
   const double two_pi = 6.283185307179586476925286766559;
   for (int k = 0; k < r / 2 && k < kMaxHalfDim; ++k) {
@@ -27,6 +30,30 @@ void rope_freqs_host(int r, double base, RopeFreqs* f) {
     f->lo[k] = (uint32_t)(F & 0xFFFFFFFFull);
     f->hi[k] = (uint32_t)(F >> 32);
   }
+}
+
+}  // namespace
+
+// The table for (r, base), from a per-thread cache of the last few pairs asked for (a call
+// otherwise spends 32-64 pow() evaluations on it).  Per thread, so no lock is taken.
+void rope_freqs_host(int r, double base, RopeFreqs* f) {
+  struct Entry {
+    int r;
+    double base;
+    RopeFreqs f;
+  };
+  constexpr int kEntries = 4;
+  thread_local Entry cache[kEntries];
+  thread_local int used = 0, next = 0;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].r == r && cache[i].base == base) {
+      *f = cache[i].f;
+      return;
+    }
+  compute_freqs(r, base, f);
+  cache[next] = Entry{r, base, *f};
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
 }
 
 }  // namespace attnfuse
@@ -67,18 +94,29 @@ attnfuse_status_t check_base(double base) {
   return ATTNFUSE_OK;
 }
 
-// The kernels are built for sm_103a only.
+// The kernels are built for sm_103a only.  A device's compute capability is queried once and the
+// answer kept (0 = not yet known, else major * 10 + minor); concurrent first calls may both query,
+// which is harmless.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_device_cc[kMaxDevices];
+
 attnfuse_status_t check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  int major = 0, minor = 0;
-  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  if (major != 10 || minor != 3)
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTNFUSE_ERR_UNSUPPORTED, "device index %d is beyond %d", dev, kMaxDevices);
+  int cc = g_device_cc[dev].load(std::memory_order_acquire);
+  if (cc == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    cc = major * 10 + minor;
+    g_device_cc[dev].store(cc, std::memory_order_release);
+  }
+  if (cc != 103)
     return fail(ATTNFUSE_ERR_UNSUPPORTED, "device %d has compute capability %d.%d; libattnfuse runs on 10.3 (sm_103a)",
-                dev, major, minor);
+                dev, cc / 10, cc % 10);
   return ATTNFUSE_OK;
 }
 
@@ -95,9 +133,40 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, N, H, d] tensor, boxes of 64 columns x 128 rows of one head, 128-byte swizzle.
+// [B, N, H, d] tensor, boxes of 64 columns x 128 rows of one head, 128-byte swizzle.  A descriptor
+// depends only on the address, the sizes and the dtype, so the last few encoded are kept per thread
+// (a repeated call then encodes nothing; no lock is taken).
+attnfuse_status_t encode_bnhd_uncached(CUtensorMap* map, const void* ptr, int B, int N, int H, int d,
+                                       attnfuse_dtype_t dtype, const char* name);
+
 attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, int H, int d, attnfuse_dtype_t dtype,
                               const char* name) {
+  struct Entry {
+    const void* ptr;
+    int B, N, H, d;
+    attnfuse_dtype_t dtype;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry cache[kEntries];
+  thread_local int used = 0, next = 0;
+  for (int i = 0; i < used; ++i) {
+    const Entry& c = cache[i];
+    if (c.ptr == ptr && c.B == B && c.N == N && c.H == H && c.d == d && c.dtype == dtype) {
+      *map = c.map;
+      return ATTNFUSE_OK;
+    }
+  }
+  const attnfuse_status_t st = encode_bnhd_uncached(map, ptr, B, N, H, d, dtype, name);
+  if (st != ATTNFUSE_OK) return st;
+  cache[next] = Entry{ptr, B, N, H, d, dtype, *map};
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status_t encode_bnhd_uncached(CUtensorMap* map, const void* ptr, int B, int N, int H, int d,
+                                       attnfuse_dtype_t dtype, const char* name) {
   auto fn = encode_fn();
   if (!fn) return fail(ATTNFUSE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
@@ -214,6 +283,15 @@ void set_last_error(const char* fmt, ...) {
   va_start(ap, fmt);
   std::vsnprintf(g_err, sizeof g_err, fmt, ap);
   va_end(ap);
+}
+
+attnfuse_status_t check_fwd_call(const void* q, const void* k, const void* v, const void* out, const float* lse, int B,
+                                 int Hq, int Hkv, int N, int d, double rope_base, attnfuse_mode_t mode,
+                                 attnfuse_dtype_t dtype) {
+  g_err[0] = '\0';
+  const attnfuse_status_t st = validate_fwd(q, k, v, out, lse, B, Hq, Hkv, N, d, rope_base, mode, dtype);
+  if (st != ATTNFUSE_OK) return st;
+  return check_device();
 }
 
 }  // namespace attnfuse

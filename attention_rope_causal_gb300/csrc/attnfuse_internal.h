@@ -5,9 +5,48 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
+#include "attnfuse.h"
 #include "rope.cuh"
 
 namespace attnfuse {
+
+// ---- per-device one-time set-up ----------------------------------------------------------------
+
+// A kernel's set-up on a device (function attributes, SM count) runs once per device and its
+// result (an int, e.g. the SM count) is kept.  Safe when several host threads make their first call
+// at once: the first runs the set-up under a lock, the others wait for it, and later calls read the
+// kept value without locking.  A set-up that fails is tried again on the next call.
+class DeviceOnce {
+ public:
+  static constexpr int kMaxDevices = 64;
+
+  template <typename F>
+  cudaError_t get(int dev, F&& setup, int* out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) {
+      *out = value_[dev];
+      return cudaSuccess;
+    }
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!done_[dev].load(std::memory_order_relaxed)) {
+      int v = 0;
+      const cudaError_t e = setup(&v);
+      if (e != cudaSuccess) return e;
+      value_[dev] = v;
+      done_[dev].store(true, std::memory_order_release);
+    }
+    *out = value_[dev];
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+  int value_[kMaxDevices] = {};
+};
 
 // ---- pre-rotation kernel --------------------------------------------------------------------
 
@@ -139,5 +178,11 @@ void rope_freqs_host(int r, double base, RopeFreqs* f);
 
 // Sets the calling thread's attnfuse_last_error() message (printf-style).
 void set_last_error(const char* fmt, ...);
+
+// The argument checks of attnfuse_rope_causal_fwd (pointers, sizes, alignment, mode, dtype, head
+// dimension, base) and the device check (sm_103), in that order; no device work.
+attnfuse_status_t check_fwd_call(const void* q, const void* k, const void* v, const void* out, const float* lse, int B,
+                                 int Hq, int Hkv, int N, int d, double rope_base, attnfuse_mode_t mode,
+                                 attnfuse_dtype_t dtype);
 
 }  // namespace attnfuse

@@ -1,4 +1,4 @@
-"""Fits the polynomials behind rope_sincos_quarter() in rope.cuh: minimax (absolute error)
+"""Fits the polynomials behind sincos_turns() in rope.cuh: minimax (absolute error)
 approximations of sin(pi/2 r) (odd, degree 7) and cos(pi/2 r) (even, degree 8) for r in [-1/2, 1/2]
 (a quarter-turn fraction after exact integer reduction to the nearest quarter turn), solved as
 linear programs on a dense grid, rounded to fp32, and re-evaluated in fp32 Horner form.

@@ -24,8 +24,10 @@
  * accumulation; P and the rotated Q/K are rounded to `dtype` once.
  *
  * Ownership and streams.  Every buffer belongs to the caller and must be device memory (q, k, v,
- * out, workspace 16-byte aligned; lse 4-byte aligned).  `stream` is a cudaStream_t (NULL = the
- * legacy default stream); all work is enqueued on it and the calls return without waiting.
+ * out, workspace 16-byte aligned; lse 4-byte aligned).  `stream` is a cudaStream_t passed as void*
+ * (so that this header needs no CUDA include; NULL = the legacy default stream); all work is
+ * enqueued on it and the calls return without waiting.  `rope_base` is a double because theta_k is
+ * computed from it in fp64.
  *
  * Errors.  Arguments are validated before anything is launched; a failed call returns a status,
  * launches nothing and leaves a message for attnfuse_last_error().  Faults raised while kernels
@@ -218,9 +220,12 @@ attnfuse_status_t attnfuse_diag_wait_timeout(uint64_t timeout_ns, void* stream);
  * the rotated Q and K go to a fixed buffer of ATTNFUSE_NOALLOC_SCRATCH_BYTES compiled into the
  * library (a __device__ array: every GPU that loads the library holds it until the process exits).
  * Calls whose rotated Q and K need more than that (attnfuse_workspace_bytes(..., PREROTATE, ...))
- * return ATTNFUSE_ERR_INVALID_ARG before launching anything.  No cudaMalloc, cudaFree or other
+ * return ATTNFUSE_ERR_INVALID_ARG before launching anything; every other argument is checked as in
+ * attnfuse_rope_causal_fwd, also before any device work.  No cudaMalloc, cudaFree or other
  * allocating call is made.  The first call on each device looks up the buffer's device address
- * (cudaGetSymbolAddress, with that device current); make that first call before any stream capture.
+ * (cudaGetSymbolAddress, with that device current), and so does the first call after the device's
+ * context was destroyed and created again (e.g. cudaDeviceReset): make such a first call before any
+ * stream capture.
  * All calls share the one buffer and it keeps the last call's contents: calls that may overlap on
  * the GPU (other streams, other host threads) race on it and must be ordered by the caller.
  */

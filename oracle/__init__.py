@@ -40,23 +40,38 @@ _lock = threading.Lock()
 _lib = None
 
 
+# Load this shared library instead of building oracle/_build/liboracle.so (the planted-mistake test
+# runs the pin suites against deliberately broken copies of the C source built this way).
+LIB_ENV = "ATTNFUSE_ORACLE_LIB"
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile an oracle C source into a shared library (plain IEEE: no fast-math, no FMA contraction)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math",
+           src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain IEEE: no fast-math, no FMA contraction)."""
+    """Compile the oracle into ``oracle/_build/liboracle.so``."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math",
-               _SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_source(_SRC, tmp)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def source_path() -> str:
+    return _SRC
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            lib = ctypes.CDLL(os.environ.get(LIB_ENV) or build())
             lib.orc_rope_rotate.restype = ctypes.c_int
             lib.orc_rope_rotate.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p, ctypes.c_int]
@@ -224,13 +239,6 @@ def rope_causal(q, k, v, base: float, rows=None, threads: int | None = None, rot
                                     lse.ctypes.data, int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError("orc_rope_causal_kv failed")
-    return out, lse
-    r = d if rotary_dim is None else int(rotary_dim)
-    rc = _load().orc_rope_causal_ex(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, dq, B, Hq, Hkv, N, d, r,
-                                    int(bool(interleaved)), float(base), sel_ptr, n_sel, out.ctypes.data,
-                                    lse.ctypes.data, int(threads or default_threads()))
-    if rc != 0:
-        raise RuntimeError("orc_rope_causal_ex failed")
     return out, lse
 
 

@@ -31,13 +31,25 @@ def call_noalloc(lib, q, k, v, out, lse, base):
         float(base), binding.DTYPES[q.dtype], torch.cuda.current_stream().cuda_stream)
 
 
-def test_rejects_problems_larger_than_the_buffer_without_a_gpu(lib):
-    # 32k tokens of 32 + 8 heads at d = 128 need 335 MB of rotated Q and K: refused before any launch.
+def test_argument_errors_come_before_any_device_work(lib):
+    # Null or misaligned pointers and unsupported sizes are refused by the same checks as the regular
+    # entry point, before the device is touched (so these run without a GPU).
+    assert lib.attnfuse_rope_causal_fwd_prerotate_noalloc(None, 0x10000, 0x10000, 0x10000, None, 1, 2, 2, 16, 64,
+                                                          1e4, 0, None) == 1
+    assert lib.attnfuse_rope_causal_fwd_prerotate_noalloc(0x10008, 0x10000, 0x10000, 0x10000, None, 1, 2, 2, 16, 64,
+                                                          1e4, 0, None) == 1
+    assert b"aligned" in lib.attnfuse_last_error()
+    assert lib.attnfuse_rope_causal_fwd_prerotate_noalloc(0x10000, 0x10000, 0x10000, 0x10000, None, 1, 2, 2, 16,
+                                                          96, 1e4, 0, None) == 2  # d = 96: unsupported
+
+
+@pytest.mark.gpu
+def test_rejects_problems_larger_than_the_buffer(lib):
+    # 32k tokens of 32 + 8 heads at d = 128 need 335 MB of rotated Q and K: refused before any launch
+    # (the size check follows the device check, so it needs the GPU to be an sm_103 part).
     st = lib.attnfuse_rope_causal_fwd_prerotate_noalloc(0x10000, 0x10000, 0x10000, 0x10000, None, 1, 32, 8, 32768,
                                                         128, 5e5, 0, None)
     assert st == 1 and b"fixed" in lib.attnfuse_last_error()
-    assert lib.attnfuse_rope_causal_fwd_prerotate_noalloc(0x10000, 0x10000, 0x10000, 0x10000, None, 1, 2, 2, 16,
-                                                          96, 1e4, 0, None) == 1
 
 
 @pytest.mark.gpu
@@ -59,3 +71,23 @@ def test_matches_regular_entry_point_on_two_calls_in_a_row(lib):
         t = TOL[w.dtype]
         assert e["max_abs"] <= t["max_abs"] and e["rel_l2"] <= t["rel_l2"], (w.name, e)
         assert e["lse_row"] <= t["lse_row"], (w.name, e)
+
+
+@pytest.mark.gpu
+def test_a_call_allocates_no_device_memory(lib):
+    # After a first call (which looks up the buffer and loads the kernels), further calls change
+    # neither the device's free memory nor what torch's allocator holds.
+    w = inputs.Workload("small", B=1, Hq=4, Hkv=2, N=512, d=128, dtype="bf16", rope_base=5e5, sigma=1.0, seed=5)
+    q, k, v = (t.cuda() for t in inputs.make_inputs(w))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), device="cuda")
+    assert call_noalloc(lib, q, k, v, out, lse, w.rope_base) == 0, binding.last_error()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    held0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        assert call_noalloc(lib, q, k, v, out, lse, w.rope_base) == 0, binding.last_error()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0 and torch.cuda.memory_allocated() == held0
+    assert binding.device_status() == 0
