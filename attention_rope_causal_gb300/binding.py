@@ -14,10 +14,11 @@ import torch
 
 from . import build as _build
 
-ATTNFUSE_FUSED, ATTNFUSE_PREROTATE, ATTNFUSE_AUTO, ATTNFUSE_SPLIT = 0, 1, 2, 3
+ATTNFUSE_FUSED, ATTNFUSE_PREROTATE, ATTNFUSE_AUTO, ATTNFUSE_SPLIT, ATTNFUSE_NONE = 0, 1, 2, 3, 4
 ATTNFUSE_BF16, ATTNFUSE_FP16 = 0, 1
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_TIMEOUT", 5: "ERR_NO_MEMORY"}
-MODES = {"fused": ATTNFUSE_FUSED, "prerotate": ATTNFUSE_PREROTATE, "auto": ATTNFUSE_AUTO, "split": ATTNFUSE_SPLIT}
+MODES = {"fused": ATTNFUSE_FUSED, "prerotate": ATTNFUSE_PREROTATE, "auto": ATTNFUSE_AUTO, "split": ATTNFUSE_SPLIT,
+         "none": ATTNFUSE_NONE}
 MODE_NAMES = {v: k for k, v in MODES.items()}
 DTYPES = {torch.bfloat16: ATTNFUSE_BF16, torch.float16: ATTNFUSE_FP16}
 

@@ -261,8 +261,10 @@ attnfuse_status_t validate_fwd(const void* q, const void* k, const void* v, cons
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "B, Hq, Hkv, N must be >= 1");
   if (N >= kMaxN) return fail(ATTNFUSE_ERR_INVALID_ARG, "N=%d exceeds the supported maximum %d", N, kMaxN - 1);
   if (Hq % Hkv != 0) return fail(ATTNFUSE_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
-  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE && mode != ATTNFUSE_AUTO && mode != ATTNFUSE_SPLIT)
-    return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0), prerotate (1), auto (2) or split (3)", (int)mode);
+  if (mode != ATTNFUSE_FUSED && mode != ATTNFUSE_PREROTATE && mode != ATTNFUSE_AUTO && mode != ATTNFUSE_SPLIT &&
+      mode != ATTNFUSE_NONE)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "mode %d is not fused (0), prerotate (1), auto (2), split (3) or none (4)",
+                (int)mode);
   attnfuse_status_t st = check_dtype_d(d, dtype);
   if (st != ATTNFUSE_OK) return st;
   if ((st = check_base(base)) != ATTNFUSE_OK) return st;
@@ -340,7 +342,7 @@ size_t attnfuse_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfus
   if (decode_eligible(B, Hq, Hkv, N, mode)) return decode_workspace_bytes(B, Hkv, Nk, d);
   if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
   if (mode == ATTNFUSE_SPLIT) return round_up(tensor_bytes(B, Nk, Hkv, d), 256);
-  if (mode != ATTNFUSE_PREROTATE) return 0;
+  if (mode != ATTNFUSE_PREROTATE) return 0;  // FUSED, NONE
   return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, Nk, Hkv, d), 256);
 }
 
@@ -407,6 +409,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
   if (st != ATTNFUSE_OK) return st;
   Opts o;
   if ((st = resolve_opts(opts, d, N, &o)) != ATTNFUSE_OK) return st;
+  if (mode == ATTNFUSE_NONE && (o.rdim != d || o.interleaved || o.qpos || o.kpos))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "mode none (no rotation) takes kv_len only: no rotary_dim, interleaved or positions");
   const int Nk = o.Nk;
   const bool decode = decode_eligible(B, Hq, Hkv, N, mode);
   if (mode == ATTNFUSE_AUTO && !decode) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);

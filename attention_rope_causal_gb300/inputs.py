@@ -55,21 +55,25 @@ LONG = Workload("long_32k", B=1, Hq=32, Hkv=8, N=32768, d=128, dtype="fp16", rop
                 seed=3)
 
 SWEEP_NS = (2048, 4096, 5500, 8192, 16384)
+SWEEP_EXTRA_NS = (1024, 1536)  # below the sweep's range, so that a crossover near 2048 is bracketed
 SWEEP_TOKENS = 16384
 
 
-def sweep_workloads():
+def sweep_workloads(extra: bool = False):
     """Crossover sweep: GQA d=128 (32/8) and MHA d=64 (16/16), N in SWEEP_NS, B = round(16384 / N),
-    fp16 and bf16, rope base 500000.  Seeds are 100 + the point's index in this list."""
+    fp16 and bf16, rope base 500000.  Seeds are 100 + the point's index in this list.  With extra,
+    the points N in SWEEP_EXTRA_NS follow (same families and dtypes, seeds continuing)."""
     out = []
     idx = 0
-    for family, (Hq, Hkv, d) in (("gqa", (32, 8, 128)), ("mha", (16, 16, 64))):
-        for dtype in ("bf16", "fp16"):
-            for N in SWEEP_NS:
-                B = max(1, round(SWEEP_TOKENS / N))
-                out.append(Workload(f"sweep_{family}_d{d}_{dtype}_N{N}", B=B, Hq=Hq, Hkv=Hkv, N=N, d=d,
-                                    dtype=dtype, rope_base=500000.0, sigma=1.0, seed=100 + idx))
-                idx += 1
+    groups = [SWEEP_NS] + ([SWEEP_EXTRA_NS] if extra else [])
+    for ns in groups:
+        for family, (Hq, Hkv, d) in (("gqa", (32, 8, 128)), ("mha", (16, 16, 64))):
+            for dtype in ("bf16", "fp16"):
+                for N in ns:
+                    B = max(1, round(SWEEP_TOKENS / N))
+                    out.append(Workload(f"sweep_{family}_d{d}_{dtype}_N{N}", B=B, Hq=Hq, Hkv=Hkv, N=N, d=d,
+                                        dtype=dtype, rope_base=500000.0, sigma=1.0, seed=100 + idx))
+                    idx += 1
     return out
 
 

@@ -283,18 +283,61 @@ def run_reference_arm(args):
 # GPU timing
 
 
-def time_steps(fn, steps, flush, stream):
-    """Per-step CUDA-event times (ms) of fn() with an L2 flush before each step, outside the events."""
+WARMUP_MIN_S = 0.05   # warm-up runs at least this long, whatever --warmup says
+SLEEP_HZ = 2.07e9     # SM cycles per second at the maximum clock (a slower clock only lengthens a sleep)
+CHUNK = 64            # steps enqueued behind one sleep
+
+
+def time_steps(fn, steps, flush, stream, clean_l2=False):
+    """Per-step CUDA-event times (ms) of fn() with an L2 flush before each step, outside the events.
+
+    The flush writes a 512 MiB buffer (L2 then holds dirty lines of it); with clean_l2 it is read
+    back as well (clean lines).  The GPU is kept behind the host: each chunk of steps is enqueued
+    behind a spin (torch.cuda._sleep) longer than the host takes to enqueue the chunk, so no step
+    ever waits for the host and host-side overhead cannot enter the measured times."""
     import torch
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    times = []
+    host_per_step = 3e-4  # s; measured on every chunk afterwards
+    scratch = torch.empty(1, dtype=torch.float32, device=flush.device) if clean_l2 else None
     with torch.cuda.stream(stream):
-        for a, b in evs:
-            flush.zero_()
-            a.record(stream)
-            fn()
-            b.record(stream)
-    stream.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+        done = 0
+        while done < steps:
+            n = min(CHUNK, steps - done)
+            torch.cuda._sleep(int((1.5 * host_per_step * n + 2e-4) * SLEEP_HZ))
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            t = time.perf_counter()
+            for a, b in evs:
+                flush.zero_()
+                if clean_l2:
+                    torch.sum(flush, dim=0, out=scratch.view(()))
+                a.record(stream)
+                fn()
+                b.record(stream)
+            host_per_step = max(host_per_step, (time.perf_counter() - t) / n)
+            stream.synchronize()
+            times += [a.elapsed_time(b) for a, b in evs]
+            done += n
+    return times
+
+
+def run_warmup(run_batch, steps, min_s=WARMUP_MIN_S, clock=time.perf_counter):
+    """Calls run_batch(n) until at least `steps` steps have run and at least min_s seconds have
+    passed (the page-4 protocol's >= 50 ms warm-up, whatever the step count says); returns
+    (steps run, seconds)."""
+    t0 = clock()
+    n = 0
+    while n < steps or clock() - t0 < min_s:
+        batch = max(1, steps - n) if n < steps else 8
+        run_batch(batch)
+        n += batch
+    return n, clock() - t0
+
+
+def warm_up(fn, steps, flush, stream):
+    """Untimed steps of fn (with the flush, as timed) under run_warmup's rule."""
+    import torch
+    torch.cuda.synchronize()
+    return run_warmup(lambda n: time_steps(fn, n, flush, stream), steps)
 
 
 def e2e_pipelined(w, q0, k0, v0, steps, warmup, nb=2):
@@ -379,38 +422,91 @@ def rope_pass_fn(w, stream):
     return lambda: binding.rope_apply(x, w.rope_base, out=y, stream=stream)
 
 
+def plain_fn(w, q, k, v, out, lse, stream):
+    """The plain attention kernel alone (mode "none") on Q and K rotated once beforehand: the second
+    stage of the pre-rotate pipeline, timed without the RoPE pass."""
+    from attention_rope_causal_gb300 import binding
+    qr, kr = binding.rope_apply(q, w.rope_base), binding.rope_apply(k, w.rope_base)
+    return lambda: binding.rope_causal_fwd(qr, kr, v, w.rope_base, mode="none", out=out, lse=lse, stream=stream)
+
+
 def measure_point(w, steps, warmup):
-    """Median-of-steps times (ms) for fused, the pre-rotate and split pipelines, and the RoPE pass alone."""
+    """Median-of-steps times (ms) for fused, the pre-rotate and split pipelines, the plain attention
+    kernel alone (mode none) and the RoPE pass alone."""
     import torch
     from attention_rope_causal_gb300 import binding
     stream = torch.cuda.current_stream()
     q, k, v, out, lse, ws = gpu_setup(w, ("fused", "prerotate", "split"))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    fns = {mode: fwd_fn(w, q, k, v, out, lse, ws[mode], mode, stream) for mode in ("fused", "prerotate", "split")}
+    fns["plain"] = plain_fn(w, q, k, v, out, lse, stream)
+    fns["rope"] = rope_pass_fn(w, stream)
     res = {}
-    for mode in ("fused", "prerotate", "split"):
-        f = fwd_fn(w, q, k, v, out, lse, ws[mode], mode, stream)
-        time_steps(f, warmup, flush, stream)
-        res[mode] = statistics.median(time_steps(f, steps, flush, stream))
-    rope_pass = rope_pass_fn(w, stream)
-    time_steps(rope_pass, warmup, flush, stream)
-    res["rope"] = statistics.median(time_steps(rope_pass, steps, flush, stream))
+    for name, f in fns.items():
+        warm_up(f, warmup, flush, stream)
+        res[name] = statistics.median(time_steps(f, steps, flush, stream))
     if binding.device_status() != 0:
         raise RuntimeError(f"device status: {binding.last_error()}")
     return res
+
+
+def rope_bytes(w) -> float:
+    """Algorithmic bytes of the pre-rotation pass: Q and K read and written once (16-bit elements)."""
+    return 2.0 * w.B * w.N * (w.Hq + w.Hkv) * w.d * 2
+
+
+def rotation_calculus(points, peak_tflops, hbm_gbs):
+    """The crossover model of the AttnFuse report (paragraph 3: pre-rotation costs memory bandwidth,
+    in-kernel rotation costs compute) set beside the measured crossover, for one family and dtype.
+
+    points: dicts with N, B, Hq, Hkv, d and the measured ms of fused, prerotate, plain and rope.
+    Per point: alpha = T_fused / T_plain - 1 (in-kernel rotation as a fraction of attention time),
+    rho = (T_prerotate - T_plain) / T_plain (what the pass adds to the pipeline, relative) and
+    rope_frac = T_rope / T_plain (the pass timed alone).
+    Model: T_fused = (1 + a) T_attn(N) and T_pre = T_attn(N) + bytes(N) / BW, with T_attn(N) =
+    flops(N) / (eta P), a = median alpha and eta = median plain-kernel efficiency over the points.
+    At fixed tokens B N (the sweep's 16384) flops grow as N and bytes do not, so the two meet at
+        N* = 2 (Hq + Hkv) eta P / (a Hq BW)
+    -- with BW the measured HBM copy bandwidth ("peak" model) and with the RoPE pass's own measured
+    GB/s ("calibrated" model).  The measured N* interpolates log(T_fused / T_pre) between points."""
+    pts = sorted(points, key=lambda r: r["N"])
+    rows = []
+    for r in pts:
+        flops = 2.0 * r["B"] * r["Hq"] * r["N"] ** 2 * r["d"]
+        rows.append(dict(N=r["N"], alpha=r["fused_ms"] / r["plain_ms"] - 1.0,
+                         rho=(r["prerotate_ms"] - r["plain_ms"]) / r["plain_ms"],
+                         rope_frac=r["rope_ms"] / r["plain_ms"],
+                         eta=flops / (r["plain_ms"] * 1e-3) / (peak_tflops * 1e12),
+                         rope_gbs=2.0 * r["B"] * r["N"] * (r["Hq"] + r["Hkv"]) * r["d"] * 2 / (r["rope_ms"] * 1e-3) / 1e9))
+    a = statistics.median(x["alpha"] for x in rows)
+    eta = statistics.median(x["eta"] for x in rows)
+    bw_rope = statistics.median(x["rope_gbs"] for x in rows)
+    Hq, Hkv = pts[0]["Hq"], pts[0]["Hkv"]
+    P = peak_tflops * 1e12
+
+    def n_star(bw_gbs):
+        return 2.0 * (Hq + Hkv) * eta * P / (a * Hq * bw_gbs * 1e9) if a > 0 else None
+
+    measured, how = crossover([r["N"] for r in pts], [r["fused_ms"] for r in pts], [r["prerotate_ms"] for r in pts])
+    return {"points": rows, "alpha_median": a, "eta_plain_median": eta, "rope_gbs_median": bw_rope,
+            "model_n_star_peak_bw": n_star(hbm_gbs), "model_n_star_measured_rope_bw": n_star(bw_rope),
+            "measured_n_star": measured, "measured_note": how}
 
 
 def run_sweep(args):
     from attention_rope_causal_gb300 import inputs
     peaks = load_peaks()
     rows = []
-    for w in inputs.sweep_workloads():
+    for w in inputs.sweep_workloads(extra=True):
         t = measure_point(w, args.steps, args.warmup)
         fl = w.causal_flops
-        qk_bytes = 2 * (w.B * w.N * (w.Hq + w.Hkv) * w.d * 2)
         rec = {"workload": w.name, "N": w.N, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "dtype": w.dtype,
-               "fused_ms": t["fused"], "prerotate_ms": t["prerotate"], "split_ms": t["split"], "rope_ms": t["rope"],
+               "fused_ms": t["fused"], "prerotate_ms": t["prerotate"], "split_ms": t["split"],
+               "plain_ms": t["plain"], "rope_ms": t["rope"],
                "fused_tflops": fl / t["fused"] / 1e9, "prerotate_tflops": fl / t["prerotate"] / 1e9,
-               "split_tflops": fl / t["split"] / 1e9, "rope_gbs": qk_bytes / t["rope"] / 1e6,
+               "split_tflops": fl / t["split"] / 1e9, "plain_tflops": fl / t["plain"] / 1e9,
+               "rope_gbs": rope_bytes(w) / t["rope"] / 1e6,
+               "alpha": t["fused"] / t["plain"] - 1.0, "rope_over_plain": t["rope"] / t["plain"],
                "fused_over_prerotate": t["fused"] / t["prerotate"],
                "fastest": min(("fused", "prerotate", "split"), key=lambda m: t[m])}
         rows.append(rec)
@@ -419,10 +515,7 @@ def run_sweep(args):
     for fam in ("gqa", "mha"):
         for dt in ("bf16", "fp16"):
             pts = [r for r in rows if r["workload"].startswith(f"sweep_{fam}_") and r["dtype"] == dt]
-            pts.sort(key=lambda r: r["N"])
-            n_star, how = crossover([r["N"] for r in pts], [r["fused_ms"] for r in pts],
-                                    [r["prerotate_ms"] for r in pts])
-            summary[f"{fam}_{dt}"] = {"n_star": n_star, "note": how}
+            summary[f"{fam}_{dt}"] = rotation_calculus(pts, peaks["bf16_tflops"], peaks["hbm_gbs"])
     print(json.dumps({"sweep_summary": summary, "peaks": peaks}), flush=True)
     return 0
 
@@ -473,9 +566,12 @@ def run_only(args):
         f = bwd_fn(w, q, k, v, out, lse, stream)
     elif args.only == "decode":
         f = decode_fn(w, "fused", stream)
-    else:
+    elif args.only != "plain":
         f = fwd_fn(w, q, k, v, out, lse, ws[args.only], args.only, stream)
-    ms = time_steps(f, args.warmup + args.steps, flush, stream)[args.warmup:]
+    if args.only == "plain":
+        f = plain_fn(w, q, k, v, out, lse, stream)
+    warm_up(f, args.warmup, flush, stream)
+    ms = time_steps(f, args.steps, flush, stream)
     st = binding.device_status()
     print(json.dumps({"only": args.only, "workload": w.name, "median_ms": statistics.median(ms), "status": st}))
     return 0 if st == 0 else 1
@@ -494,7 +590,7 @@ def run_ours(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     step = fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)
 
-    time_steps(step, args.warmup, flush, stream)
+    warm_steps, warm_s = warm_up(step, args.warmup, flush, stream)
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0.0)
     barrier(world)
@@ -520,27 +616,24 @@ def run_ours(args):
     e2e_s = max_over_ranks(e2e_step_ms * args.steps / 1e3, world)
 
     # the competing pre-rotation path, and the RoPE pass alone (HBM-bound)
-    pre = fwd_fn(w, q, k, v, out, lse, ws["prerotate"], "prerotate", stream)
-    time_steps(pre, args.warmup, flush, stream)
-    pre_ms = statistics.median(time_steps(pre, max(20, args.steps // 10), flush, stream))
-    spl = fwd_fn(w, q, k, v, out, lse, ws["split"], "split", stream)
-    time_steps(spl, args.warmup, flush, stream)
-    split_ms = statistics.median(time_steps(spl, max(20, args.steps // 10), flush, stream))
+    side_steps = max(20, args.steps // 10)
+
+    def median_ms(f, clean_l2=False):
+        warm_up(f, args.warmup, flush, stream)
+        return statistics.median(time_steps(f, side_steps, flush, stream, clean_l2=clean_l2))
+
+    pre_ms = median_ms(fwd_fn(w, q, k, v, out, lse, ws["prerotate"], "prerotate", stream))
+    split_ms = median_ms(fwd_fn(w, q, k, v, out, lse, ws["split"], "split", stream))
+    plain_ms = median_ms(plain_fn(w, q, k, v, out, lse, stream))
     rope_pass = rope_pass_fn(w, stream)
-    time_steps(rope_pass, args.warmup, flush, stream)
-    rope_ms = statistics.median(time_steps(rope_pass, max(20, args.steps // 10), flush, stream))
-    rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
+    rope_ms = median_ms(rope_pass)
+    rope_ms_clean = median_ms(rope_pass, clean_l2=True)
+    rope_b = 2 * (q.numel() + k.numel()) * q.element_size()
     # the backward pass on the forward's out / lse (a training step's second half)
     fwd_fn(w, q, k, v, out, lse, ws["fused"], "fused", stream)()
-    bwd = bwd_fn(w, q, k, v, out, lse, stream)
-    time_steps(bwd, args.warmup, flush, stream)
-    bwd_ms = statistics.median(time_steps(bwd, max(20, args.steps // 10), flush, stream))
+    bwd_ms = median_ms(bwd_fn(w, q, k, v, out, lse, stream))
     # one decode step against w.N cached keys: the decode kernels (fused mode) and the tile kernels
-    dec_ms = {}
-    for mode in ("fused", "split"):
-        dec = decode_fn(w, mode, stream)
-        time_steps(dec, args.warmup, flush, stream)
-        dec_ms[mode] = statistics.median(time_steps(dec, max(20, args.steps // 10), flush, stream))
+    dec_ms = {mode: median_ms(decode_fn(w, mode, stream)) for mode in ("fused", "split")}
     kv_bytes = 2 * k.numel() * k.element_size()
     if binding.device_status() != 0:
         raise RuntimeError(f"device status: {binding.last_error()}")
@@ -555,7 +648,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
                    "rope_base": w.rope_base, "mode": "fused", "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every step (512 MiB write, outside the timed events)"},
+                   "l2": "flushed before every step (512 MiB write, outside the timed events)",
+                   "queue": "steps enqueued behind a GPU spin, so the host never gates a step"},
         "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
@@ -566,10 +660,22 @@ def run_ours(args):
                 "schedule": "H2D, compute and D2H on three streams over two buffer sets; time from the first "
                             "H2D to the last D2H"},
         "gpu_launches": args.steps,
-        "prerotate": {"ms": pre_ms, "tflops": w.causal_flops / (pre_ms / 1e3) / 1e12, "rope_ms": rope_ms,
-                      "rope_gbs": rope_bytes / (rope_ms / 1e3) / 1e9,
-                      "rope_frac_of_hbm": rope_bytes / (rope_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                      "fused_over_prerotate": per_launch_ms / pre_ms},
+        "warmup_run": {"steps": warm_steps, "seconds": warm_s, "rule": f">= {args.warmup} steps and >= "
+                                                                           f"{WARMUP_MIN_S * 1e3:.0f} ms"},
+        "prerotate": {"ms": pre_ms, "tflops": w.causal_flops / (pre_ms / 1e3) / 1e12,
+                      "fused_over_prerotate": per_launch_ms / pre_ms,
+                      "rope_pass": {"bytes": rope_b,
+                                    "ms_after_write_flush": rope_ms,
+                                    "gbs_after_write_flush": rope_b / (rope_ms / 1e3) / 1e9,
+                                    "ms_after_clean_flush": rope_ms_clean,
+                                    "gbs_after_clean_flush": rope_b / (rope_ms_clean / 1e3) / 1e9,
+                                    "frac_of_hbm_after_clean_flush": rope_b / (rope_ms_clean / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                    "note": "CUDA events; the write flush leaves L2 full of dirty lines that drain "
+                                            "during the pass, the clean flush reads its buffer back first; ncu's "
+                                            "figure for the same launch (cold, serialised) is in profiles/"}},
+        "plain_attention": {"ms": plain_ms, "tflops": w.causal_flops / (plain_ms / 1e3) / 1e12,
+                            "alpha_fused": per_launch_ms / plain_ms - 1.0,
+                            "note": "mode none: the pre-rotate path's attention kernel alone on rotated Q, K"},
         "split": {"ms": split_ms, "tflops": w.causal_flops / (split_ms / 1e3) / 1e12,
                   "note": "K rotated by the pre-rotation pass, query tiles rotated on chip"},
         "backward": {"ms": bwd_ms, "tflops": 2.5 * w.causal_flops / (bwd_ms / 1e3) / 1e12,
@@ -599,7 +705,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=inputs.LLAMA.name, choices=sorted(inputs.NAMED))
     ap.add_argument("--sweep", action="store_true", help="run the crossover sweep instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("fused", "prerotate", "split", "rope", "backward", "decode"),
+    ap.add_argument("--only", choices=("fused", "prerotate", "split", "plain", "rope", "backward", "decode"),
                     help="time one path alone (for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

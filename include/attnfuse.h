@@ -45,7 +45,13 @@
 extern "C" {
 #endif
 
-typedef enum { ATTNFUSE_FUSED = 0, ATTNFUSE_PREROTATE = 1, ATTNFUSE_AUTO = 2, ATTNFUSE_SPLIT = 3 } attnfuse_mode_t;
+typedef enum {
+  ATTNFUSE_FUSED = 0,
+  ATTNFUSE_PREROTATE = 1,
+  ATTNFUSE_AUTO = 2,
+  ATTNFUSE_SPLIT = 3,
+  ATTNFUSE_NONE = 4
+} attnfuse_mode_t;
 
 typedef enum { ATTNFUSE_BF16 = 0, ATTNFUSE_FP16 = 1 } attnfuse_dtype_t;
 
@@ -68,6 +74,11 @@ typedef enum {
  *                              query tile on chip (each is read once): rotation cost paid once per
  *                              element for both tensors.
  *   mode = ATTNFUSE_AUTO:      whichever mode attnfuse_select_mode returns for the shape.
+ *   mode = ATTNFUSE_NONE:      no rotation: q and k are taken as already rotated (e.g. by
+ *                              attnfuse_rope_apply) and the attention kernel of the pre-rotate path
+ *                              runs on them alone -- the "plain causal attention" that follows the
+ *                              standalone RoPE pass in the pages' pre-rotation path.  Takes kv_len
+ *                              but no rotation option (rotary_dim, interleaved, positions).
  * FUSED and AUTO calls with few queries per KV head -- (Hq / Hkv) N <= 16 query rows (a decode
  * step, a speculative-decode step) -- run split-KV decode kernels instead: each CTA rotates one
  * slice of one KV head's keys and the head's query rows on chip and runs the two products as
@@ -83,7 +94,7 @@ attnfuse_status_t attnfuse_rope_causal_fwd(const void* q, const void* k, const v
                                            attnfuse_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                            void* stream);
 
-/* Bytes of workspace attnfuse_rope_causal_fwd needs: 0 for FUSED; for PREROTATE the rotated copies
+/* Bytes of workspace attnfuse_rope_causal_fwd needs: 0 for FUSED and NONE; for PREROTATE the rotated copies
  * of Q and K (each rounded up to 256 bytes); for SPLIT the rotated K; for AUTO those of the selected
  * mode; for FUSED and AUTO at the decode shapes the decode kernels' partial results (per key
  * slice and KV head, 16 query-row slots of d + 2 floats).  Returns 0 for invalid arguments. */

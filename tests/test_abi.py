@@ -71,6 +71,14 @@ def test_rope_apply_rejects_bad_arguments(lib, kw, status):
     assert lib.attnfuse_rope_apply(a["x"], a["y"], a["B"], a["N"], a["H"], a["d"], a["base"], a["dtype"], None) == status
 
 
+def test_none_mode_needs_no_workspace_and_takes_no_rotation_option(lib):
+    assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 4, 0) == 0
+    opts = binding.RopeOpts(64, 0, 0, None, None)  # rotary_dim: meaningless without a rotation
+    st = lib.attnfuse_rope_causal_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 128, 128, 1e4, 4, 0, None, 0,
+                                         ctypes.byref(opts), None)
+    assert st == 1 and b"none" in lib.attnfuse_last_error()
+
+
 def test_workspace_bytes(lib):
     assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 0, 0) == 0
     q = 1 * 4096 * 32 * 128 * 2
@@ -96,7 +104,7 @@ def test_split_mode_workspace_is_the_rotated_keys(lib):
     assert lib.attnfuse_workspace_bytes(1, 32, 8, 4096, 128, 3, 0) == 1 * 4096 * 8 * 128 * 2
     assert lib.attnfuse_workspace_bytes(1, 1, 1, 1, 64, 3, 1) == 256
     assert fwd(lib, mode=3, ws=FAKE, ws_bytes=16) == 1       # workspace too small for K'
-    assert fwd(lib, mode=4) == 1
+    assert fwd(lib, mode=5) == 1                              # no mode 5
 
 
 def test_auto_mode_workspace_is_that_of_the_selected_mode(lib):

@@ -141,6 +141,20 @@ def test_auto_mode_runs_the_selected_mode(shape):
     assert_close(oa.double().numpy(), la.double().numpy(), o_ref, l_ref, dt, f"auto ({sel}) {shape}")
 
 
+@pytest.mark.parametrize("shape", [(1, 300, 4, 2, 128, "bf16"), (2, 257, 2, 2, 64, "fp16"), (1, 4096, 32, 8, 128, "bf16")])
+def test_none_mode_is_the_prerotate_paths_attention(shape):
+    # mode "none" runs the pre-rotate path's attention kernel on q and k as given; fed the RoPE
+    # pass's output it reproduces the pre-rotate mode bit for bit (same kernels, same operands).
+    B, N, Hq, Hkv, d, dt = shape
+    q, k, v = (t.cuda() for t in draw(B, N, Hq, Hkv, d, dt, seed=41))
+    qr, kr = binding.rope_apply(q, 5e5), binding.rope_apply(k, 5e5)
+    on, ln = binding.rope_causal_fwd(qr, kr, v, 5e5, mode="none")
+    op, lp = binding.rope_causal_fwd(q, k, v, 5e5, mode="prerotate")
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert torch.equal(on, op) and torch.equal(ln, lp)
+
+
 def test_lse_optional():
     q, k, v = draw(1, 200, 2, 1, 64, "bf16", seed=3)
     out_a, _ = binding.rope_causal_fwd(q.cuda(), k.cuda(), v.cuda(), 1e4, want_lse=False)
