@@ -69,6 +69,32 @@ def test_small_full(B, N, Hq, Hkv, d, dt, mode):
     assert_close(out.double().numpy(), lse.double().numpy(), o_ref, l_ref, dt, f"{mode} {B}x{N}x{Hq}/{Hkv}x{d} {dt}")
 
 
+# d = 128 with query-head groups of 4, 8, 12 and 16 (the Llama-3-8B layout and its neighbours):
+# head-pair units of the fused kernel, ragged lengths around 64 and 128 rows, one to several units
+# per CTA.
+GROUPED = [
+    # B, N, Hq, Hkv, dtype
+    (1, 1, 4, 1, "bf16"),
+    (1, 63, 4, 1, "fp16"),
+    (1, 64, 4, 1, "bf16"),
+    (1, 65, 4, 1, "bf16"),
+    (2, 129, 8, 2, "fp16"),
+    (1, 191, 4, 1, "bf16"),
+    (3, 257, 4, 1, "bf16"),
+    (1, 384, 8, 1, "fp16"),
+    (1, 1000, 16, 1, "bf16"),
+    (2, 700, 12, 3, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,dt", GROUPED)
+def test_grouped_heads_full(B, N, Hq, Hkv, dt):
+    q, k, v = draw(B, N, Hq, Hkv, 128, dt, seed=N * 5 + Hq)
+    o_ref, l_ref = oracle.rope_causal(q, k, v, 5e5)
+    out, lse = run_gpu(q, k, v, 5e5, "fused")
+    assert_close(out.double().numpy(), lse.double().numpy(), o_ref, l_ref, dt, f"grouped {B}x{N}x{Hq}/{Hkv} {dt}")
+
+
 def test_tiny_workload_both_modes():
     w = inputs.TINY
     q, k, v = inputs.make_inputs(w)
@@ -87,7 +113,8 @@ def test_row_zero_is_v0():
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_rescale_path_one_hot(mode):
+@pytest.mark.parametrize("H", [2, 4])
+def test_rescale_path_one_hot(mode, H):
     # Energy only in the slowest pair (k = 63 with k + 64 = 127; theta = 1e4^(-126/128) ~ 1.2e-4),
     # q_i = (a, 0), k_j = (j/8, 0): the score a (j/8) cos((i-j) theta) / sqrt(d) rises with j by
     # more than 22 per key, so the softmax of row i is one-hot on j = i and the running max jumps
@@ -96,7 +123,7 @@ def test_rescale_path_one_hot(mode):
     # rounding of the rotated keys (j/8)(cos, sin)(j theta), which can shrink a neighbour's score gap
     # to ~11 and leak e^-11 ~ 2e-5 of its value (|v| < 5): atol 1e-4.  A missing or wrong rescale
     # would leave earlier tiles' values in O, errors of order one.
-    B, N, H, d = 1, 640, 2, 128
+    B, N, d = 1, 640, 128  # H query heads on one KV head
     q = torch.zeros((B, N, H, d), dtype=torch.float16)
     k = torch.zeros((B, N, 1, d), dtype=torch.float16)
     q[..., 63] = 2048.0
@@ -110,14 +137,15 @@ def test_rescale_path_one_hot(mode):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
-def test_running_max_jumps(mode, dt):
+@pytest.mark.parametrize("Hq", [4, 8])
+def test_running_max_jumps(mode, dt, Hq):
     # q_63 = 8 and k_63 = c_t on key tile t, in the pair with the slowest frequency (theta ~ 2.6e-6
     # at base 5e5, so cos((i-j) theta) ~ 1): every score of key tile t is shifted by about
     # 8 c_t / sqrt(128) nats, which is 1.02 c_t in log2 units, on top of the N(0,1) scores.  With
     # c = 0, 12, 30, 15, 36 a row's running max grows by ~12 at key tile 1 (kept: P reaches 2^12),
     # by ~18 at tile 2 (the tile is redone with its own max) and by ~6 at tile 4.  Every element is
     # compared with the oracle.
-    B, N, Hq, Hkv, d = 1, 640, 4, 2, 128
+    B, N, Hkv, d = 1, 640, 2, 128  # Hq = 4 or 8: groups of two or four
     q, k, v = draw(B, N, Hq, Hkv, d, dt, seed=21)
     c = torch.tensor([0.0, 12.0, 30.0, 15.0, 36.0]).repeat_interleave(128)[:N]
     q[..., 63] = 8.0
