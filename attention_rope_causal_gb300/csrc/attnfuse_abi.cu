@@ -320,12 +320,13 @@ attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnf
   (void)d;
   (void)dtype;
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0) return ATTNFUSE_FUSED;
-  // Measured on GB300 (bench.py --sweep): with 4:1 GQA, rotating K in a pass and Q on chip (split)
-  // is fastest at 8 of the 10 points in N in [2048, 16384] (pre-rotation at N = 8192, within 2%),
-  // fused slowest everywhere; with MHA d=64 fused ties pre-rotation at N = 2048 (N* ~ 2060) and
-  // pre-rotation wins above (split within 1% of it).
-  if (Hq / Hkv >= 2) return N >= 2048 ? ATTNFUSE_SPLIT : ATTNFUSE_FUSED;
-  return N >= 2064 ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
+  // Measured on GB300 (bench.py --sweep, N from 1024 to 16384 at 16384 tokens, bf16 and fp16): with
+  // 4:1 GQA, rotating K in a pass and Q on chip (split) is fastest at 12 of the 14 points (pre-rotation
+  // at N = 16384, within 0.4%) and fused is slowest everywhere; with MHA d = 64, fused is fastest at
+  // N = 1024 and 1536 and pre-rotation from N = 2048 (interpolated crossover N* = 1862 in bf16, 1865
+  // in fp16), split within 1% of pre-rotation.
+  if (Hq / Hkv >= 2) return N >= 1024 ? ATTNFUSE_SPLIT : ATTNFUSE_FUSED;
+  return N >= 1864 ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
 }
 
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype) {
