@@ -19,9 +19,9 @@
 // fp32 max and sum, P rounded to the input type), O += P V by MMAs (warp w: 8 d / 64 columns) with
 // the accumulators in registers.  It writes the unnormalised O, the running max (log2 units) and the
 // sum of its split.
-// attn_decode_combine_kernel: one warp per (batch, KV head, row) merges the splits (rescaling each
-// by 2^(m_s - m)) into out and lse; launched as a programmatic dependent of the first kernel, it
-// waits (griddepcontrol.wait) for that grid to complete before reading the partials.
+// attn_decode_combine_kernel: one CTA per (row, KV head, batch) merges the splits (rescaling each by
+// 2^(m_s - m)) into out and lse; launched as a programmatic dependent of the first kernel, it waits
+// (griddepcontrol.wait) for that grid to complete before reading the partials.
 // No spin-waits: the first kernel synchronises only with __syncthreads, so the second one's wait
 // ends when the first grid does.
 #include <cuda_runtime.h>
@@ -413,71 +413,92 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D)) attn_decode_k
   }
 }
 
-// One warp per (batch, KV head, row): m = max_s m_s, l = sum_s l_s 2^(m_s - m),
-// out = sum_s O_s 2^(m_s - m) / l, lse = ln 2 (m + log2 l).  The lanes read the splits' (m, l)
-// pairs in parallel and pass each split's weight to the others by shuffle, so the O loads of
-// consecutive splits are independent and overlap.
+// One CTA of 256 threads per (row, KV head, batch): m = max_s m_s, w_s = 2^(m_s - m),
+// l = sum_s l_s w_s, out = sum_s O_s w_s / l, lse = ln 2 (m + log2 l).  The splits' (m, l) pairs
+// are read in one pass by as many threads, the weights go to shared memory, and each of the 8 warps
+// sums the O rows of every 8th split (lane = 4 or 2 consecutive columns) with loads that do not
+// depend on one another; a shared-memory pass adds the 8 warps' sums.  Two rounds of loads in all,
+// whatever the number of splits.
+constexpr int kCombineThreads = 256;
+constexpr int kMaxSplits = 1024;  // decode_plan never makes more
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) attn_decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kCombineThreads) attn_decode_combine_kernel(const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  const int g = p.Hq / p.Hkv, rows = g * p.N;
-  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
-  if (w >= (long long)p.B * p.Hkv * rows) return;
-  const int row = (int)(w % rows);
-  const int hk = (int)((w / rows) % p.Hkv);
-  const int b = (int)(w / ((long long)rows * p.Hkv));
+  constexpr int NW = kCombineThreads / 32;
+  constexpr int PER = D / 32;  // columns per lane
+  __shared__ float s_w[kMaxSplits];
+  __shared__ float s_red[NW][D];
+  __shared__ float s_part[2][NW];
+  const int row = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int g = p.Hq / p.Hkv;
   const int hl = row / p.N, i = row % p.N, h = hk * g + hl;
   const size_t base = ((size_t)b * p.Hkv + hk) * p.n_splits * kDecodeMaxRows + row;
   const int S = p.n_splits;
   ptx::grid_dep_wait();  // the partials of every split are complete and visible
-  float m = -INFINITY;
-  for (int s = lane; s < S; s += 32) m = fmaxf(m, p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2]);
+  // (m, l) of this thread's splits; a split with no visible key of this row has m = -inf (weight 0)
+  float m_loc = -INFINITY;
+  for (int s = tid; s < S; s += kCombineThreads) {
+    const float ms = p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2];
+    s_w[s] = ms;
+    m_loc = fmaxf(m_loc, ms);
+  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  constexpr int PER = D / 32;  // columns per lane
+  for (int off = 16; off > 0; off >>= 1) m_loc = fmaxf(m_loc, __shfl_xor_sync(0xFFFFFFFFu, m_loc, off));
+  if (lane == 0) s_part[0][warp] = m_loc;
+  __syncthreads();
+  float m = s_part[0][0];
+#pragma unroll
+  for (int k = 1; k < NW; ++k) m = fmaxf(m, s_part[0][k]);
+  float l_loc = 0.f;
+  for (int s = tid; s < S; s += kCombineThreads) {
+    const float ms = s_w[s];
+    const float wgt = ms == -INFINITY ? 0.f : ptx::ex2_approx(ms - m);
+    s_w[s] = wgt;
+    if (wgt != 0.f) l_loc = fmaf(p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2 + 1], wgt, l_loc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l_loc += __shfl_xor_sync(0xFFFFFFFFu, l_loc, off);
+  if (lane == 0) s_part[1][warp] = l_loc;
+  __syncthreads();
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float l = 0.f;
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    float wgt = 0.f;  // 0 for a split with no visible key of this row (its O is 0 too)
-    if (s0 + lane < S) {
-      const size_t slot = base + (size_t)(s0 + lane) * kDecodeMaxRows;
-      const float ms = p.part_ml[slot * 2];
-      if (ms != -INFINITY) {
-        wgt = ptx::ex2_approx(ms - m);
-        l = fmaf(p.part_ml[slot * 2 + 1], wgt, l);
-      }
-    }
-    const int cnt = min(32, S - s0);
 #pragma unroll 4
-    for (int u = 0; u < cnt; ++u) {
-      const float wu = __shfl_sync(0xFFFFFFFFu, wgt, u);
-      const float* o = p.part_o + (base + (size_t)(s0 + u) * kDecodeMaxRows) * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(o);
-        acc[0] = fmaf(v.x, wu, acc[0]);
-        acc[1] = fmaf(v.y, wu, acc[1]);
-        acc[2] = fmaf(v.z, wu, acc[2]);
-        acc[3] = fmaf(v.w, wu, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(o);
-        acc[0] = fmaf(v.x, wu, acc[0]);
-        acc[1] = fmaf(v.y, wu, acc[1]);
-      }
+  for (int s = warp; s < S; s += NW) {
+    const float wu = s_w[s];
+    const float* o = p.part_o + (base + (size_t)s * kDecodeMaxRows) * D + lane * PER;
+    if constexpr (PER == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(o);
+      acc[0] = fmaf(v.x, wu, acc[0]);
+      acc[1] = fmaf(v.y, wu, acc[1]);
+      acc[2] = fmaf(v.z, wu, acc[2]);
+      acc[3] = fmaf(v.w, wu, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(o);
+      acc[0] = fmaf(v.x, wu, acc[0]);
+      acc[1] = fmaf(v.y, wu, acc[1]);
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
-  const float inv = 1.f / l;
-  T* dst = reinterpret_cast<T*>(p.out) + (((size_t)b * p.N + i) * p.Hq + h) * D + lane * PER;
+  for (int e = 0; e < PER; ++e) s_red[warp][lane * PER + e] = acc[e];
+  __syncthreads();
+  if (tid < D / 2) {
+    float l = 0.f;
 #pragma unroll
-  for (int e = 0; e < PER; e += 2) {
-    const uint32_t wv = Pack<BF16>::pack(acc[e] * inv, acc[e + 1] * inv);
-    *reinterpret_cast<uint32_t*>(dst + e) = wv;
+    for (int k = 0; k < NW; ++k) l += s_part[1][k];
+    const float inv = 1.f / l;
+    float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      x0 += s_red[k][2 * tid];
+      x1 += s_red[k][2 * tid + 1];
+    }
+    T* dst = reinterpret_cast<T*>(p.out) + (((size_t)b * p.N + i) * p.Hq + h) * D + 2 * tid;
+    *reinterpret_cast<uint32_t*>(dst) = Pack<BF16>::pack(x0 * inv, x1 * inv);
+    if (tid == 0 && p.lse != nullptr) p.lse[((size_t)b * p.Hq + h) * p.N + i] = (m + log2f(l)) * kLn2;
   }
-  if (lane == 0 && p.lse != nullptr) p.lse[((size_t)b * p.Hq + h) * p.N + i] = (m + log2f(l)) * kLn2;
 }
 
 template <int D, bool BF16>
@@ -496,12 +517,11 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
                                 DecCfg<D>::SMEM, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long warps = (long long)p.B * p.Hkv * (p.Hq / p.Hkv) * p.N;
-  const long long blocks = (warps * 32 + 255) / 256;
+  if (p.n_splits > kMaxSplits) return cudaErrorInvalidConfiguration;
   // Programmatic dependent launch: the combine grid's launch overlaps the decode grid's tail.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((unsigned)((p.Hq / p.Hkv) * p.N), (unsigned)p.Hkv, (unsigned)p.B);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
