@@ -9,21 +9,24 @@
 // ("AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraphs 1-2: RoPE on Q
 // and K before the product, causal mask, softmax).
 //
-// attn_decode_kernel: one CTA per (KV head, split of keys_per_split keys, batch), 256 threads, two
-// (d = 128) or three (d = 64) CTAs per SM.  The CTA rotates its query rows once (exact cos/sin per row) into fp32 shared
-// memory, then walks its keys 64 at a time: the next chunk's K and V rows are loaded into registers
-// (16-byte loads) while the current chunk is processed; K is rotated in shared memory by cos/sin
-// carried from chunk to chunk (advanced by the exact rotation of 64 positions, recomputed exactly
-// every 16 chunks; exact per key with explicit positions) and rounded to the input type like the
-// other paths; S = Q K^T by m16n8k16 MMAs (warp w: keys 8w .. 8w + 7), online softmax per row (exp2,
-// fp32 max and sum, P rounded to the input type), O += P V by MMAs (warp w: 8 d / 64 columns) with
-// the accumulators in registers.  It writes the unnormalised O, the running max (log2 units) and the
-// sum of its split.
-// attn_decode_combine_kernel: one CTA per (row, KV head, batch) merges the splits (rescaling each by
+// attn_decode_kernel: one CTA per (KV head, slice of keys_per_split keys, batch), eight warps that
+// never wait on one another inside the key loop.  The slice is cut into 16-key chunks; warp w takes
+// chunks w, w + 8, w + 16, ... and owns a ring of three shared-memory stages, each holding one chunk's
+// K and V rows, filled by TMA (cp.async.bulk.tensor, 128-byte swizzle) on the warp's own mbarriers,
+// so up to three chunks per warp are in flight while it computes.  Per chunk the warp rotates the
+// chunk's K rows in place (cos/sin carried along the warp's rows and chunks by angle addition,
+// exact again every 16 chunks; exact per key with explicit positions; rounded to the input type
+// like the other paths), computes S = Q K^T for the <= 16 query rows as m16n8k16 tensor-core tiles
+// (Q fragments kept in registers), runs the online softmax on the fragments in registers (exp2,
+// fp32 max and sum), and adds P V with P passed straight from the score fragments to the operand
+// fragments (P rounded to the input type).  At the end the four warps' partial (O, max, sum) are
+// merged in shared memory and the CTA writes the slice's partial.  Eight warps of one CTA per SM at
+// d = 128 (two CTAs at d = 64) keep 16 chunks per SM in flight while eight warps compute.
+// attn_decode_combine_kernel: one CTA per (row, KV head, batch) merges the slices (rescaling each by
 // 2^(m_s - m)) into out and lse; launched as a programmatic dependent of the first kernel, it waits
 // (griddepcontrol.wait) for that grid to complete before reading the partials.
-// No spin-waits: the first kernel synchronises only with __syncthreads, so the second one's wait
-// ends when the first grid does.
+// Every mbarrier wait is bounded (1 s): a warp that gives up records bit 0 in the decode status word
+// (attnfuse_device_status), stops, and lets its copies in flight land before the CTA exits.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -35,52 +38,45 @@
 
 namespace attnfuse {
 
+__device__ unsigned int g_decode_status = 0;
+
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kChunk = 64;  // keys per step
+constexpr int kWarps = kDecodeWarps;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kChunk = kDecodeChunk;  // keys per chunk (one TMA box of rows)
+constexpr int kTiles = kChunk / 8;    // 8-key score tiles per chunk
+constexpr int kKSteps = kChunk / 16;  // 16-key steps of P V per chunk
+constexpr int kStagesPerWarp = 3;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned long long kWaitNs = 1000000000ull;
 
 template <int D>
 struct DecCfg {
-  // 16-bit elements per row of the Q, K and V tiles in shared memory: consecutive rows 16 bytes apart
-  // modulo 128, so the eight row addresses of an ldmatrix fall in distinct banks.
-  static constexpr int KSTRIDE = D + 8;
-  static constexpr int PSTRIDE = kChunk + 8;  // the same for P
-  static constexpr uint32_t OFF_Q = 0;                                          // fp32 [16][D]
-  static constexpr uint32_t OFF_QH = OFF_Q + kDecodeMaxRows * D * 4;            // 16-bit [16][KSTRIDE]
-  static constexpr uint32_t OFF_K = OFF_QH + kDecodeMaxRows * KSTRIDE * 2;      // 16-bit [64][KSTRIDE]
-  static constexpr uint32_t OFF_V = OFF_K + kChunk * KSTRIDE * 2;               // 16-bit [64][KSTRIDE]
-  static constexpr int SSTRIDE = kChunk + 8;  // fp32 scores per row: the eight rows of an MMA
-                                              // fragment's store fall in distinct banks
-  static constexpr uint32_t OFF_S = OFF_V + kChunk * KSTRIDE * 2;               // fp32 [16][SSTRIDE]
-  static constexpr uint32_t OFF_P = OFF_S + kDecodeMaxRows * SSTRIDE * 4;       // 16-bit [16][PSTRIDE]
-  static constexpr uint32_t OFF_ROW = OFF_P + kDecodeMaxRows * PSTRIDE * 2;     // fp32 [16] m, l, alpha
-  static constexpr uint32_t OFF_FREQ = OFF_ROW + 3 * kDecodeMaxRows * 4;        // u32 F_k lo[64], hi[64]
-  static constexpr uint32_t OFF_STEP = OFF_FREQ + 2 * 64 * 4;                   // u64 c[4][8], s[4][8]
-  static constexpr uint32_t SMEM = OFF_STEP + 8 * sizeof(RopeCS8);
-  static_assert(OFF_QH % 16 == 0 && OFF_K % 16 == 0 && OFF_V % 16 == 0 && OFF_P % 16 == 0 && OFF_STEP % 16 == 0,
-                "ldmatrix rows and 16-byte stores need 16-byte aligned regions");
+  static constexpr uint32_t BOX = kChunk * 128;                 // kChunk rows x 64 16-bit columns, swizzled
+  static constexpr uint32_t KBYTES = (D / 64) * BOX;            // one chunk of K (or V)
+  static constexpr uint32_t STAGE = 2 * KBYTES;                 // K then V
+  static constexpr int QSTRIDE = D + 8;                         // 16-bit Q rows, padded for ldmatrix
+  static constexpr int GPR = D / 16;                            // rotation groups (8 frequencies) per row
+  static constexpr int RS = 32 / GPR;                           // rows a warp rotates per pass
+  static constexpr int PASSES = kChunk / RS;
+  static constexpr uint32_t OFF_RING = 0;
+  static constexpr uint32_t OFF_QF = OFF_RING + kWarps * kStagesPerWarp * STAGE;  // fp32 [16][D]
+  static constexpr uint32_t OFF_QH = OFF_QF + kDecodeMaxRows * D * 4;             // 16-bit [16][QSTRIDE]
+  static constexpr uint32_t OFF_FREQ = OFF_QH + kDecodeMaxRows * QSTRIDE * 2;     // u32 lo[64], hi[64]
+  static constexpr uint32_t OFF_STEP = OFF_FREQ + 2 * 64 * 4;                     // RopeCS8 [GPR]: RS rows
+  static constexpr uint32_t OFF_SKIP = OFF_STEP + GPR * sizeof(RopeCS8);          // RopeCS8 [GPR]: next chunk
+  static constexpr uint32_t OFF_BAR = OFF_SKIP + GPR * sizeof(RopeCS8);           // u64 [warps][stages]
+  static constexpr uint32_t SMEM = OFF_BAR + kWarps * kStagesPerWarp * 8 + 1024;  // + alignment slack
+  // The warps' partials are merged in the ring after the key loop: O [warps][16][D] and m, l.
+  static_assert(kWarps * kDecodeMaxRows * (D + 2) * 4 <= kWarps * kStagesPerWarp * STAGE, "merge area");
+  static_assert(OFF_QH % 16 == 0 && OFF_STEP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 };
 
-// Offsets, inside a head vector, of the 8 rotation pairs of frequency group fg (frequencies
-// 8 fg .. 8 fg + 7): pair t is (a[t], b[t]).  Half-split over the rotary dimension r: (8 fg + t,
-// r/2 + 8 fg + t); interleaved: (16 fg + 2t, 16 fg + 2t + 1).
-__device__ __forceinline__ void pair_index(int fg, int t, int r, bool interleaved, int& ia, int& ib) {
-  if (interleaved) {
-    ia = 16 * fg + 2 * t;
-    ib = ia + 1;
-  } else {
-    ia = 8 * fg + t;
-    ib = r / 2 + ia;
-  }
-}
-
-// Warp-level tensor-core products for the (<= 16)-row tiles: ldmatrix fragments and the
-// m16n8k16 MMA (fp32 accumulators).  tcgen05's smallest M (64) would leave three quarters of
-// every product empty here.
-__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+// 16-byte chunk `ci` (columns 8 ci .. 8 ci + 7) of row r of a chunk of kChunk rows stored as 128-byte
+// swizzled boxes of 64 columns: box ci / 8, logical chunk ci % 8 at physical chunk (ci % 8) ^ (r % 8).
+__device__ __forceinline__ uint32_t sw_off(int r, int ci) {
+  return (uint32_t)(ci >> 3) * (uint32_t)(kChunk * 128) + (uint32_t)r * 128u + (uint32_t)((((ci & 7) ^ (r & 7))) * 16);
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -97,14 +93,7 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t (&r)[2]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(addr)
-               : "memory");
-}
-
-// c += a b: a the 16x16 row-major fragment, (b0, b1) the 16x8 column-major fragment.
+// c += a b: a the 16x16 row-major fragment, (b0, b1) the 16x8 column-major fragment (fp32 accumulate).
 template <bool BF16>
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   if constexpr (BF16) {
@@ -122,68 +111,85 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
   }
 }
 
+// Bounded wait on a TMA barrier; false (and bit 0 of the decode status word) if it ran out.
+__device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(&g_decode_status, 1u);
+      return false;
+    }
+  }
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D)) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
+    attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   using C = DecCfg<D>;
-  constexpr int KS = C::KSTRIDE;
-  constexpr int NT = D / 64;  // 8-column output tiles per warp in P V (8 warps cover d columns)
-  extern __shared__ __align__(16) uint8_t smem[];
-  float* sQ = reinterpret_cast<float*>(smem + C::OFF_Q);
-  T* sQh = reinterpret_cast<T*>(smem + C::OFF_QH);
-  T* sK = reinterpret_cast<T*>(smem + C::OFF_K);
-  T* sV = reinterpret_cast<T*>(smem + C::OFF_V);
-  float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
-  T* sP = reinterpret_cast<T*>(smem + C::OFF_P);
-  float* sM = reinterpret_cast<float*>(smem + C::OFF_ROW);
-  float* sL = sM + kDecodeMaxRows;
-  float* sA = sL + kDecodeMaxRows;
-  uint32_t* sF = reinterpret_cast<uint32_t*>(smem + C::OFF_FREQ);  // lo[64] then hi[64]
-  // cos/sin of 64 positions per frequency group, field-major ([j][group]) so that the lanes of a
-  // warp, which hold consecutive groups, read consecutive words
-  uint64_t* sStepC = reinterpret_cast<uint64_t*>(smem + C::OFF_STEP);
-  uint64_t* sStepS = sStepC + 4 * 8;
+  constexpr int NT = D / 8;    // 8-column output tiles of P V
+  constexpr int KS = D / 16;   // k-steps of Q K^T
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle: 1024-byte aligned boxes
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  float* sQ = reinterpret_cast<float*>(sgen + C::OFF_QF);
+  T* sQh = reinterpret_cast<T*>(sgen + C::OFF_QH);
+  uint32_t* sF = reinterpret_cast<uint32_t*>(sgen + C::OFF_FREQ);  // lo[64] then hi[64]
+  RopeCS8* sStep = reinterpret_cast<RopeCS8*>(sgen + C::OFF_STEP);
+  RopeCS8* sSkip = reinterpret_cast<RopeCS8*>(sgen + C::OFF_SKIP);
+  uint64_t* sBar = reinterpret_cast<uint64_t*>(sgen + C::OFF_BAR);
 
-  // KV head fastest: CTAs launched together read the same key rows of all heads (whole DRAM pages)
   const int hk = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int g8 = lane / 4, t4 = lane % 4;  // MMA fragment row and column-pair of this lane
-  // the combine kernel may launch now; it waits for this grid's completion before reading
-  ptx::grid_dep_launch_dependents();
+  const int g8 = lane / 4, t4 = lane % 4;  // MMA fragment row and column pair of this lane
   const int g = p.Hq / p.Hkv;
   const int rows = g * p.N;  // row = local head * N + query index
-  const int r = 2 * p.rot_chunks * 8;  // rotary dimension
+  const int R = p.rot_chunks;  // rotation groups actually rotated (rotary dimension / 16)
   const bool il = p.interleaved != 0;
   const int key0 = split * p.keys_per_split;
   const int key_end = min(p.Nk, key0 + p.keys_per_split);
+  const int nch = (key_end - key0 + kChunk - 1) / kChunk;
+  const bool skip_all = *reinterpret_cast<volatile unsigned int*>(&g_decode_status) != 0u;
 
-  // K and V rows of a chunk: warp w loads rows 8w .. 8w + 7 (LPT 16-byte pieces per lane, 16 or 8
-  // lanes per row), all loads issued before any is used; the next chunk's are in flight while the
-  // current one is computed on, the first chunk's while the query rows are prepared.
-  constexpr int LPT = D / 32;  // 4 (d = 128) or 2 (d = 64)
-  uint4 kpre[LPT], vpre[LPT];
-  auto piece = [&](int n, int& kr, int& c8) {
-    const int local = 32 * n + lane;
-    kr = 8 * warp + local / (D / 8);
-    c8 = local % (D / 8);
-  };
-  auto load_chunk = [&](int kc) {
+  if (tid == 0) {
+    for (int i = 0; i < kWarps * kStagesPerWarp; ++i) ptx::mbar_init(ptx::smem_u32(sBar + i), 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  ptx::grid_dep_launch_dependents();  // the combine kernel may launch; it waits for this grid
+
+  // Each warp's first chunks are requested before anything else happens.
+  auto stage_addr = [&](int st) { return sbase + C::OFF_RING + (uint32_t)(warp * kStagesPerWarp + st) * C::STAGE; };
+  auto issue = [&](int c, int st) {
+    const uint32_t bar = ptx::smem_u32(sBar + warp * kStagesPerWarp + st);
+    const uint32_t dst = stage_addr(st);
+    ptx::mbar_arrive_expect_tx(bar, C::STAGE);
+    const int row0 = key0 + kChunk * c;
 #pragma unroll
-    for (int n = 0; n < LPT; ++n) {
-      int kr, c8;
-      piece(n, kr, c8);
-      const int j = kc + kr;
-      kpre[n] = vpre[n] = make_uint4(0, 0, 0, 0);  // zero past the split or the sequence
-      if (j < key_end) {
-        const size_t off = (((size_t)b * p.Nk + j) * p.Hkv + hk) * D + 8 * c8;
-        kpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k) + off));
-        vpre[n] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v) + off));
-      }
+    for (int bx = 0; bx < D / 64; ++bx) {
+      ptx::tma_load_4d(dst + bx * C::BOX, &tmK, bar, 64 * bx, hk, row0, b);
+      ptx::tma_load_4d(dst + C::KBYTES + bx * C::BOX, &tmV, bar, 64 * bx, hk, row0, b);
     }
   };
-  if (key0 < key_end) load_chunk(key0);
+  int issued = 0;  // chunks of this warp requested so far (the warp's chunks are warp + kWarps i)
+  if (!skip_all && lane == 0) {
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+  }
+  if (!skip_all) {
+    for (int st = 0; st < kStagesPerWarp; ++st) {
+      const int c = warp + kWarps * st;
+      if (c >= nch) break;
+      if (lane == 0) issue(c, st);
+      ++issued;
+    }
+  }
 
-  // ---- query rows into fp32 shared memory; row state; P's padding rows stay zero ----------------
+  // ---- query rows: fp32 in shared memory, rotated exactly per row, rounded once, 16-bit copy ------
   for (int idx = tid; idx < rows * (D / 8); idx += kThreads) {
     const int row = idx / (D / 8), c8 = idx % (D / 8);
     const int hl = row / p.N, i = row % p.N;
@@ -198,218 +204,226 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D)) attn_decode_k
       sQ[row * D + 8 * c8 + 2 * e + 1] = hi;
     }
   }
-  if (tid < kDecodeMaxRows) {
-    sM[tid] = -INFINITY;
-    sL[tid] = 0.f;
-    sA[tid] = 0.f;
-  }
-  for (int idx = tid; idx < kDecodeMaxRows * C::PSTRIDE / 2; idx += kThreads) reinterpret_cast<uint32_t*>(sP)[idx] = 0u;
-  // F_k in shared memory: per-lane frequency indices would serialise constant-bank loads.
   if (tid < 64) sF[tid] = p.freqs.lo[tid];
   else if (tid < 128) sF[tid] = p.freqs.hi[tid - 64];
   __syncthreads();
-  // ---- rotate the query rows (exact cos/sin per row), rounded to the input type once --------------
-  for (int idx = tid; idx < rows * p.rot_chunks; idx += kThreads) {
-    const int row = idx / p.rot_chunks, fg = idx % p.rot_chunks;
+  const int r = 2 * R * 8;  // rotary dimension
+  for (int idx = tid; idx < rows * R; idx += kThreads) {
+    const int row = idx / R, fg = idx % R;
     const int i = row % p.N;
     const int32_t pos = p.qpos ? p.qpos[(size_t)b * p.N + i] : p.q_off + i;
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      float c, s;
-      rope_cs_signed(pos, sF[8 * fg + t], sF[64 + 8 * fg + t], c, s);
-      int ia, ib;
-      pair_index(fg, t, r, il, ia, ib);
-      const float x = sQ[row * D + ia], y = sQ[row * D + ib];
+      float c, s_;
+      rope_cs_signed(pos, sF[8 * fg + t], sF[64 + 8 * fg + t], c, s_);
+      const int ia = il ? 16 * fg + 2 * t : 8 * fg + t;
+      const int ib = il ? ia + 1 : r / 2 + ia;
       float xr, yr;
-      rope_pair(x, y, c, s, xr, yr);
+      rope_pair(sQ[row * D + ia], sQ[row * D + ib], c, s_, xr, yr);
       float2 rr;
       Pack<BF16>::unpack(Pack<BF16>::pack(xr, yr), rr.x, rr.y);
       sQ[row * D + ia] = rr.x;
       sQ[row * D + ib] = rr.y;
     }
   }
-  if (tid < p.rot_chunks) {
-    RopeCS8 st;
-    rope_cs8_exact((uint32_t)kChunk, sF, sF + 64, 8 * tid, st);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      sStepC[8 * j + tid] = st.c[j];
-      sStepS[8 * j + tid] = st.s[j];
-    }
-  }
+  // cos/sin steps of a rotation group: RS rows (between a lane's passes) and kChunk (kWarps - 1) + RS
+  // rows (from a lane's last row of one chunk to its first row of the warp's next chunk)
+  if (tid < R) rope_cs8_exact((uint32_t)C::RS, sF, sF + 64, 8 * tid, sStep[tid]);
+  else if (tid >= 64 && tid < 64 + R)
+    rope_cs8_exact((uint32_t)(kChunk * (kWarps - 1) + C::RS), sF, sF + 64, 8 * (tid - 64), sSkip[tid - 64]);
   __syncthreads();
-  // 16-bit copy for the MMA (exact: every entry is a value of the input type); rows >= rows zero.
   for (int idx = tid; idx < kDecodeMaxRows * (D / 2); idx += kThreads) {
     const int row = idx / (D / 2), e = 2 * (idx % (D / 2));
     const uint32_t w = row < rows ? Pack<BF16>::pack(sQ[row * D + e], sQ[row * D + e + 1]) : 0u;
-    *reinterpret_cast<uint32_t*>(sQh + row * KS + e) = w;
+    *reinterpret_cast<uint32_t*>(sQh + row * C::QSTRIDE + e) = w;
   }
-  // (read by every warp as A fragments in each chunk's score product: sQh is stable from here on)
+  __syncthreads();
+  // Q as A fragments, one per k-step (16 columns), for the whole key loop
+  uint32_t qa[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+    ldsm_x4(ptx::smem_u32(sQh + (lane % 16) * C::QSTRIDE + 16 * ks + 8 * (lane / 16)), qa[ks]);
 
-  // O accumulators of this warp: rows g8 and g8 + 8, columns n0 + 8 nt + 2 t4 (+1).
-  const int n0 = warp * 8 * NT;
+  // Per lane: rows g8 and g8 + 8 of the fragments; last visible key of each (-1: a padding row).
+  int lim[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int row = g8 + 8 * h;
+    lim[h] = row < rows ? min(key_end - 1, p.q_off + row % p.N) : -1;
+  }
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float o[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-  // cos/sin of the thread's key-rotation items (see below); their advance by 64 positions is shared
-  // per frequency group (sStepC, sStepS).
-  constexpr int KIT = D / 64;  // rotation items per lane: 8 keys x at most D/16 groups per warp
-  RopeCS8 kcs[KIT];
-
-  for (int kc = key0; kc < key_end; kc += kChunk) {
-    __syncthreads();  // every warp is done with the previous chunk's V and P
-    // Warp w owns K rows 8w .. 8w + 7 from the store through the rotation to the score product, so
-    // only V (read by every warp) needs the CTA-wide barriers.
+  // Key rotation items of this lane: rotation group fg, rows rsub + RS pass of each chunk.
+  const int fg = lane % C::GPR, rsub = lane / C::GPR;
+  const bool rot_lane = fg < R;
+  const int ca = il ? 2 * fg : fg, cb = il ? 2 * fg + 1 : fg + R;
+  RopeCS8 kcs, step;
+  if (rot_lane) step = sStep[fg];
+  bool ok = !skip_all;
+  int done = 0;  // chunks of this warp consumed
+  for (int c = warp; ok && c < nch; c += kWarps, ++done) {
+    const int st = done % kStagesPerWarp;
+    if (!(ok = __all_sync(0xFFFFFFFFu, wait_stage(ptx::smem_u32(sBar + warp * kStagesPerWarp + st),
+                                                   (uint32_t)((done / kStagesPerWarp) & 1)))))
+      break;
+    const uint32_t kst = stage_addr(st), vst = kst + C::KBYTES;
+    const int j0 = key0 + kChunk * c;
+    // ---- rotate this chunk's K rows in place ------------------------------------------------------
+    if (rot_lane) {
+      if (p.kpos == nullptr && done % 16 == 0)
+        rope_cs8_exact((uint32_t)(j0 + rsub), sF, sF + 64, 8 * fg, kcs);
 #pragma unroll
-    for (int n = 0; n < LPT; ++n) {
-      int kr, c8;
-      piece(n, kr, c8);
-      *reinterpret_cast<uint4*>(sK + kr * KS + 8 * c8) = kpre[n];
-      *reinterpret_cast<uint4*>(sV + kr * KS + 8 * c8) = vpre[n];
-    }
-    if (kc + kChunk < key_end) load_chunk(kc + kChunk);
-    __syncwarp();
-    // ---- rotate the warp's keys in place -------------------------------------------------------
-    // Lane item n: key row kr, frequency group fg (8 frequencies, two 16-byte pieces).  Positions
-    // j: cos/sin carried from chunk to chunk by the exact rotation of 64 positions, exact again every
-    // 16 chunks; explicit positions: exact per key.
-#pragma unroll
-    for (int n = 0; n < KIT; ++n) {
-      const int local = 32 * n + lane;
-      if (local >= 8 * p.rot_chunks) break;
-      const int kr = 8 * warp + local / p.rot_chunks, fg = local % p.rot_chunks;
-      const int j = kc + kr;
-      if (p.kpos != nullptr) {
-        if (j < key_end) rope_cs8_exact_signed(p.kpos[(size_t)b * p.Nk + j], sF, sF + 64, 8 * fg, kcs[n]);
-      } else if (((kc - key0) / kChunk) % 16 == 0) {
-        rope_cs8_exact((uint32_t)j, sF, sF + 64, 8 * fg, kcs[n]);
-      }
-      if (j < key_end) {
-        T* row = sK + kr * KS;
+      for (int pass = 0; pass < C::PASSES; ++pass) {
+        const int row = rsub + C::RS * pass;
+        const int j = j0 + row;
+        if (p.kpos != nullptr) {
+          const int jc = min(j, p.Nk - 1);  // rows past the sequence hold zeros: any angle will do
+          rope_cs8_exact_signed(p.kpos[(size_t)b * p.Nk + jc], sF, sF + 64, 8 * fg, kcs);
+        }
+        const uint32_t xo = sw_off(row, ca), yo = sw_off(row, cb);
+        uint4 x = ptx::lds128(kst + xo), y = ptx::lds128(kst + yo);
         if (il) {
-          uint4* a = reinterpret_cast<uint4*>(row + 16 * fg);
-          uint4 x = a[0], y = a[1];
-          rope_rotate_chunk_il_cs8<BF16>(x, kcs[n], 0);
-          rope_rotate_chunk_il_cs8<BF16>(y, kcs[n], 1);
-          a[0] = x;
-          a[1] = y;
+          rope_rotate_chunk_il_cs8<BF16>(x, kcs, 0);
+          rope_rotate_chunk_il_cs8<BF16>(y, kcs, 1);
         } else {
-          uint4* xa = reinterpret_cast<uint4*>(row + 8 * fg);
-          uint4* ya = reinterpret_cast<uint4*>(row + r / 2 + 8 * fg);
-          uint4 x = *xa, y = *ya;
-          rope_rotate_chunk_cs8<BF16>(x, y, kcs[n]);
-          *xa = x;
-          *ya = y;
+          rope_rotate_chunk_cs8<BF16>(x, y, kcs);
         }
-      }
-      if (p.kpos == nullptr) {
-        RopeCS8 st;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          st.c[jj] = sStepC[8 * jj + fg];
-          st.s[jj] = sStepS[8 * jj + fg];
-        }
-        rope_cs8_advance(kcs[n], st);
+        ptx::sts128(kst + xo, x);
+        ptx::sts128(kst + yo, y);
+        if (p.kpos == nullptr) rope_cs8_advance(kcs, pass + 1 < C::PASSES ? step : sSkip[fg]);
       }
     }
     __syncwarp();
-    // ---- scores (log2 units) S = Q K^T: warp w takes keys 8w .. 8w + 7 -------------------------
-    {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S = Q K^T (log2 units): kTiles tiles of 8 keys -------------------------------------------
+    float sc[kTiles][4];
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ks += 2) {
-        uint32_t qa0[4], qa1[4], bk[4];  // query k-steps ks, ks + 1; the keys' 16x8 fragments of both
-        ldsm_x4(smem_u32(sQh + (lane % 16) * KS + 16 * ks + 8 * (lane / 16)), qa0);
-        ldsm_x4(smem_u32(sQh + (lane % 16) * KS + 16 * (ks + 1) + 8 * (lane / 16)), qa1);
-        ldsm_x4(smem_u32(sK + (8 * warp + lane % 8) * KS + 16 * ks + 8 * (lane / 8)), bk);
-        mma_16816<BF16>(c, qa0, bk[0], bk[1]);
-        mma_16816<BF16>(c, qa1, bk[2], bk[3]);
-      }
+    for (int nt = 0; nt < kTiles; ++nt) {
+      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = g8 + 8 * h;
-        if (row < rows) {
-          const int i = row % p.N;
-          const int kr = 8 * warp + 2 * t4, j = kc + kr;
-          const int lim = min(key_end - 1, p.q_off + i);  // last visible key
-          *reinterpret_cast<float2*>(sS + row * C::SSTRIDE + kr) =
-              make_float2(j <= lim ? c[2 * h] * p.scale_log2 : -INFINITY,
-                          j + 1 <= lim ? c[2 * h + 1] * p.scale_log2 : -INFINITY);
-        }
+      for (int ks = 0; ks < KS; ks += 2) {
+        uint32_t bk[4];  // keys 8 nt .. 8 nt + 7, columns 16 ks .. 16 ks + 31
+        const int krow = 8 * nt + (lane % 8);
+        ldsm_x4(kst + sw_off(krow, 2 * ks + lane / 8), bk);
+        mma_16816<BF16>(sc[nt], qa[ks], bk[0], bk[1]);
+        mma_16816<BF16>(sc[nt], qa[ks + 1], bk[2], bk[3]);
       }
     }
-    __syncthreads();
-    // ---- online softmax per row: warp w takes rows w, w + 8 -----------------------------------
-    for (int row = warp; row < rows; row += kThreads / 32) {
-      const float s0 = sS[row * C::SSTRIDE + lane], s1 = sS[row * C::SSTRIDE + lane + 32];
-      float mx = fmaxf(s0, s1);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-      const float m_old = sM[row];
-      const float m_new = fmaxf(m_old, mx);
-      // a row that has seen no visible key yet keeps m = -inf, P = 0
-      const float p0 = m_new == -INFINITY ? 0.f : ptx::ex2_approx(s0 - m_new);
-      const float p1 = m_new == -INFINITY ? 0.f : ptx::ex2_approx(s1 - m_new);
-      float sum = p0 + p1;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-      // P rounded to the input type for the product, like the tile kernels
-      sP[row * C::PSTRIDE + lane] = static_cast<T>(p0);
-      sP[row * C::PSTRIDE + lane + 32] = static_cast<T>(p1);
-      if (lane == 0) {
-        const float alpha = m_old == -INFINITY ? 0.f : ptx::ex2_approx(m_old - m_new);
-        sA[row] = alpha;
-        sL[row] = sL[row] * alpha + sum;
-        sM[row] = m_new;
-      }
-    }
-    __syncthreads();
-    // ---- O = O alpha + P V: warp w takes columns n0 .. n0 + 8 NT - 1 ---------------------------
-    {
-      const float a_lo = sA[g8], a_hi = sA[g8 + 8];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        o[nt][0] *= a_lo;
-        o[nt][1] *= a_lo;
-        o[nt][2] *= a_hi;
-        o[nt][3] *= a_hi;
-      }
-#pragma unroll
-      for (int kk = 0; kk < kChunk / 16; ++kk) {
-        uint32_t pa[4];
-        ldsm_x4(smem_u32(sP + (lane % 16) * C::PSTRIDE + 16 * kk + 8 * (lane / 16)), pa);
-        const int mi = lane / 8;
-        if constexpr (NT == 2) {
-          uint32_t bv[4];  // keys 16 kk .. +15 of columns n0 .. n0 + 7 and n0 + 8 .. n0 + 15
-          ldsm_x4_trans(smem_u32(sV + (16 * kk + lane % 8 + 8 * (mi % 2)) * KS + n0 + 8 * (mi / 2)), bv);
-          mma_16816<BF16>(o[0], pa, bv[0], bv[1]);
-          mma_16816<BF16>(o[1], pa, bv[2], bv[3]);
-        } else {
-          uint32_t bv[2];
-          ldsm_x2_trans(smem_u32(sV + (16 * kk + lane % 8 + 8 * (mi % 2)) * KS + n0), bv);
-          mma_16816<BF16>(o[0], pa, bv[0], bv[1]);
-        }
-      }
-    }
-  }
-  // ---- partials of this split ------------------------------------------------------------------
-  const size_t base = (((size_t)b * p.Hkv + hk) * p.n_splits + split) * kDecodeMaxRows;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+    // ---- online softmax on the fragments: rows g8 (h = 0) and g8 + 8 (h = 1) ----------------------
+    uint32_t pa[kKSteps][4];  // P as the A fragments of the 16-key steps of P V
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int row = g8 + 8 * h;
-      if (row < rows) {
-        const int col = n0 + 8 * nt + 2 * t4;
-        *reinterpret_cast<float2*>(p.part_o + (base + row) * D + col) = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+      float sv[2 * kTiles];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < kTiles; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + 8 * nt + 2 * t4 + e;
+          const float v = j <= lim[h] ? sc[nt][2 * h + e] * p.scale_log2 : -INFINITY;
+          sv[2 * nt + e] = v;
+          mx = fmaxf(mx, v);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      const float m_new = fmaxf(m_run[h], mx);
+      // a row that has seen no visible key keeps m = -inf, P = 0, O = 0
+      const float alpha = m_run[h] == -INFINITY ? 0.f : ptx::ex2_approx(m_run[h] - m_new);
+      float pv[2 * kTiles], sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 2 * kTiles; ++e) {
+        pv[e] = m_new == -INFINITY ? 0.f : ptx::ex2_approx(sv[e] - m_new);
+        sum += pv[e];
+      }
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+      l_run[h] = l_run[h] * alpha + sum;
+      m_run[h] = m_new;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][2 * h] *= alpha;
+        o[nt][2 * h + 1] *= alpha;
+      }
+      // Score tiles 2 kk and 2 kk + 1 (keys 16 kk .. 16 kk + 15) form the A fragment of key step kk:
+      // a0 / a1 = tile 2 kk, rows g8 / g8 + 8; a2 / a3 = tile 2 kk + 1, rows g8 / g8 + 8.
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        pa[kk][h] = Pack<BF16>::pack(pv[4 * kk], pv[4 * kk + 1]);
+        pa[kk][2 + h] = Pack<BF16>::pack(pv[4 * kk + 2], pv[4 * kk + 3]);
       }
     }
+    // ---- O += P V: 16 keys per step, 16 columns per ldmatrix ------------------------------------
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; ++kk) {
+      const int vrow = 16 * kk + (lane % 8) + 8 * ((lane / 8) % 2);
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        uint32_t bv[4];  // keys 16 kk .. +15, columns 16 n2 .. +7 (bv[0..1]) and +8 .. +15 (bv[2..3])
+        ldsm_x4_trans(vst + sw_off(vrow, 2 * n2 + lane / 16), bv);
+        mma_16816<BF16>(o[2 * n2], pa[kk], bv[0], bv[1]);
+        mma_16816<BF16>(o[2 * n2 + 1], pa[kk], bv[2], bv[3]);
+      }
+    }
+    __syncwarp();
+    // ---- refill this stage with the warp's chunk kStagesPerWarp steps ahead ------------------------
+    const int cn = c + kWarps * kStagesPerWarp;
+    if (cn < nch) {
+      if (lane == 0) {
+        ptx::fence_proxy_async_smem();  // this warp's reads of the stage before TMA overwrites it
+        issue(cn, st);
+      }
+      ++issued;
+    }
   }
+  // Copies still in flight (only after a wait ran out) must land before shared memory is released.
+  if (lane == 0)
+    for (int k = done; k < issued; ++k) {
+      const uint32_t bar = ptx::smem_u32(sBar + warp * kStagesPerWarp + k % kStagesPerWarp);
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar, (uint32_t)((k / kStagesPerWarp) & 1)))
+        if (ptx::globaltimer_ns() - t0 > kWaitNs) break;
+    }
   __syncthreads();
-  if (tid < rows) {
-    p.part_ml[(base + tid) * 2] = sM[tid];
-    p.part_ml[(base + tid) * 2 + 1] = sL[tid];
+
+  // ---- merge the warps' partials in the ring, write this slice's (O, m, l) ----------------------
+  float* mO = reinterpret_cast<float*>(sgen + C::OFF_RING);     // [warps][16][D]
+  float* mM = mO + kWarps * kDecodeMaxRows * D;                 // [warps][16]
+  float* mL = mM + kWarps * kDecodeMaxRows;                     // [warps][16]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = g8 + 8 * h, col = 8 * nt + 2 * t4;
+      *reinterpret_cast<float2*>(mO + (warp * kDecodeMaxRows + row) * D + col) = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+    }
+  if (t4 == 0)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mM[warp * kDecodeMaxRows + g8 + 8 * h] = m_run[h];
+      mL[warp * kDecodeMaxRows + g8 + 8 * h] = l_run[h];
+    }
+  __syncthreads();
+  const size_t base = (((size_t)b * p.Hkv + hk) * p.n_splits + split) * kDecodeMaxRows;
+  for (int idx = tid; idx < rows * D; idx += kThreads) {
+    const int row = idx / D, col = idx % D;
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) m = fmaxf(m, mM[w * kDecodeMaxRows + row]);
+    float acc = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = mM[w * kDecodeMaxRows + row];
+      const float wt = mw == -INFINITY ? 0.f : ptx::ex2_approx(mw - m);
+      acc = fmaf(mO[(w * kDecodeMaxRows + row) * D + col], wt, acc);
+      l = fmaf(mL[w * kDecodeMaxRows + row], wt, l);
+    }
+    p.part_o[(base + row) * D + col] = acc;
+    if (col == 0) {
+      p.part_ml[(base + row) * 2] = m;
+      p.part_ml[(base + row) * 2 + 1] = l;
+    }
   }
 }
 
@@ -502,7 +516,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_decode_combine_kernel(co
 }
 
 template <int D, bool BF16>
-cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_impl(const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
   static DeviceOnce once;  // shared-memory attribute set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -514,7 +528,7 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
   }, &unused);
   if (e != cudaSuccess) return e;
   attn_decode_kernel<D, BF16><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(kThreads),
-                                DecCfg<D>::SMEM, stream>>>(p);
+                                DecCfg<D>::SMEM, stream>>>(maps.k, maps.v, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.n_splits > kMaxSplits) return cudaErrorInvalidConfiguration;
@@ -536,9 +550,20 @@ cudaError_t launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_attn_decode(const DecodeParams& p, int d, bool bf16, cudaStream_t stream) {
-  if (d == 128) return bf16 ? launch_decode_impl<128, true>(p, stream) : launch_decode_impl<128, false>(p, stream);
-  return bf16 ? launch_decode_impl<64, true>(p, stream) : launch_decode_impl<64, false>(p, stream);
+cudaError_t launch_attn_decode(const DecodeMaps& maps, const DecodeParams& p, int d, bool bf16, cudaStream_t stream) {
+  if (d == 128)
+    return bf16 ? launch_decode_impl<128, true>(maps, p, stream) : launch_decode_impl<128, false>(maps, p, stream);
+  return bf16 ? launch_decode_impl<64, true>(maps, p, stream) : launch_decode_impl<64, false>(maps, p, stream);
+}
+
+cudaError_t read_and_clear_decode_status(unsigned int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_decode_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  if (*value != 0u) {
+    const unsigned int zero = 0u;
+    e = cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(unsigned int));
+  }
+  return e;
 }
 
 }  // namespace attnfuse

@@ -137,13 +137,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // depends only on the address, the sizes and the dtype, so the last few encoded are kept per thread
 // (a repeated call then encodes nothing; no lock is taken).
 attnfuse_status_t encode_bnhd_uncached(CUtensorMap* map, const void* ptr, int B, int N, int H, int d,
-                                       attnfuse_dtype_t dtype, const char* name);
+                                       attnfuse_dtype_t dtype, int box_rows, const char* name);
 
+// box_rows: tokens per box (128 for the attention tiles, 32 for the decode kernel's key chunks).
 attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, int H, int d, attnfuse_dtype_t dtype,
-                              const char* name) {
+                              const char* name, int box_rows = 128) {
   struct Entry {
     const void* ptr;
-    int B, N, H, d;
+    int B, N, H, d, box_rows;
     attnfuse_dtype_t dtype;
     CUtensorMap map;
   };
@@ -152,26 +153,26 @@ attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, i
   thread_local int used = 0, next = 0;
   for (int i = 0; i < used; ++i) {
     const Entry& c = cache[i];
-    if (c.ptr == ptr && c.B == B && c.N == N && c.H == H && c.d == d && c.dtype == dtype) {
+    if (c.ptr == ptr && c.B == B && c.N == N && c.H == H && c.d == d && c.box_rows == box_rows && c.dtype == dtype) {
       *map = c.map;
       return ATTNFUSE_OK;
     }
   }
-  const attnfuse_status_t st = encode_bnhd_uncached(map, ptr, B, N, H, d, dtype, name);
+  const attnfuse_status_t st = encode_bnhd_uncached(map, ptr, B, N, H, d, dtype, box_rows, name);
   if (st != ATTNFUSE_OK) return st;
-  cache[next] = Entry{ptr, B, N, H, d, dtype, *map};
+  cache[next] = Entry{ptr, B, N, H, d, box_rows, dtype, *map};
   next = (next + 1) % kEntries;
   if (used < kEntries) ++used;
   return ATTNFUSE_OK;
 }
 
 attnfuse_status_t encode_bnhd_uncached(CUtensorMap* map, const void* ptr, int B, int N, int H, int d,
-                                       attnfuse_dtype_t dtype, const char* name) {
+                                       attnfuse_dtype_t dtype, int box_rows, const char* name) {
   auto fn = encode_fn();
   if (!fn) return fail(ATTNFUSE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)N * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, dtype == ATTNFUSE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -193,14 +194,15 @@ bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
   return rows <= kDecodeMaxRows && B <= 65535 && Hkv <= 65535;  // grid limits
 }
 
-// Splits of the keys, in 64-key chunks: the number of slices that minimises (waves of CTAs) x (chunks
-// per slice + a CTA's fixed work, about two chunks' time measured) with decode_ctas_per_sm(d) CTAs
-// resident per SM on 152 SMs, fewest slices among equals (each slice adds a partial to merge).  A
-// slice count rounded up past a whole wave would double the time.
+// Splits of the keys, in 32-key chunks: the number of slices that minimises (waves of CTAs) x
+// (chunks per warp of a slice + a CTA's fixed work, about three chunks' time) with
+// decode_ctas_per_sm(d) CTAs resident per SM on 152 SMs and kDecodeWarps warps per CTA, fewest
+// slices among equals (each slice adds a partial to merge).  A slice count rounded up past a whole
+// wave would double the time.
 void decode_plan(int B, int Hkv, int Nk, int d, int* keys_per_split, int* n_splits) {
   const long long kSlots = 152LL * decode_ctas_per_sm(d);
-  constexpr long long kFixedChunks = 2;
-  const int chunks = (Nk + 63) / 64;
+  constexpr long long kFixedChunks = 3;
+  const int chunks = (Nk + kDecodeChunk - 1) / kDecodeChunk;
   const long long heads = (long long)B * Hkv;
   long long best_cost = -1;
   int best_per = chunks;
@@ -209,13 +211,13 @@ void decode_plan(int B, int Hkv, int Nk, int d, int* keys_per_split, int* n_spli
     const int per = (chunks + s - 1) / s;
     const long long n = (chunks + per - 1) / per;  // slices actually needed
     const long long waves = (heads * n + kSlots - 1) / kSlots;
-    const long long cost = waves * (per + kFixedChunks);
+    const long long cost = waves * ((per + kDecodeWarps - 1) / kDecodeWarps + kFixedChunks);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_per = per;
     }
   }
-  *keys_per_split = 64 * best_per;
+  *keys_per_split = kDecodeChunk * best_per;
   *n_splits = (Nk + *keys_per_split - 1) / *keys_per_split;
 }
 
@@ -459,7 +461,13 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
     const size_t slots = (size_t)B * Hkv * dp.n_splits * kDecodeMaxRows;
     dp.part_o = static_cast<float*>(ws);
     dp.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(slots * d * sizeof(float), 256));
-    cudaError_t e = launch_attn_decode(dp, d, dtype == ATTNFUSE_BF16, s);
+    DecodeMaps dm;
+    if ((st = encode_bnhd(&dm.k, k, B, Nk, Hkv, d, dtype, "k", kDecodeChunk)) != ATTNFUSE_OK ||
+        (st = encode_bnhd(&dm.v, v, B, Nk, Hkv, d, dtype, "v", kDecodeChunk)) != ATTNFUSE_OK) {
+      if (owned) cudaFreeAsync(owned, s);
+      return st;
+    }
+    cudaError_t e = launch_attn_decode(dm, dp, d, dtype == ATTNFUSE_BF16, s);
     if (owned) cudaFreeAsync(owned, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ATTNFUSE_OK;
@@ -727,6 +735,10 @@ attnfuse_status_t attnfuse_device_status(void* stream) {
   e = read_and_clear_bwd_status(&vb);
   if (e != cudaSuccess) return cuda_fail(e, "device status (backward)");
   v |= vb;
+  unsigned int vd = 0;
+  e = read_and_clear_decode_status(&vd);
+  if (e != cudaSuccess) return cuda_fail(e, "device status (decode)");
+  v |= vd;
   if (v != 0u) return fail(ATTNFUSE_ERR_TIMEOUT, "a kernel barrier wait ran out (device status 0x%x)", v);
   return ATTNFUSE_OK;
 }

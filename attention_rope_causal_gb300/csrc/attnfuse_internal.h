@@ -110,10 +110,12 @@ cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bo
 
 constexpr int kDecodeMaxRows = 16;  // query rows per KV head: (Hq / Hkv) * N
 
-// Decode CTAs (256 threads) resident per SM: the kernel's register cap and the key-slice planner
-// both follow it.  d = 64 fits three (80 registers, no spills); d = 128 two (three would spill
-// the carried cos/sin).
-constexpr int decode_ctas_per_sm(int d) { return d == 64 ? 3 : 2; }
+// Decode CTAs (eight warps, each with a ring of three 16-key stages) resident per SM: the kernel's
+// launch bounds and the key-slice planner both follow it.  The rings take 192 KB of shared memory
+// at d = 128 (one CTA) and 96 KB at d = 64 (two).
+constexpr int decode_ctas_per_sm(int d) { return d == 64 ? 2 : 1; }
+constexpr int kDecodeChunk = 16;  // keys per TMA box and per step of a decode warp
+constexpr int kDecodeWarps = 8;   // warps per decode CTA, each walking every eighth chunk
 
 struct DecodeParams {
   const void* q;          // [B, N, Hq, d]
@@ -126,7 +128,7 @@ struct DecodeParams {
   const int32_t* kpos;    // [B, Nk] or nullptr (j)
   int rot_chunks;         // rotary_dim / 16
   int interleaved;
-  int keys_per_split;     // multiple of 64
+  int keys_per_split;     // multiple of kDecodeChunk
   int n_splits;
   float scale_log2;       // log2(e) / sqrt(d)
   float* part_o;          // [B, Hkv, n_splits, rows, d] unnormalised partial outputs
@@ -134,8 +136,15 @@ struct DecodeParams {
   RopeFreqs freqs;
 };
 
+struct DecodeMaps {
+  CUtensorMap k, v;  // [B, Nk, Hkv, d] in boxes of 64 columns x kDecodeChunk rows, 128-byte swizzle
+};
+
 // Split-KV decode: one CTA per (split, KV head, batch) writes partials, a second kernel merges them.
-cudaError_t launch_attn_decode(const DecodeParams& p, int d, bool bf16, cudaStream_t stream);
+cudaError_t launch_attn_decode(const DecodeMaps& maps, const DecodeParams& p, int d, bool bf16, cudaStream_t stream);
+
+// Reads and clears the decode kernels' device status word (call after synchronising).
+cudaError_t read_and_clear_decode_status(unsigned int* value);
 
 // ---- backward kernels ------------------------------------------------------------------------
 
