@@ -427,13 +427,16 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
   }
 }
 
-// One CTA of 256 threads per (row, KV head, batch): m = max_s m_s, w_s = 2^(m_s - m),
+// One CTA of 128 threads per (row, KV head, batch): m = max_s m_s, w_s = 2^(m_s - m),
 // l = sum_s l_s w_s, out = sum_s O_s w_s / l, lse = ln 2 (m + log2 l).  The splits' (m, l) pairs
-// are read in one pass by as many threads, the weights go to shared memory, and each of the 8 warps
-// sums the O rows of every 8th split (lane = 4 or 2 consecutive columns) with loads that do not
-// depend on one another; a shared-memory pass adds the 8 warps' sums.  Two rounds of loads in all,
+// are read in one pass by as many threads, the weights go to shared memory, and each of the 4 warps
+// sums the O rows of every 4th split (lane = 4 or 2 consecutive columns) with loads that do not
+// depend on one another; a shared-memory pass adds the 4 warps' sums.  Two rounds of loads in all,
 // whatever the number of splits.
-constexpr int kCombineThreads = 256;
+// 128 threads: with the decode kernel's 226 registers x 256 threads on an SM, a combine CTA still
+// fits beside it (registers and shared memory), so the programmatic dependent's CTAs are resident
+// and waiting when the decode grid finishes.
+constexpr int kCombineThreads = 128;
 constexpr int kMaxSplits = 1024;  // decode_plan never makes more
 
 template <int D, bool BF16>
