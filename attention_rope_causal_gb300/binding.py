@@ -51,6 +51,7 @@ _SIGNATURES = {
                                     [ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                      ctypes.POINTER(RopeOpts), ctypes.c_void_p]),
     "attnfuse_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "attnfuse_bwd_workspace_bytes_ex": (ctypes.c_size_t, [ctypes.c_int] * 6 + [ctypes.POINTER(RopeOpts)]),
     "attnfuse_workspace_bytes_ex": (ctypes.c_size_t, [ctypes.c_int] * 7 + [ctypes.POINTER(RopeOpts)]),
     "attnfuse_select_mode": (ctypes.c_int, [ctypes.c_int] * 6),
     "attnfuse_rope_causal_fwd_prerotate_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -196,18 +197,22 @@ def rope_apply(x, rope_base: float, out=None, stream=None, rotary_dim=None, inte
     return out
 
 
-def bwd_workspace_bytes(B, Hq, Hkv, N, d, dtype=torch.bfloat16) -> int:
-    return int(load().attnfuse_bwd_workspace_bytes(B, Hq, Hkv, N, d, DTYPES[dtype]))
+def bwd_workspace_bytes(B, Hq, Hkv, N, d, dtype=torch.bfloat16, kv_len=None) -> int:
+    if kv_len is None:
+        return int(load().attnfuse_bwd_workspace_bytes(B, Hq, Hkv, N, d, DTYPES[dtype]))
+    opts = RopeOpts(0, 0, int(kv_len), None, None)
+    return int(load().attnfuse_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, DTYPES[dtype], ctypes.byref(opts)))
 
 
 def rope_causal_bwd(q, k, v, out, lse, dout, rope_base: float, dq=None, dk=None, dv=None, workspace=None,
                     stream=None, rotary_dim=None, interleaved: bool = False, q_positions=None, k_positions=None):
-    """Backward pass through ``attnfuse_rope_causal_bwd`` (``_ex`` with a RoPE variant or positions):
-    (dq, dk, dv) for q [B, N, Hq, d], k/v [B, N, Hkv, d], the forward's out [B, N, Hq, d] and lse
-    [B, Hq, N] (float32), and dout = dL/dout.  All CUDA tensors, contiguous, one 16-bit dtype (lse
-    float32); positions [B, N] CUDA int32."""
+    """Backward pass through ``attnfuse_rope_causal_bwd`` (``_ex`` with a RoPE variant, positions or
+    more keys than queries): (dq, dk, dv) for q [B, N, Hq, d], k/v [B, Nk, Hkv, d] with Nk >= N (the
+    queries are the last N of the Nk tokens), the forward's out [B, N, Hq, d] and lse [B, Hq, N]
+    (float32), and dout = dL/dout.  All CUDA tensors, contiguous, one 16-bit dtype (lse float32);
+    q_positions [B, N] and k_positions [B, Nk] CUDA int32."""
     B, N, Hq, d = q.shape
-    Hkv = k.shape[2]
+    Nk, Hkv = k.shape[1], k.shape[2]
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse), ("dout", dout)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
@@ -219,8 +224,8 @@ def rope_causal_bwd(q, k, v, out, lse, dout, rope_base: float, dq=None, dk=None,
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    opts = _opts(rotary_dim, interleaved, 0, _positions(q_positions, B * N, "q_positions"),
-                 _positions(k_positions, B * N, "k_positions"))
+    opts = _opts(rotary_dim, interleaved, Nk if Nk != N else 0, _positions(q_positions, B * N, "q_positions"),
+                 _positions(k_positions, B * Nk, "k_positions"))
     if opts is None:
         _check(load().attnfuse_rope_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                                                _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(rope_base), DTYPES[q.dtype],
@@ -263,7 +268,7 @@ class RopeCausalAttention(torch.autograd.Function):
         q, k, v, out, lse = ctx.saved_tensors
         rope_base, rotary_dim, interleaved = ctx.rope
         dq, dk, dv = rope_causal_bwd(q, k, v, out, lse, dout.contiguous(), rope_base, rotary_dim=rotary_dim,
-                                     interleaved=interleaved)
+                                     interleaved=interleaved)  # k, v may hold more rows than q
         return dq, dk, dv, None, None, None, None
 
 

@@ -162,6 +162,19 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ A
   }
 }
 
+// Causal structure with Nk >= N keys (the N queries are the last N of the Nk tokens: query row i
+// sees key j iff j <= q_off + i, q_off = Nk - N).  With q_off = 0 these are key tile kt's first
+// query tile kt and query tile t's key tiles 0 .. t.
+// First query tile with a row that sees some key of key tile kt.
+__device__ __forceinline__ int first_qtile(int kt, const AttnBwdParams& p) {
+  const int v = kt * BM - p.q_off;
+  return v <= 0 ? 0 : v / BM;
+}
+// Number of key tiles some row of query tile t sees.
+__device__ __forceinline__ int qtile_keytiles(int t, const AttnBwdParams& p) {
+  return (p.q_off + min(t * BM + BM - 1, p.N - 1)) / BM + 1;
+}
+
 // R(pos)^T applied to the pair (x, y) = (row[e], row[e + d/2]) with frequency F_e.
 __device__ __forceinline__ void unrotate_pair(float& x, float& y, uint32_t pos, uint32_t flo, uint32_t fhi) {
   float c, s;
@@ -293,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool skip = __shfl_sync(0xFFFFFFFFu, ctl.skip, 0) != 0;
   const unsigned long long tmo = p.timeout_ns;
   const int g = p.Hq / p.Hkv, nt = p.n_tiles, bh_count = p.B * p.Hkv;
-  const int total = bh_count * nt;
+  const int total = bh_count * p.n_ktiles;
 
   if (!skip && warp == 0) {
     // ------------------------------------------ TMA producer ------------------------------
@@ -316,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_tile<D>(sV, &tmV, bar_addr(ctl.res_full), hk, kt * BM, b);
       }
       ++uc;
-      const int nq = nt - kt;
+      const int t0 = first_qtile(kt, p), nq = nt - t0;
       for (int s = 0; s < g * nq; ++s) {
-        const int h = hk * g + s / nq, t = kt + s % nq, st = gs & 1;
+        const int h = hk * g + s / nq, t = t0 + s % nq, st = gs & 1;
         if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
         // L = lse * log2(e) and D of the tile's 128 query rows (rows past N: L = +inf, so P = 0).
         float* vL = sVec + st * 2 * BM;
@@ -357,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
       const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
       if (u >= total) break;
-      const int kt = u / bh_count, nsteps = g * (nt - kt);
+      const int kt = u / bh_count, nsteps = g * (nt - first_qtile(kt, p));
       if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
       if (!(ok = wait_warp(bar_addr(ctl.ring_full[gs & 1]), (gs >> 1) & 1, ctl, tmo))) break;
       ptx::tc_fence_after();
@@ -406,14 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
       if (u >= total) break;
       const int kt = u / bh_count, bh = u - kt * bh_count, b = bh / p.Hkv, hk = bh - b * p.Hkv;
-      const int nq = nt - kt;
+      const int t0 = first_qtile(kt, p), nq = nt - t0;
       for (int s = 0; s < g * nq; ++s) {
-        const int t = kt + s % nq, st = gs & 1;
+        const int t = t0 + s % nq, st = gs & 1;
         if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
         if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
         ptx::tc_fence_after();
         const float* vL = sVec + st * 2 * BM;
-        const bool diag = t == kt;  // query c of the tile sees key r iff c >= r
+        // query c of the tile sees key r iff c >= r - delta; only tiles with delta < 127 mask anything
+        const int delta = p.q_off + (t - kt) * BM;
+        const bool diag = delta < BM - 1;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int q0 = 64 * wg + 32 * c;
@@ -428,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -vL[q]));
             float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -vL[q + 1]));
             if (diag) {
-              if (q < r) p0 = 0.f;
-              if (q + 1 < r) p1 = 0.f;
+              if (q < r - delta) p0 = 0.f;
+              if (q + 1 < r - delta) p1 = 0.f;
             }
             const float d0 = p0 * (__uint_as_float(dv[2 * e]) - vL[BM + q]);
             const float d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - vL[BM + q + 1]);
@@ -470,9 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar_addr(ctl.acc_empty));
       ++uc;
       const int j = kt * BM + r;
-      if (j < p.N) {
-        T* dvrow = reinterpret_cast<T*>(p.dv) + (((size_t)b * p.N + j) * p.Hkv + hk) * D;
-        T* dkrow = reinterpret_cast<T*>(p.dk) + (((size_t)b * p.N + j) * p.Hkv + hk) * D;
+      if (j < p.Nk) {
+        T* dvrow = reinterpret_cast<T*>(p.dv) + (((size_t)b * p.Nk + j) * p.Hkv + hk) * D;
+        T* dkrow = reinterpret_cast<T*>(p.dk) + (((size_t)b * p.Nk + j) * p.Hkv + hk) * D;
 #pragma unroll
         for (int v = 0; v < HV / 8; ++v) {
           uint4 w;
@@ -512,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================ dQ ======================================================
 // Unit u: query tile t = nt - 1 - u / (B Hq) (descending: the longest units first) of head h, batch
-// b; steps: key tiles j = 0 .. t of KV head h / g.
+// b; steps: the key tiles j of KV head h / g that some row of the tile sees (0 .. t when N == Nk).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -561,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_tile<D>(sO, &tmO, bar_addr(ctl.res_full), h, t * BM, b);
       }
       ++uc;
-      for (int j = 0; j <= t; ++j) {
+      for (int j = 0, nkj = qtile_keytiles(t, p); j < nkj; ++j) {
         const int st = gs & 1;
         if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
         if (lane == 0) {
@@ -595,10 +610,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       issue_s(gs, 0);
       issue_s(gs, 1);
-      for (int j = 0; j <= t; ++j) {
+      const int nkj = qtile_keytiles(t, p);
+      for (int j = 0; j < nkj; ++j) {
         const int st = gs & 1;
         const uint32_t sK = sRing + st * 2 * C::TILE;
-        const bool more = j < t;
+        const bool more = j + 1 < nkj;
         for (int half = 0; half < 2; ++half) {
           if (!(ok = wait_warp(bar_addr(ctl.p_ready[half]), gs & 1, ctl, tmo))) break;
           if (j == 0 && half == 0 && uc > 0 && !(ok = wait_warp(bar_addr(ctl.acc_empty), (uc - 1) & 1, ctl, tmo)))
@@ -640,10 +656,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t srow = ((size_t)b * p.Hq + h) * p.N + i;
       const float L = i < p.N ? p.lse[srow] * kLog2e : INFINITY;  // rows past N: P = 0
       const float Dr = i < p.N ? p.Dvec[srow] : 0.f;
-      for (int j = 0; j <= t; ++j) {
+      const int nkj = qtile_keytiles(t, p);
+      for (int j = 0; j < nkj; ++j) {
         if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
         ptx::tc_fence_after();
-        const bool diag = j == t;  // key c of the tile is visible to query r iff c <= r
+        // key c of the tile is visible to query r iff c <= r + delta; only tiles with delta < 127 mask
+        const int delta = p.q_off + (t - j) * BM;
+        const bool diag = delta < BM - 1;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int k0 = 64 * wg + 32 * c;
@@ -658,8 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -L));
             float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -L));
             if (diag) {
-              if (k > r) p0 = 0.f;
-              if (k + 1 > r) p1 = 0.f;
+              if (k > r + delta) p0 = 0.f;
+              if (k + 1 > r + delta) p1 = 0.f;
             }
             dsp[e] = pack2<BF16>(p0 * (__uint_as_float(dv[2 * e]) - Dr), p1 * (__uint_as_float(dv[2 * e + 1]) - Dr));
           }
@@ -695,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[e] = __uint_as_float(qx[e]) * p.inv_sqrt_d;
           y[e] = __uint_as_float(qy[e]) * p.inv_sqrt_d;
           const int k = wg * QK + e;
-          if (p.unrotate) unrotate_pair(x[e], y[e], (uint32_t)i, p.freqs.lo[k], p.freqs.hi[k]);
+          if (p.unrotate) unrotate_pair(x[e], y[e], (uint32_t)(p.q_off + i), p.freqs.lo[k], p.freqs.hi[k]);
         }
 #pragma unroll
         for (int v = 0; v < QK / 8; ++v) {
@@ -762,7 +781,7 @@ cudaError_t launch_bwd_impl(const AttnBwdMaps& m, const AttnBwdParams& p, cudaSt
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = launch_dependent(bwd_prep_kernel<D, BF16>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
-  e = launch_persistent<2 * D + BF16 * 1>(bwd_dkdv_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hkv * p.n_tiles, m, p,
+  e = launch_persistent<2 * D + BF16 * 1>(bwd_dkdv_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hkv * p.n_ktiles, m, p,
                                           stream);
   if (e != cudaSuccess) return e;
   return launch_persistent<2 * D + BF16 * 1 + 1000>(bwd_dq_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hq * p.n_tiles,

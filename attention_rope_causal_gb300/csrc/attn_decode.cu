@@ -208,29 +208,34 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
   else if (tid < 128) sF[tid] = p.freqs.hi[tid - 64];
   __syncthreads();
   const int r = 2 * R * 8;  // rotary dimension
-  for (int idx = tid; idx < rows * R; idx += kThreads) {
-    const int row = idx / R, fg = idx % R;
+  // one rotation pair per thread: row, frequency k = 8 fg + t
+  for (int idx = tid; idx < rows * R * 8; idx += kThreads) {
+    const int row = idx / (8 * R), kf = idx % (8 * R), fg = kf / 8, t = kf % 8;
     const int i = row % p.N;
     const int32_t pos = p.qpos ? p.qpos[(size_t)b * p.N + i] : p.q_off + i;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      float c, s_;
-      rope_cs_signed(pos, sF[8 * fg + t], sF[64 + 8 * fg + t], c, s_);
-      const int ia = il ? 16 * fg + 2 * t : 8 * fg + t;
-      const int ib = il ? ia + 1 : r / 2 + ia;
-      float xr, yr;
-      rope_pair(sQ[row * D + ia], sQ[row * D + ib], c, s_, xr, yr);
-      float2 rr;
-      Pack<BF16>::unpack(Pack<BF16>::pack(xr, yr), rr.x, rr.y);
-      sQ[row * D + ia] = rr.x;
-      sQ[row * D + ib] = rr.y;
-    }
+    float c, s_;
+    rope_cs_signed(pos, sF[kf], sF[64 + kf], c, s_);
+    const int ia = il ? 16 * fg + 2 * t : kf;
+    const int ib = il ? ia + 1 : r / 2 + ia;
+    float xr, yr;
+    rope_pair(sQ[row * D + ia], sQ[row * D + ib], c, s_, xr, yr);
+    float2 rr;
+    Pack<BF16>::unpack(Pack<BF16>::pack(xr, yr), rr.x, rr.y);
+    sQ[row * D + ia] = rr.x;
+    sQ[row * D + ib] = rr.y;
   }
-  // cos/sin steps of a rotation group: RS rows (between a lane's passes) and kChunk (kWarps - 1) + RS
-  // rows (from a lane's last row of one chunk to its first row of the warp's next chunk)
-  if (tid < R) rope_cs8_exact((uint32_t)C::RS, sF, sF + 64, 8 * tid, sStep[tid]);
-  else if (tid >= 64 && tid < 64 + R)
-    rope_cs8_exact((uint32_t)(kChunk * (kWarps - 1) + C::RS), sF, sF + 64, 8 * (tid - 64), sSkip[tid - 64]);
+  // cos/sin steps of a rotation group, one frequency per thread: RS rows (between a lane's passes)
+  // and kChunk (kWarps - 1) + RS rows (from a lane's last row of one chunk to its first row of the
+  // warp's next chunk).  RopeCS8 holds frequency 8 fg + 2 j + e at float 2 j + e of c (and of s).
+  if (tid < 16 * R) {
+    const int which = tid / (8 * R), kf = tid % (8 * R), fg = kf / 8, t = kf % 8;
+    const uint32_t steps = which == 0 ? (uint32_t)C::RS : (uint32_t)(kChunk * (kWarps - 1) + C::RS);
+    float c, s_;
+    rope_cs(steps, sF[kf], sF[64 + kf], c, s_);
+    float* dst = reinterpret_cast<float*>(which == 0 ? &sStep[fg] : &sSkip[fg]);
+    dst[t] = c;
+    dst[8 + t] = s_;
+  }
   __syncthreads();
   for (int idx = tid; idx < kDecodeMaxRows * (D / 2); idx += kThreads) {
     const int row = idx / (D / 2), e = 2 * (idx % (D / 2));

@@ -603,9 +603,16 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
 }
 
 size_t attnfuse_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype) {
+  return attnfuse_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, dtype, nullptr);
+}
+
+size_t attnfuse_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype,
+                                       const attnfuse_rope_opts_t* opts) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   if (dtype != ATTNFUSE_BF16 && dtype != ATTNFUSE_FP16) return 0;
-  return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, N, Hkv, d), 256) +
+  const int Nk = (opts && opts->kv_len) ? opts->kv_len : N;
+  if (Nk < N) return 0;
+  return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, Nk, Hkv, d), 256) +
          round_up((size_t)B * Hq * N * sizeof(float), 256);
 }
 
@@ -627,14 +634,14 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   if (st != ATTNFUSE_OK) return st;
   Opts o;
   if ((st = resolve_opts(opts, d, N, &o)) != ATTNFUSE_OK) return st;
-  if (o.Nk != N) return fail(ATTNFUSE_ERR_INVALID_ARG, "the backward pass takes kv_len 0 (= N) only");
+  const int Nk = o.Nk;
   // The half-split form over all d at positions i and j is rotated back in the kernels' epilogues;
   // any other form runs a pre-rotation pass with the negated positions over dq and dk afterwards.
   const bool plain_form = o.rdim == d && o.interleaved == 0 && !o.qpos && !o.kpos;
   if (!lse || !dout || !dq || !dk || !dv) return fail(ATTNFUSE_ERR_INVALID_ARG, "lse, dout, dq, dk and dv must be non-null");
   if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
     return fail(ATTNFUSE_ERR_INVALID_ARG, "dout, dq, dk and dv must be 16-byte aligned");
-  const size_t need = attnfuse_bwd_workspace_bytes(B, Hq, Hkv, N, d, dtype);
+  const size_t need = attnfuse_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, dtype, opts);
   if (workspace) {
     if (workspace_bytes < need)
       return fail(ATTNFUSE_ERR_INVALID_ARG, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
@@ -656,7 +663,7 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   }
   void* qr = ws;
   void* kr = static_cast<char*>(ws) + round_up(tensor_bytes(B, N, Hq, d), 256);
-  float* Dv = reinterpret_cast<float*>(static_cast<char*>(kr) + round_up(tensor_bytes(B, N, Hkv, d), 256));
+  float* Dv = reinterpret_cast<float*>(static_cast<char*>(kr) + round_up(tensor_bytes(B, Nk, Hkv, d), 256));
 
   AttnBwdParams p;
   std::memset(&p, 0, sizeof p);
@@ -664,7 +671,10 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.N = N;
+  p.Nk = Nk;
+  p.q_off = Nk - N;
   p.n_tiles = (N + 127) / 128;
+  p.n_ktiles = (Nk + 127) / 128;
   p.out = out;
   p.dout = dout;
   p.lse = lse;
@@ -678,8 +688,9 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   p.timeout_ns = kTimeoutNs;
   rope_freqs_host(d, rope_base, &p.freqs);
 
-  // One pre-rotation launch per (tensor, position source); both tensors in one launch when they share
-  // positions i, j.  sign = 1: q', k' before the kernels; -1: dq, dk rotated back after them.
+  // One pre-rotation launch per tensor (queries at q_off + i or q_positions over N tokens, keys at j
+  // or k_positions over Nk), or both tensors in one launch when they share tokens and positions.
+  // neg = 0: q', k' before the kernels; 1: dq, dk rotated back after them (R(p)^T = R(-p)).
   RopeApplyParams rp;
   std::memset(&rp, 0, sizeof rp);
   rp.rot_chunks = o.rdim / 16;
@@ -687,35 +698,42 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   rope_freqs_host(o.rdim, rope_base, &rp.freqs);
   auto rotate = [&](const void* xq, void* yq, const void* xk, void* yk, int neg) -> cudaError_t {
     rp.pos_neg = neg;
-    rp.N = N;
-    rp.tokens = (long long)B * N;
     const RopeJob jq{xq, yq, Hq, (Hq + kHeadsPerGroup - 1) / kHeadsPerGroup};
     const RopeJob jk{xk, yk, Hkv, (Hkv + kHeadsPerGroup - 1) / kHeadsPerGroup};
-    if (!o.qpos && !o.kpos) {
+    if (Nk == N && !o.qpos && !o.kpos) {
       rp.job[0] = jq;
       rp.job[1] = jk;
       rp.njobs = 2;
+      rp.N = N;
+      rp.tokens = (long long)B * N;
       rp.groups_total = jq.groups + jk.groups;
       rp.pos = nullptr;
+      rp.pos_off = 0;
       return launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
     }
     rp.njobs = 1;
     rp.job[0] = jq;
+    rp.N = N;
+    rp.tokens = (long long)B * N;
     rp.groups_total = jq.groups;
     rp.pos = o.qpos;
+    rp.pos_off = Nk - N;
     cudaError_t err = launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
     if (err != cudaSuccess) return err;
     rp.job[0] = jk;
+    rp.N = Nk;
+    rp.tokens = (long long)B * Nk;
     rp.groups_total = jk.groups;
     rp.pos = o.kpos;
+    rp.pos_off = 0;
     return launch_rope_apply(rp, d, dtype == ATTNFUSE_BF16, s);
   };
   cudaError_t e = rotate(q, qr, k, kr, 0);
   if (e != cudaSuccess) st = cuda_fail(e, "rope_apply launch");
   AttnBwdMaps maps;
   if (st == ATTNFUSE_OK && (st = encode_bnhd(&maps.q, qr, B, N, Hq, d, dtype, "q'")) == ATTNFUSE_OK &&
-      (st = encode_bnhd(&maps.k, kr, B, N, Hkv, d, dtype, "k'")) == ATTNFUSE_OK &&
-      (st = encode_bnhd(&maps.v, v, B, N, Hkv, d, dtype, "v")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.k, kr, B, Nk, Hkv, d, dtype, "k'")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.v, v, B, Nk, Hkv, d, dtype, "v")) == ATTNFUSE_OK &&
       (st = encode_bnhd(&maps.dout, dout, B, N, Hq, d, dtype, "dout")) == ATTNFUSE_OK) {
     e = launch_attn_bwd(maps, p, d, dtype == ATTNFUSE_BF16, s);
     if (e != cudaSuccess) st = cuda_fail(e, "backward launch");

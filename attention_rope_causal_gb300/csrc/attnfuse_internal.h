@@ -150,17 +150,20 @@ cudaError_t read_and_clear_decode_status(unsigned int* value);
 
 struct AttnBwdParams {
   int B, Hq, Hkv, N;
-  int n_tiles;            // ceil(N / 128)
+  int Nk;                 // key/value rows per batch entry (>= N); the queries are the last N
+  int q_off;              // Nk - N: query row i is token q_off + i and sees keys j <= q_off + i
+  int n_tiles;            // ceil(N / 128): query tiles
+  int n_ktiles;           // ceil(Nk / 128): key tiles
   const void* out;        // [B, N, Hq, d] forward output
   const void* dout;       // [B, N, Hq, d] dL/dout
   const float* lse;       // [B, Hq, N] forward log-sum-exp (natural log)
   float* Dvec;            // [B, Hq, N] workspace: dout . out per row
   void* dq;               // [B, N, Hq, d]
-  void* dk;               // [B, N, Hkv, d]
-  void* dv;               // [B, N, Hkv, d]
+  void* dk;               // [B, Nk, Hkv, d]
+  void* dv;               // [B, Nk, Hkv, d]
   float scale_log2;       // log2(e) / sqrt(d)
   float inv_sqrt_d;
-  int unrotate;           // 1: the epilogues apply R^T (half-split over all d, positions i and j);
+  int unrotate;           // 1: the epilogues apply R^T (half-split over all d, positions q_off + i and j);
                           // 0: they write the gradients in the rotated frame (a pass rotates back)
   unsigned long long timeout_ns;
   RopeFreqs freqs;        // F_k, k < d/2 (half-split, rotary dimension d)

@@ -189,10 +189,14 @@ attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const v
                                            int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
                                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* attnfuse_rope_causal_bwd for the RoPE variants and explicit positions of attnfuse_rope_opts_t
- * (rotary_dim, interleaved, q_positions [B, N], k_positions [B, N]; kv_len must be 0 or N).  The
- * kernels produce the gradients in the rotated frame and a pre-rotation pass with the negated
- * positions rotates dq and dk back (R^T). */
+/* attnfuse_rope_causal_bwd for every option of attnfuse_rope_opts_t: the RoPE variants (rotary_dim,
+ * interleaved), explicit positions (q_positions [B, N], k_positions [B, Nk]) and more keys than
+ * queries (kv_len = Nk >= N: k, v, dk, dv are [B, Nk, Hkv, d], the N queries are the last N of the
+ * Nk tokens and query i sees keys j <= Nk - N + i, as in the forward -- the backward of a prefill
+ * that extends a cache).  For the half-split form over all d entries at the default positions the
+ * kernels rotate the gradients back themselves; otherwise they produce them in the rotated frame
+ * and a pre-rotation pass with the negated positions rotates dq and dk back (R^T).  `workspace`
+ * holds attnfuse_bwd_workspace_bytes_ex(...) bytes. */
 attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, const void* v, const void* out,
                                               const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                                               int Hq, int Hkv, int N, int d, double rope_base, attnfuse_dtype_t dtype,
@@ -201,6 +205,12 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
 
 /* Bytes of workspace attnfuse_rope_causal_bwd needs (0 for invalid arguments). */
 size_t attnfuse_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype);
+
+/* Bytes of workspace attnfuse_rope_causal_bwd_ex needs with these options: rotated q [B, N, Hq, d],
+ * rotated k [B, Nk, Hkv, d] (Nk = kv_len, 0 meaning N) and D [B, Hq, N] float, each rounded up to
+ * 256 bytes (0 for invalid arguments). */
+size_t attnfuse_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype,
+                                       const attnfuse_rope_opts_t* opts);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word.  Returns

@@ -95,6 +95,13 @@ def _load():
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.orc_rope_causal_bwd_kv.restype = ctypes.c_int
+            lib.orc_rope_causal_bwd_kv.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.orc_rope_causal_bwd_ex.restype = ctypes.c_int
             lib.orc_rope_causal_bwd_ex.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -255,14 +262,15 @@ def _rows(rows, N: int, what: str):
 
 def rope_causal_bwd(q, k, v, dout, base: float, q_rows=None, k_rows=None, threads: int | None = None,
                     rotary_dim: int | None = None, interleaved: bool = False, q_positions=None, k_positions=None):
-    """Backward pass of :func:`rope_causal` (N queries and keys, default positions): the gradients of
-    L = sum(dout * out) with respect to q, k and v (no lse term).
+    """Backward pass of :func:`rope_causal`: the gradients of L = sum(dout * out) with respect to q,
+    k and v (no lse term).
 
-    q, dout: [B, N, Hq, d]; k, v: [B, N, Hkv, d], one dtype (bf16/fp16 torch tensors, fp16 or fp64
-    arrays).  q_rows / k_rows select the query rows whose dq and the key rows whose dk, dv are
-    returned (default: all, in order).  rotary_dim, interleaved, q_positions and k_positions ([B, N]
-    each) select the RoPE form as for :func:`rope_causal`.  Returns (dq [B, Rq, Hq, d], dk [B, Rk, Hkv, d],
-    dv [B, Rk, Hkv, d]) as float64.
+    q, dout: [B, Nq, Hq, d]; k, v: [B, Nk, Hkv, d] with Nk >= Nq (the queries are the last Nq of the
+    Nk tokens, as in :func:`rope_causal`), one dtype (bf16/fp16 torch tensors, fp16 or fp64 arrays).
+    q_rows / k_rows select the query rows whose dq and the key rows whose dk, dv are returned
+    (default: all, in order).  rotary_dim, interleaved, q_positions ([B, Nq]) and k_positions
+    ([B, Nk]) select the RoPE form as for :func:`rope_causal`.  Returns (dq [B, Rq, Hq, d],
+    dk [B, Rk, Hkv, d], dv [B, Rk, Hkv, d]) as float64.
     """
     qr, dq_ = _as_raw(q)
     kr, dk_ = _as_raw(k)
@@ -271,24 +279,26 @@ def rope_causal_bwd(q, k, v, dout, base: float, q_rows=None, k_rows=None, thread
     if not (dq_ == dk_ == dv_ == dg_):
         raise TypeError("q, k, v, dout must share one dtype")
     B, N, Hq, d = qr.shape
-    Hkv = kr.shape[2]
-    if kr.shape != (B, N, Hkv, d) or vr.shape != (B, N, Hkv, d) or gr.shape != qr.shape:
-        raise ValueError("k, v must be [B, N, Hkv, d] and dout [B, N, Hq, d]")
+    Nk, Hkv = kr.shape[1], kr.shape[2]
+    if kr.shape != (B, Nk, Hkv, d) or vr.shape != (B, Nk, Hkv, d) or gr.shape != qr.shape:
+        raise ValueError("k, v must be [B, Nk, Hkv, d] and dout [B, N, Hq, d]")
+    if Nk < N:
+        raise ValueError("k and v must hold at least as many tokens as q")
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
     qpos = _positions(q_positions, B, N, "q_positions")
-    kpos = _positions(k_positions, B, N, "k_positions")
+    kpos = _positions(k_positions, B, Nk, "k_positions")
     qp, nq, _qs = _rows(q_rows, N, "q_rows")
-    kp, nk, _ks = _rows(k_rows, N, "k_rows")
+    kp, nk, _ks = _rows(k_rows, Nk, "k_rows")
     dq = np.zeros((B, nq, Hq, d))
     dk = np.zeros((B, nk, Hkv, d))
     dv = np.zeros((B, nk, Hkv, d))
     r = d if rotary_dim is None else int(rotary_dim)
-    rc = _load().orc_rope_causal_bwd_ex(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, gr.ctypes.data, dq_, B, Hq,
-                                        Hkv, N, d, r, int(bool(interleaved)), float(base),
+    rc = _load().orc_rope_causal_bwd_kv(qr.ctypes.data, kr.ctypes.data, vr.ctypes.data, gr.ctypes.data, dq_, B, Hq,
+                                        Hkv, N, Nk, d, r, int(bool(interleaved)), float(base),
                                         None if qpos is None else qpos.ctypes.data,
                                         None if kpos is None else kpos.ctypes.data, qp, nq, kp, nk, dq.ctypes.data,
                                         dk.ctypes.data, dv.ctypes.data, int(threads or default_threads()))
     if rc != 0:
-        raise RuntimeError("orc_rope_causal_bwd failed")
+        raise RuntimeError("orc_rope_causal_bwd_kv failed")
     return dq, dk, dv

@@ -335,15 +335,16 @@ int orc_rope_causal(const void *q, const void *k, const void *v, int dtype, int 
 }
 
 /* ------------------------------------------------------------------------------------------- */
-/* Public entry 4: the backward pass of entry 2 (N queries and keys, positions i and j).         */
+/* Public entry 4: the backward pass of entry 3 (Nq queries, the last Nq of Nk >= Nq tokens;   */
+/* query i sees keys j <= (Nk - Nq) + i; positions (Nk - Nq) + i and j unless given).           */
 /*                                                                                               */
-/* Given dO = dL/dO for the loss L, with P_ij = softmax_j(s_ij) over j <= i, s_ij = q'_i.k'_j/   */
+/* Given dO = dL/dO for the loss L, with P_ij = softmax_j(s_ij) over visible j, s_ij = q'_i.k'_j/ */
 /* sqrt(d), q' = R(i) q_i, k' = R(j) k_j (R(p) the RoPE rotation at position p), the chain rule  */
 /* through o_i = sum_j P_ij v_j gives                                                            */
-/*   dv_j   = sum_{h in the group of j's head} sum_{i >= j} P_ij dO_i                            */
+/*   dv_j   = sum_{h in the group of j's head} sum_{i that see j} P_ij dO_i                      */
 /*   dP_ij  = dO_i . v_j                                                                          */
 /*   dS_ij  = P_ij (dP_ij - sum_k P_ik dP_ik)            (softmax Jacobian)                       */
-/*   dq'_i  = sum_j dS_ij k'_j / sqrt(d),   dk'_j = sum_{h, i >= j} dS_ij q'_i / sqrt(d)           */
+/*   dq'_i  = sum_j dS_ij k'_j / sqrt(d),   dk'_j = sum_{h, i that see j} dS_ij q'_i / sqrt(d)     */
 /*   dq_i   = R(i)^T dq'_i,                 dk_j  = R(j)^T dk'_j    (R^T = rotation by -p)        */
 /* The loss has no lse term (dL/dlse = 0).  Pass 1 (per query row) computes dq and keeps the row  */
 /* max m_i, denominator l_i and D_i = sum_k P_ik dP_ik; pass 2 (per key row) recomputes P_ij from  */
@@ -353,15 +354,15 @@ int orc_rope_causal(const void *q, const void *k, const void *v, int dtype, int 
 typedef struct {
   const void *v, *dout;
   int dtype;
-  int B, Hq, Hkv, N, d;
+  int B, Hq, Hkv, Nq, Nk, d;
   rope_form_t form;
   const double *theta;
-  const double *qrot, *krot; /* [B, N, Hq, d], [B, N, Hkv, d] */
-  const double *qpos;        /* [B, N] rotation positions of the queries, or NULL: i */
-  const int64_t *qslot;      /* [N]: output slot of query row i, or -1 if its dq is not reported */
+  const double *qrot, *krot; /* [B, Nq, Hq, d], [B, Nk, Hkv, d] */
+  const double *qpos;        /* [B, Nq] rotation positions of the queries, or NULL: (Nk - Nq) + i */
+  const int64_t *qslot;      /* [Nq]: output slot of query row i, or -1 if its dq is not reported */
   int64_t nq;                /* reported query rows per batch entry */
   double *dq;                /* [B, nq, Hq, d] */
-  double *m, *l, *D;         /* [B, Hq, N] row statistics */
+  double *m, *l, *D;         /* [B, Hq, Nq] row statistics */
 } bwd_q_ctx_t;
 
 static double dot_d(const double *a, const double *b, int d) {
@@ -370,75 +371,80 @@ static double dot_d(const double *a, const double *b, int d) {
   return s;
 }
 
-/* One item = one (b, h, i). scratch: dO_i (d), dq' (d), scores (N), dP (N). */
+/* One item = one (b, h, i).  Query i sees keys j <= last = (Nk - Nq) + i.
+ * scratch: dO_i (d), dq' (d), scores (Nk), dP (Nk). */
 static void bwd_q_item(void *vctx, int64_t item, double *scratch) {
   bwd_q_ctx_t *c = (bwd_q_ctx_t *)vctx;
-  int N = c->N, d = c->d;
-  int64_t i = item % N;
-  int h = (int)((item / N) % c->Hq);
-  int b = (int)(item / ((int64_t)N * c->Hq));
+  int Nq = c->Nq, Nk = c->Nk, d = c->d;
+  int64_t i = item % Nq;
+  int h = (int)((item / Nq) % c->Hq);
+  int b = (int)(item / ((int64_t)Nq * c->Hq));
   int hk = h / (c->Hq / c->Hkv);
-  double *dOi = scratch, *dqr = scratch + d, *s = scratch + 2 * d, *dP = s + N;
-  const double *qi = c->qrot + (((size_t)b * N + (size_t)i) * c->Hq + h) * d;
-  size_t obase = (((size_t)b * N + (size_t)i) * c->Hq + h) * d;
+  int64_t last = (int64_t)(Nk - Nq) + i;
+  double *dOi = scratch, *dqr = scratch + d, *s = scratch + 2 * d, *dP = s + Nk;
+  const double *qi = c->qrot + (((size_t)b * Nq + (size_t)i) * c->Hq + h) * d;
+  size_t obase = (((size_t)b * Nq + (size_t)i) * c->Hq + h) * d;
   for (int e = 0; e < d; ++e) dOi[e] = load_elem(c->dout, c->dtype, obase + e);
   double scale = 1.0 / sqrt((double)d);
   double mx = -INFINITY;
-  for (int64_t j = 0; j <= i; ++j) {
-    const double *kj = c->krot + (((size_t)b * N + (size_t)j) * c->Hkv + hk) * d;
+  for (int64_t j = 0; j <= last; ++j) {
+    const double *kj = c->krot + (((size_t)b * Nk + (size_t)j) * c->Hkv + hk) * d;
     s[j] = dot_d(qi, kj, d) * scale;
     if (s[j] > mx) mx = s[j];
     double dp = 0.0;
-    size_t vbase = (((size_t)b * N + (size_t)j) * c->Hkv + hk) * d;
+    size_t vbase = (((size_t)b * Nk + (size_t)j) * c->Hkv + hk) * d;
     for (int e = 0; e < d; ++e) dp += dOi[e] * load_elem(c->v, c->dtype, vbase + e);
     dP[j] = dp;
   }
   double den = 0.0;
-  for (int64_t j = 0; j <= i; ++j) den += exp(s[j] - mx);
+  for (int64_t j = 0; j <= last; ++j) den += exp(s[j] - mx);
   double Dsum = 0.0;
-  for (int64_t j = 0; j <= i; ++j) Dsum += exp(s[j] - mx) / den * dP[j];
-  size_t st = ((size_t)b * c->Hq + h) * N + (size_t)i;
+  for (int64_t j = 0; j <= last; ++j) Dsum += exp(s[j] - mx) / den * dP[j];
+  size_t st = ((size_t)b * c->Hq + h) * Nq + (size_t)i;
   c->m[st] = mx;
   c->l[st] = den;
   c->D[st] = Dsum;
   int64_t slot = c->qslot[i];
   if (slot < 0) return;
   for (int e = 0; e < d; ++e) dqr[e] = 0.0;
-  for (int64_t j = 0; j <= i; ++j) {
+  for (int64_t j = 0; j <= last; ++j) {
     double dS = exp(s[j] - mx) / den * (dP[j] - Dsum);
-    const double *kj = c->krot + (((size_t)b * N + (size_t)j) * c->Hkv + hk) * d;
+    const double *kj = c->krot + (((size_t)b * Nk + (size_t)j) * c->Hkv + hk) * d;
     for (int e = 0; e < d; ++e) dqr[e] += dS * kj[e] * scale;
   }
   double *out = c->dq + (((size_t)b * (size_t)c->nq + (size_t)slot) * c->Hq + h) * d;
-  double qp = c->qpos ? c->qpos[(size_t)b * N + (size_t)i] : (double)i;
+  double qp = c->qpos ? c->qpos[(size_t)b * Nq + (size_t)i] : (double)last;
   rope_rotate_vec(dqr, out, c->form, -qp, c->theta); /* R(p_i)^T */
 }
 
 typedef struct {
   const void *v, *dout;
   int dtype;
-  int B, Hq, Hkv, N, d;
+  int B, Hq, Hkv, Nq, Nk, d;
   rope_form_t form;
   const double *theta;
   const double *qrot, *krot;
-  const double *kpos;        /* [B, N] rotation positions of the keys, or NULL: j */
+  const double *kpos;        /* [B, Nk] rotation positions of the keys, or NULL: j */
   const int64_t *ksel;
   int64_t nk;
   const double *m, *l, *D;
   double *dk, *dv; /* [B, nk, Hkv, d] */
 } bwd_k_ctx_t;
 
-/* One item = one (b, hk, selected key row). scratch: v_j (d), dk' (d), dv (d), dO_i (d). */
+/* One item = one (b, hk, selected key row j).  Key j is seen by query rows i >= j - (Nk - Nq).
+ * scratch: v_j (d), dk' (d), dv (d), dO_i (d). */
 static void bwd_k_item(void *vctx, int64_t item, double *scratch) {
   bwd_k_ctx_t *c = (bwd_k_ctx_t *)vctx;
-  int N = c->N, d = c->d;
+  int Nq = c->Nq, Nk = c->Nk, d = c->d;
   int64_t sl = item % c->nk;
   int hk = (int)((item / c->nk) % c->Hkv);
   int b = (int)(item / (c->nk * c->Hkv));
   int64_t j = c->ksel ? c->ksel[sl] : sl;
+  int64_t first = j - (int64_t)(Nk - Nq);
+  if (first < 0) first = 0;
   int g = c->Hq / c->Hkv;
   double *vj = scratch, *dkr = scratch + d, *dvj = scratch + 2 * d, *dOi = scratch + 3 * d;
-  size_t vbase = (((size_t)b * N + (size_t)j) * c->Hkv + hk) * d;
+  size_t vbase = (((size_t)b * Nk + (size_t)j) * c->Hkv + hk) * d;
   for (int e = 0; e < d; ++e) {
     vj[e] = load_elem(c->v, c->dtype, vbase + e);
     dkr[e] = 0.0;
@@ -447,11 +453,11 @@ static void bwd_k_item(void *vctx, int64_t item, double *scratch) {
   const double *kj = c->krot + vbase;
   double scale = 1.0 / sqrt((double)d);
   for (int h = hk * g; h < (hk + 1) * g; ++h) {
-    for (int64_t i = j; i < N; ++i) { /* causal: query rows i >= j see key j */
-      const double *qi = c->qrot + (((size_t)b * N + (size_t)i) * c->Hq + h) * d;
-      size_t st = ((size_t)b * c->Hq + h) * N + (size_t)i;
+    for (int64_t i = first; i < Nq; ++i) { /* causal: query rows that see key j */
+      const double *qi = c->qrot + (((size_t)b * Nq + (size_t)i) * c->Hq + h) * d;
+      size_t st = ((size_t)b * c->Hq + h) * Nq + (size_t)i;
       double p = exp(dot_d(qi, kj, d) * scale - c->m[st]) / c->l[st];
-      size_t obase = (((size_t)b * N + (size_t)i) * c->Hq + h) * d;
+      size_t obase = (((size_t)b * Nq + (size_t)i) * c->Hq + h) * d;
       for (int e = 0; e < d; ++e) dOi[e] = load_elem(c->dout, c->dtype, obase + e);
       double dP = dot_d(dOi, vj, d);
       double dS = p * (dP - c->D[st]);
@@ -462,7 +468,7 @@ static void bwd_k_item(void *vctx, int64_t item, double *scratch) {
     }
   }
   size_t obase = (((size_t)b * c->nk + (size_t)sl) * c->Hkv + hk) * d;
-  double kp = c->kpos ? c->kpos[(size_t)b * N + (size_t)j] : (double)j;
+  double kp = c->kpos ? c->kpos[(size_t)b * Nk + (size_t)j] : (double)j;
   rope_rotate_vec(dkr, c->dk + obase, c->form, -kp, c->theta); /* R(p_j)^T */
   for (int e = 0; e < d; ++e) c->dv[obase + e] = dvj[e];
 }
@@ -473,7 +479,8 @@ typedef struct {
   int H, N;
   rope_form_t form;
   const double *theta;
-  const double *pos; /* [B, N] positions, or NULL: n */
+  const double *pos; /* [B, N] positions, or NULL: pos_off + n */
+  int pos_off;
   double *out;
 } rot_all_ctx_t;
 
@@ -481,7 +488,7 @@ typedef struct {
 static void rot_all_item(void *vctx, int64_t bn, double *scratch) {
   rot_all_ctx_t *c = (rot_all_ctx_t *)vctx;
   int d = c->form.d;
-  double pos = c->pos ? c->pos[bn] : (double)(bn % c->N);
+  double pos = c->pos ? c->pos[bn] : (double)(c->pos_off + bn % c->N);
   for (int h = 0; h < c->H; ++h) {
     size_t base = ((size_t)bn * c->H + h) * d;
     for (int e = 0; e < d; ++e) scratch[e] = load_elem(c->x, c->dtype, base + e);
@@ -489,48 +496,48 @@ static void rot_all_item(void *vctx, int64_t bn, double *scratch) {
   }
 }
 
-/* q_pos, k_pos: [B, N] rotation positions (NULL: the token index), as for entry 3. */
-int orc_rope_causal_bwd_ex(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,
-                           int Hkv, int N, int d, int rotary_dim, int interleaved, double base, const double *q_pos,
-                           const double *k_pos, const int64_t *q_rows, int64_t nq, const int64_t *k_rows, int64_t nk,
-                           double *dq, double *dk, double *dv, int nthreads) {
+/* q_pos [B, Nq], k_pos [B, Nk]: rotation positions (NULL: the defaults), as for entry 3. */
+int orc_rope_causal_bwd_kv(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,
+                           int Hkv, int Nq, int Nk, int d, int rotary_dim, int interleaved, double base,
+                           const double *q_pos, const double *k_pos, const int64_t *q_rows, int64_t nq,
+                           const int64_t *k_rows, int64_t nk, double *dq, double *dk, double *dv, int nthreads) {
   rope_form_t f = {d, rotary_dim, interleaved};
-  if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 1 || Hq < 1 || Hkv < 1 || N < 1 || !form_ok(f) ||
-      (Hq % Hkv) != 0)
+  if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < Nq ||
+      !form_ok(f) || (Hq % Hkv) != 0)
     return -1;
-  if (!q_rows) nq = N;
-  if (!k_rows) nk = N;
+  if (!q_rows) nq = Nq;
+  if (!k_rows) nk = Nk;
   if (nq < 0 || nk < 0) return -1;
   for (int64_t s = 0; q_rows && s < nq; ++s)
-    if (q_rows[s] < 0 || q_rows[s] >= N) return -1;
+    if (q_rows[s] < 0 || q_rows[s] >= Nq) return -1;
   for (int64_t s = 0; k_rows && s < nk; ++s)
-    if (k_rows[s] < 0 || k_rows[s] >= N) return -1;
+    if (k_rows[s] < 0 || k_rows[s] >= Nk) return -1;
 
-  size_t nst = (size_t)B * Hq * N;
+  size_t nst = (size_t)B * Hq * Nq;
   double *theta = (double *)malloc(sizeof(double) * (size_t)(f.r / 2));
-  double *qrot = (double *)malloc(sizeof(double) * (size_t)B * N * Hq * d);
-  double *krot = (double *)malloc(sizeof(double) * (size_t)B * N * Hkv * d);
+  double *qrot = (double *)malloc(sizeof(double) * (size_t)B * Nq * Hq * d);
+  double *krot = (double *)malloc(sizeof(double) * (size_t)B * Nk * Hkv * d);
   double *stats = (double *)malloc(sizeof(double) * 3 * nst);
-  int64_t *qslot = (int64_t *)malloc(sizeof(int64_t) * (size_t)N);
+  int64_t *qslot = (int64_t *)malloc(sizeof(int64_t) * (size_t)Nq);
   int rc = -1;
   if (theta && qrot && krot && stats && qslot) {
     rope_frequencies(f.r, base, theta);
-    for (int64_t i = 0; i < N; ++i) qslot[i] = q_rows ? -1 : i;
+    for (int64_t i = 0; i < Nq; ++i) qslot[i] = q_rows ? -1 : i;
     for (int64_t s = 0; q_rows && s < nq; ++s) qslot[q_rows[s]] = s;
-    rot_all_ctx_t rq = {q, dtype, Hq, N, f, theta, q_pos, qrot};
-    orc_pool_t p1 = {rot_all_item, &rq, (int64_t)B * N, 0, (size_t)d, 0};
-    rot_all_ctx_t rk = {k, dtype, Hkv, N, f, theta, k_pos, krot};
-    orc_pool_t p2 = {rot_all_item, &rk, (int64_t)B * N, 0, (size_t)d, 0};
+    rot_all_ctx_t rq = {q, dtype, Hq, Nq, f, theta, q_pos, Nk - Nq, qrot};
+    orc_pool_t p1 = {rot_all_item, &rq, (int64_t)B * Nq, 0, (size_t)d, 0};
+    rot_all_ctx_t rk = {k, dtype, Hkv, Nk, f, theta, k_pos, 0, krot};
+    orc_pool_t p2 = {rot_all_item, &rk, (int64_t)B * Nk, 0, (size_t)d, 0};
     rc = orc_run(&p1, nthreads);
     if (rc == 0) rc = orc_run(&p2, nthreads);
     if (rc == 0) {
-      bwd_q_ctx_t qc = {v, dout, dtype, B, Hq, Hkv, N, d, f, theta, qrot, krot, q_pos, qslot, nq, dq,
+      bwd_q_ctx_t qc = {v, dout, dtype, B, Hq, Hkv, Nq, Nk, d, f, theta, qrot, krot, q_pos, qslot, nq, dq,
                         stats, stats + nst, stats + 2 * nst};
-      orc_pool_t p3 = {bwd_q_item, &qc, (int64_t)B * Hq * N, 0, (size_t)(2 * d + 2 * N), 0};
+      orc_pool_t p3 = {bwd_q_item, &qc, (int64_t)B * Hq * Nq, 0, (size_t)(2 * d + 2 * Nk), 0};
       rc = orc_run(&p3, nthreads);
     }
     if (rc == 0 && nk > 0) {
-      bwd_k_ctx_t kc = {v, dout, dtype, B, Hq, Hkv, N, d, f, theta, qrot, krot, k_pos, k_rows, nk,
+      bwd_k_ctx_t kc = {v, dout, dtype, B, Hq, Hkv, Nq, Nk, d, f, theta, qrot, krot, k_pos, k_rows, nk,
                         stats, stats + nst, stats + 2 * nst, dk, dv};
       orc_pool_t p4 = {bwd_k_item, &kc, (int64_t)B * Hkv * nk, 0, (size_t)(4 * d), 0};
       rc = orc_run(&p4, nthreads);
@@ -542,6 +549,14 @@ int orc_rope_causal_bwd_ex(const void *q, const void *k, const void *v, const vo
   free(stats);
   free(qslot);
   return rc;
+}
+
+int orc_rope_causal_bwd_ex(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,
+                           int Hkv, int N, int d, int rotary_dim, int interleaved, double base, const double *q_pos,
+                           const double *k_pos, const int64_t *q_rows, int64_t nq, const int64_t *k_rows, int64_t nk,
+                           double *dq, double *dk, double *dv, int nthreads) {
+  return orc_rope_causal_bwd_kv(q, k, v, dout, dtype, B, Hq, Hkv, N, N, d, rotary_dim, interleaved, base, q_pos, k_pos,
+                                q_rows, nq, k_rows, nk, dq, dk, dv, nthreads);
 }
 
 int orc_rope_causal_bwd(const void *q, const void *k, const void *v, const void *dout, int dtype, int B, int Hq,

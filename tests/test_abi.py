@@ -219,3 +219,15 @@ def test_binding_rejects_host_tensors_before_the_library():
         binding.rope_apply(q, 1e4)
     with pytest.raises(ValueError):
         binding.rope_causal_bwd(q, kv, kv, q, lse, q, 1e4)
+
+
+def test_backward_workspace_with_more_keys_than_queries():
+    # q' over N tokens, k' over Nk = kv_len, D over N (float), each rounded up to 256 bytes.
+    import torch
+    B, N, Nk, Hq, Hkv, d = 2, 130, 517, 8, 2, 128
+    up = lambda x: (x + 255) // 256 * 256
+    want = up(B * N * Hq * d * 2) + up(B * Nk * Hkv * d * 2) + up(B * Hq * N * 4)
+    assert binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16, kv_len=Nk) == want
+    assert binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16, kv_len=N) == \
+        binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16)
+    assert binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16, kv_len=N - 1) == 0

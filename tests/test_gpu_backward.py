@@ -159,3 +159,64 @@ def test_backward_explicit_index_positions_agree_with_the_default():
     for x, y in zip(a, b):
         err = (x.double() - y.double()).norm() / y.double().norm()
         assert float(err) <= 2.0 ** -7, float(err)
+
+
+PREFILL = [
+    # B, N, Nk, Hq, Hkv, d, dtype, rotary_dim, interleaved, explicit positions
+    (1, 128, 256, 2, 2, 64, "bf16", None, False, False),    # offset a whole tile
+    (1, 200, 333, 4, 2, 128, "bf16", None, False, False),   # ragged offset (133) and tails
+    (2, 130, 517, 8, 2, 128, "fp16", None, False, False),   # offset 387, GQA 4:1, two batch entries
+    (1, 1, 300, 4, 1, 64, "bf16", None, False, False),      # one query after 299 cached keys
+    (1, 64, 1000, 6, 3, 64, "fp16", None, False, False),    # many key tiles every query sees in full
+    (1, 190, 321, 4, 2, 128, "bf16", 64, False, False),     # partial rotary: the pass rotates back
+    (1, 150, 290, 2, 1, 64, "fp16", None, True, True),      # interleaved pairs, explicit positions
+]
+
+
+@pytest.mark.parametrize("B,N,Nk,Hq,Hkv,d,dt,r,il,pos", PREFILL)
+def test_backward_with_more_keys_than_queries_matches_oracle(B, N, Nk, Hq, Hkv, d, dt, r, il, pos):
+    # The queries are the last N of the Nk tokens (query i sees keys j <= Nk - N + i): the backward
+    # of a prefill that extends a cache.  The kernels start each key tile's query loop at the first
+    # query tile that sees it and mask where the offset diagonal crosses a tile.
+    q, k, v = inputs.make_kv_inputs(B, N, Nk, Hq, Hkv, d, dt, seed=N + Nk + d)
+    g = torch.Generator().manual_seed(N + Nk)
+    dout = torch.randn(q.shape, generator=g).to(q.dtype)
+    qp = inputs.make_positions(B, N, seed=N) if pos else None
+    kp = inputs.make_positions(B, Nk, seed=Nk) if pos else None
+    kw = dict(rotary_dim=r, interleaved=il)
+    dev = dict(kw, q_positions=None if qp is None else qp.cuda(), k_positions=None if kp is None else kp.cuda())
+    qc, kc, vc, dc = q.cuda(), k.cuda(), v.cuda(), dout.cuda()
+    o, l = binding.rope_causal_fwd(qc, kc, vc, 1e4, mode="prerotate", **dev)
+    dq, dk, dv = binding.rope_causal_bwd(qc, kc, vc, o, l, dc, 1e4, **dev)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert dk.shape == k.shape and dv.shape == v.shape
+    rq, rk, rv = oracle.rope_causal_bwd(q, k, v, dout, 1e4, q_positions=None if qp is None else qp.numpy(),
+                                        k_positions=None if kp is None else kp.numpy(), **kw)
+    label = f"{B}x{N}/{Nk}x{Hq}/{Hkv}x{d} {dt} r={r} il={il} pos={pos}"
+    assert_grad_close(dq.cpu(), rq, dt, "dq " + label)
+    assert_grad_close(dk.cpu(), rk, dt, "dk " + label)
+    assert_grad_close(dv.cpu(), rv, dt, "dv " + label)
+
+
+def test_backward_prefill_is_the_full_backward_restricted_to_the_last_queries():
+    # Nk tokens with zero dout on the first Nk - N queries: the full (N = Nk) backward gives the same
+    # dk, dv as the prefill backward over the last N queries, and its dq rows there are the
+    # prefill's dq.  Both routes on the GPU; the match is up to the two forwards' rounding of out.
+    B, N, Nk, Hq, Hkv, d = 1, 170, 420, 4, 2, 128
+    q_all, k, v = inputs.make_kv_inputs(B, Nk, Nk, Hq, Hkv, d, "bf16", seed=5)
+    g = torch.Generator().manual_seed(6)
+    dout_all = torch.randn(q_all.shape, generator=g).to(q_all.dtype)
+    dout_all[:, : Nk - N] = 0
+    qc, kc, vc = q_all.cuda(), k.cuda(), v.cuda()
+    o, l = binding.rope_causal_fwd(qc, kc, vc, 1e4)
+    fq, fk, fv = binding.rope_causal_bwd(qc, kc, vc, o, l, dout_all.cuda(), 1e4)
+    qs, ds = qc[:, Nk - N:].contiguous(), dout_all[:, Nk - N:].contiguous().cuda()
+    o2, l2 = binding.rope_causal_fwd(qs, kc, vc, 1e4)
+    pq, pk, pv = binding.rope_causal_bwd(qs, kc, vc, o2, l2, ds, 1e4)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    for x, y, name in ((pq, fq[:, Nk - N:], "dq"), (pk, fk, "dk"), (pv, fv, "dv")):
+        err = (x.double() - y.double()).norm() / y.double().norm()
+        assert float(err) <= BTOL["bf16"]["rel_l2"] / 2, (name, float(err))
+

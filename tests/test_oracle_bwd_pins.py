@@ -120,3 +120,79 @@ def test_gqa_key_gradients_sum_the_group():
     _, dk_m, dv_m = oracle.rope_causal_bwd(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2), dout, 1e4)
     np.testing.assert_allclose(dk[:, :, 0], dk_m.sum(axis=2), rtol=0, atol=1e-13)
     np.testing.assert_allclose(dv[:, :, 0], dv_m.sum(axis=2), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# More keys than queries (a prefill against a cache): the Nq queries are the last Nq of Nk tokens.
+
+
+@pytest.mark.parametrize("Nq,Nk,Hq,Hkv,d,r,il,pos", [(5, 9, 2, 1, 8, None, False, False), (1, 6, 4, 2, 16, None, False, False),
+                                                     (3, 11, 2, 2, 16, 8, True, False), (4, 7, 2, 1, 8, None, False, True)])
+def test_prefill_gradients_match_finite_differences(Nq, Nk, Hq, Hkv, d, r, il, pos):
+    B, base = 2, 100.0
+    q, k, v = _rand((B, Nq, Hq, d), 11), _rand((B, Nk, Hkv, d), 12), _rand((B, Nk, Hkv, d), 13)
+    dout = _rand((B, Nq, Hq, d), 14)
+    kw = dict(rotary_dim=r, interleaved=il)
+    if pos:
+        rng0 = np.random.default_rng(31)
+        kw.update(q_positions=rng0.integers(-50, 300, size=(B, Nq)), k_positions=rng0.integers(-50, 300, size=(B, Nk)))
+    dq, dk, dv = oracle.rope_causal_bwd(q, k, v, dout, base, **kw)
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    eps = 1e-6
+    rng = np.random.default_rng(15)
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(12):
+            idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(**{**args, name: xp}, dout=dout, base=base, **kw)
+            lm = _loss(**{**args, name: xm}, dout=dout, base=base, **kw)
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - g[idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, g[idx])
+
+
+def _rope_torch_at(x, pos, base):
+    """RoPE (half-split pairs) at the given token positions, as complex multiplication.  x: [B, N, H, d]."""
+    B, N, H, d = x.shape
+    h = d // 2
+    theta = base ** (-2.0 * torch.arange(h, dtype=torch.float64) / d)
+    ang = torch.as_tensor(pos, dtype=torch.float64)[:, None] * theta[None, :]
+    z = torch.complex(x[..., :h], x[..., h:]) * torch.polar(torch.ones_like(ang), ang)[None, :, None, :]
+    return torch.cat([z.real, z.imag], dim=-1)
+
+
+def test_prefill_gradients_match_torch_autograd():
+    # queries at positions Nk - Nq + i, keys at j, query i sees keys j <= Nk - Nq + i (bottom-right)
+    B, Nq, Nk, Hq, Hkv, d, base = 2, 13, 40, 4, 2, 16, 1e4
+    q = torch.tensor(_rand((B, Nq, Hq, d), 16), requires_grad=True)
+    k = torch.tensor(_rand((B, Nk, Hkv, d), 17), requires_grad=True)
+    v = torch.tensor(_rand((B, Nk, Hkv, d), 18), requires_grad=True)
+    dout = torch.tensor(_rand((B, Nq, Hq, d), 19))
+    g, off = Hq // Hkv, Nk - Nq
+    qr = _rope_torch_at(q, np.arange(off, Nk), base).transpose(1, 2)
+    kr = _rope_torch_at(k, np.arange(Nk), base).repeat_interleave(g, dim=2).transpose(1, 2)
+    vr = v.repeat_interleave(g, dim=2).transpose(1, 2)
+    mask = torch.arange(Nk)[None, :] <= (off + torch.arange(Nq))[:, None]
+    out = torch.nn.functional.scaled_dot_product_attention(qr, kr, vr, attn_mask=mask).transpose(1, 2)
+    (out * dout).sum().backward()
+    dq, dk, dv = oracle.rope_causal_bwd(q.detach().numpy(), k.detach().numpy(), v.detach().numpy(), dout.numpy(), base)
+    np.testing.assert_allclose(dq, q.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, k.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, v.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_prefill_is_the_full_backward_with_zero_gradient_on_the_cached_rows():
+    # With dout = 0 on the first Nk - Nq query rows of a full causal problem over Nk tokens, those
+    # rows add nothing to any gradient, and the last Nq rows are the prefill's queries.
+    B, Nq, Nk, Hq, Hkv, d, base = 1, 6, 20, 2, 1, 16, 1e4
+    q, k, v = _rand((B, Nk, Hq, d), 20), _rand((B, Nk, Hkv, d), 21), _rand((B, Nk, Hkv, d), 22)
+    dout = _rand((B, Nk, Hq, d), 23)
+    dout[:, : Nk - Nq] = 0.0
+    dq_full, dk_full, dv_full = oracle.rope_causal_bwd(q, k, v, dout, base)
+    dq, dk, dv = oracle.rope_causal_bwd(q[:, Nk - Nq:], k, v, dout[:, Nk - Nq:], base)
+    np.testing.assert_allclose(dq, dq_full[:, Nk - Nq:], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, dk_full, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, dv_full, rtol=0, atol=1e-13)
+    assert np.all(dq_full[:, : Nk - Nq] == 0.0)

@@ -41,8 +41,8 @@ MUTANTS = {
         ("  for (int64_t j = 0; j <= last; ++j) {\n    double p = score[j] / denom;",
          "  for (int64_t j = 0; j < last + (last == 0); ++j) {\n    double p = score[j] / denom;")],
     "GQA head map h mod Hkv": [("int hk = h / g; /* GQA", "int hk = h % c->Hkv; /* GQA")],
-    "softmax scale missing": [("  double scale = 1.0 / sqrt((double)d);\n  double mx = -INFINITY;\n  for (int64_t j = 0; j <= last",
-                               "  double scale = 1.0;\n  double mx = -INFINITY;\n  for (int64_t j = 0; j <= last")],
+    "softmax scale missing": [("  double scale = 1.0 / sqrt((double)d);\n  double mx = -INFINITY;\n  for (int64_t j = 0; j <= last; ++j) { /*",
+                               "  double scale = 1.0;\n  double mx = -INFINITY;\n  for (int64_t j = 0; j <= last; ++j) { /*")],
     "lse in log2 units": [("= mx + log(denom);", "= mx + log2(denom);")],
     "lse without the max": [("score[j] = exp(score[j] - mx);", "score[j] = exp(score[j]);")],
     "probabilities not normalised": [("double p = score[j] / denom;", "double p = score[j];")],
@@ -57,7 +57,10 @@ MUTANTS = {
     # more keys than queries, explicit positions
     "query i sees keys j <= i with extra keys": [("int64_t last = (int64_t)(c->Nk - c->Nq) + i;",
                                                   "int64_t last = i;")],
-    "default query position i": [(": (double)last;", ": (double)i;")],
+    "default query position i": [("c->qpos[(size_t)b * c->Nq + (size_t)i] : (double)last;",
+                                  "c->qpos[(size_t)b * c->Nq + (size_t)i] : (double)i;")],
+    "dq rotated back at position i": [("c->qpos[(size_t)b * Nq + (size_t)i] : (double)last;",
+                                       "c->qpos[(size_t)b * Nq + (size_t)i] : (double)i;")],
     "key positions without the batch stride": [("double pos = c->kpos ? c->kpos[bj] : (double)j;",
                                                 "double pos = c->kpos ? c->kpos[j] : (double)j;")],
     "query positions without the batch stride": [("c->qpos[(size_t)b * c->Nq + (size_t)i]", "c->qpos[(size_t)i]")],
@@ -76,7 +79,10 @@ MUTANTS = {
     "dk without the scale": [("dkr[e] += dS * qi[e] * scale;", "dkr[e] += dS * qi[e];")],
     "dq without the scale": [("for (int e = 0; e < d; ++e) dqr[e] += dS * kj[e] * scale;",
                               "for (int e = 0; e < d; ++e) dqr[e] += dS * kj[e];")],
-    "key pass skips the diagonal": [("for (int64_t i = j; i < N; ++i) {", "for (int64_t i = j + 1; i < N; ++i) {")],
+    "key pass skips the diagonal": [("for (int64_t i = first; i < Nq; ++i) {", "for (int64_t i = first + 1; i < Nq; ++i) {")],
+    "key pass without the cached queries' offset": [("int64_t first = j - (int64_t)(Nk - Nq);", "int64_t first = j;")],
+    "query pass mask without the offset": [("int64_t last = (int64_t)(Nk - Nq) + i;", "int64_t last = i;")],
+    "backward query position without the offset": [("(double)(c->pos_off + bn % c->N)", "(double)(bn % c->N)")],
     "key pass sums one head of the group": [("for (int h = hk * g; h < (hk + 1) * g; ++h) {",
                                              "for (int h = hk * g; h < hk * g + 1; ++h) {")],
 }
