@@ -77,6 +77,7 @@ struct __align__(8) BwdCtrl {
   uint32_t tmem_base;
   int abort_flag;
   int skip;
+  int unit_slot[8];                      // dQ: unit of the producer's k-th resident load at [k % 8]
 };
 static_assert(sizeof(BwdCtrl) <= 256, "control block");
 
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ A
   ptx::grid_dep_launch_dependents();
   ptx::grid_dep_wait();  // launched as a dependent of the pre-rotation pass
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tid == 0) *p.unit_ctr = 0;  // read by the dQ kernel, which starts after this grid completes
   const long long row = tid / TPR;
   const int part = (int)(tid % TPR);
   const long long rows = (long long)p.B * p.N * p.Hq;
@@ -217,8 +219,11 @@ __device__ __forceinline__ void issue_acc(uint32_t dst, uint32_t a, uint32_t b, 
 
 constexpr uint32_t kHalfRows = 64 * 128;  // byte offset of row 64 inside a 128-row box
 
-// Common prologue of both kernels: barriers, tensor memory, skip flag.
-template <int D>
+// Common prologue of both kernels: barriers, tensor memory, skip flag.  The dK/dV kernel waits for
+// the D kernel and only then lets the dQ kernel launch, so D, q' and k' are complete when the dQ
+// kernel starts; the dQ kernel reads nothing the dK/dV kernel writes and runs beside it (its CTAs
+// take the SMs the dK/dV CTAs leave), waiting for that grid only before it exits.
+template <int D, bool DQ>
 __device__ __forceinline__ void bwd_setup(BwdCtrl& ctl, int warp) {
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_addr(ctl.res_full), 1);
@@ -248,8 +253,12 @@ __device__ __forceinline__ void bwd_setup(BwdCtrl& ctl, int warp) {
   ptx::tc_fence_after();
   // Launched as a programmatic dependent of the previous kernel in the chain: the set-up above
   // overlaps its end; nothing it wrote is read before this wait.
-  ptx::grid_dep_launch_dependents();
-  ptx::grid_dep_wait();
+  if constexpr (DQ) {
+    ptx::grid_dep_launch_dependents();
+  } else {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
+  }
 }
 
 __device__ __forceinline__ void bwd_teardown(BwdCtrl& ctl, int warp, uint32_t tmem) {
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
 
-  bwd_setup<D>(ctl, warp);
+  bwd_setup<D, false>(ctl, warp);
   const uint32_t tmem = ctl.tmem_base;
   const bool skip = __shfl_sync(0xFFFFFFFFu, ctl.skip, 0) != 0;
   const unsigned long long tmo = p.timeout_ns;
@@ -528,6 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ================================ dQ ======================================================
 // Unit u: query tile t = nt - 1 - u / (B Hq) (descending: the longest units first) of head h, batch
 // b; steps: the key tiles j of KV head h / g that some row of the tile sees (0 .. t when N == Nk).
+// Units are handed out in that order by a global counter: the producer takes the next one when it
+// has room for a resident pair and publishes it in the control block before the pair's copies
+// (the resident barrier's completion makes it visible to the other roles); a CTA that starts late,
+// on an SM a dK/dV CTA has just left, simply takes fewer units.  A value >= the unit count, posted
+// with a copy-less arrival on the resident barrier, ends every role.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -548,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
 
-  bwd_setup<D>(ctl, warp);
+  bwd_setup<D, true>(ctl, warp);
   const uint32_t tmem = ctl.tmem_base;
   const bool skip = __shfl_sync(0xFFFFFFFFu, ctl.skip, 0) != 0;
   const unsigned long long tmo = p.timeout_ns;
@@ -565,12 +579,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int gs = 0, uc = 0;
     bool ok = true;
-    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
-      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
-      if (u >= total) break;
-      const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
+    for (;;) {
       if (!(ok = wait_warp(bar_addr(ctl.res_empty), (uc & 1) ^ 1, ctl, tmo))) break;
+      int u = 0;
+      if (lane == 0) u = atomicAdd(p.unit_ctr, 1);
+      u = __shfl_sync(0xFFFFFFFFu, u, 0);
+      if (u >= total) {
+        if (lane == 0) {
+          ctl.unit_slot[uc & 7] = total;
+          ptx::mbar_arrive(bar_addr(ctl.res_full));
+        }
+        break;
+      }
+      const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
       if (lane == 0) {
+        ctl.unit_slot[uc & 7] = u;
         ptx::mbar_arrive_expect_tx(bar_addr(ctl.res_full), 2 * C::TILE);
         tma_tile<D>(sQ, &tmQ, bar_addr(ctl.res_full), h, t * BM, b);
         tma_tile<D>(sO, &tmO, bar_addr(ctl.res_full), h, t * BM, b);
@@ -601,11 +624,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_kmajor<D>(tmem + COL_DP + 64 * half, sO, sV, IDESC_S);  // dP = dO V^T
       ptx::mma_commit_w(bar_addr(ctl.s_full[half]));
     };
-    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
-      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+    for (;;) {
+      if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
+      const int u = *reinterpret_cast<volatile int*>(&ctl.unit_slot[uc & 7]);
       if (u >= total) break;
       const int t = nt - 1 - u / bh_count;
-      if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
       if (!(ok = wait_warp(bar_addr(ctl.ring_full[gs & 1]), (gs >> 1) & 1, ctl, tmo))) break;
       ptx::tc_fence_after();
       issue_s(gs, 0);
@@ -648,8 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     int gs = 0, uc = 0;
     bool ok = true;
-    for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
-      const int u = unit_of_round(rnd, blockIdx.x, gridDim.x);
+    for (;;) {
+      if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
+      const int u = *reinterpret_cast<volatile int*>(&ctl.unit_slot[uc & 7]);
       if (u >= total) break;
       const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
       const int i = t * BM + r;
@@ -734,6 +758,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   bwd_teardown(ctl, warp, tmem);
+  // The grid completes only after the dK/dV grid it ran beside, so whatever follows on the stream
+  // (the pass that rotates dq and dk back, the caller's work) sees both gradients.
+  ptx::grid_dep_wait();
 }
 
 // Launch as a programmatic dependent of the previous kernel on the stream (it waits in-kernel).

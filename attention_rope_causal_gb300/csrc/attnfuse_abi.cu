@@ -613,7 +613,7 @@ size_t attnfuse_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, att
   const int Nk = (opts && opts->kv_len) ? opts->kv_len : N;
   if (Nk < N) return 0;
   return round_up(tensor_bytes(B, N, Hq, d), 256) + round_up(tensor_bytes(B, Nk, Hkv, d), 256) +
-         round_up((size_t)B * Hq * N * sizeof(float), 256);
+         round_up((size_t)B * Hq * N * sizeof(float), 256) + 256;  // + the dQ kernel's unit counter
 }
 
 attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -664,6 +664,7 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   void* qr = ws;
   void* kr = static_cast<char*>(ws) + round_up(tensor_bytes(B, N, Hq, d), 256);
   float* Dv = reinterpret_cast<float*>(static_cast<char*>(kr) + round_up(tensor_bytes(B, Nk, Hkv, d), 256));
+  int* unit_ctr = reinterpret_cast<int*>(reinterpret_cast<char*>(Dv) + round_up((size_t)B * Hq * N * sizeof(float), 256));
 
   AttnBwdParams p;
   std::memset(&p, 0, sizeof p);
@@ -686,6 +687,7 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   p.inv_sqrt_d = (float)(1.0 / std::sqrt((double)d));
   p.unrotate = plain_form ? 1 : 0;
   p.timeout_ns = kTimeoutNs;
+  p.unit_ctr = unit_ctr;
   rope_freqs_host(d, rope_base, &p.freqs);
 
   // One pre-rotation launch per tensor (queries at q_off + i or q_positions over N tokens, keys at j

@@ -166,6 +166,7 @@ struct AttnBwdParams {
   int unrotate;           // 1: the epilogues apply R^T (half-split over all d, positions q_off + i and j);
                           // 0: they write the gradients in the rotated frame (a pass rotates back)
   unsigned long long timeout_ns;
+  int* unit_ctr;          // workspace: next unit of the dQ kernel (zeroed by the D kernel)
   RopeFreqs freqs;        // F_k, k < d/2 (half-split, rotary dimension d)
 };
 

@@ -181,8 +181,9 @@ attnfuse_status_t attnfuse_rope_apply_ex(const void* x, void* y, int B, int N, i
  * (GQA: a KV head's dk, dv sum over its query heads; L's dependence on lse is not propagated).
  * Layouts as the forward: q, out, dout, dq [B, N, Hq, d]; k, v, dk, dv [B, N, Hkv, d]; lse
  * [B, Hq, N] float32 (required).  Outputs must not overlap the inputs.  `workspace` holds
- * attnfuse_bwd_workspace_bytes(...) bytes (rotated q and k, and D); NULL allocates with
- * cudaMallocAsync / cudaFreeAsync on `stream`.  Errors as for the forward.
+ * attnfuse_bwd_workspace_bytes(...) bytes (rotated q and k, D, a work counter) and serves one call
+ * at a time; NULL allocates with cudaMallocAsync / cudaFreeAsync on `stream`.  Errors as for the
+ * forward.
  */
 attnfuse_status_t attnfuse_rope_causal_bwd(const void* q, const void* k, const void* v, const void* out,
                                            const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
@@ -208,7 +209,9 @@ size_t attnfuse_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfu
 
 /* Bytes of workspace attnfuse_rope_causal_bwd_ex needs with these options: rotated q [B, N, Hq, d],
  * rotated k [B, Nk, Hkv, d] (Nk = kv_len, 0 meaning N) and D [B, Hq, N] float, each rounded up to
- * 256 bytes (0 for invalid arguments). */
+ * 256 bytes, then 256 bytes for the dQ kernel's work counter (0 for invalid arguments).  One
+ * workspace serves one call at a time: calls in flight together on different streams need their
+ * own. */
 size_t attnfuse_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfuse_dtype_t dtype,
                                        const attnfuse_rope_opts_t* opts);
 

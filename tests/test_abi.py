@@ -188,7 +188,8 @@ def test_backward_workspace_bytes(lib):
     q = 1 * 4096 * 32 * 128 * 2
     k = 1 * 4096 * 8 * 128 * 2
     dvec = 32 * 4096 * 4
-    assert lib.attnfuse_bwd_workspace_bytes(1, 32, 8, 4096, 128, 0) == q + k + dvec
+    counter = 256  # the dQ kernel's work counter
+    assert lib.attnfuse_bwd_workspace_bytes(1, 32, 8, 4096, 128, 0) == q + k + dvec + counter
     assert lib.attnfuse_bwd_workspace_bytes(1, 32, 8, 4096, 96, 0) == 0
     assert lib.attnfuse_bwd_workspace_bytes(0, 32, 8, 4096, 128, 0) == 0
 
@@ -222,11 +223,12 @@ def test_binding_rejects_host_tensors_before_the_library():
 
 
 def test_backward_workspace_with_more_keys_than_queries():
-    # q' over N tokens, k' over Nk = kv_len, D over N (float), each rounded up to 256 bytes.
+    # q' over N tokens, k' over Nk = kv_len, D over N (float), each rounded up to 256 bytes, and 256
+    # bytes for the dQ kernel's work counter.
     import torch
     B, N, Nk, Hq, Hkv, d = 2, 130, 517, 8, 2, 128
     up = lambda x: (x + 255) // 256 * 256
-    want = up(B * N * Hq * d * 2) + up(B * Nk * Hkv * d * 2) + up(B * Hq * N * 4)
+    want = up(B * N * Hq * d * 2) + up(B * Nk * Hkv * d * 2) + up(B * Hq * N * 4) + 256
     assert binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16, kv_len=Nk) == want
     assert binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16, kv_len=N) == \
         binding.bwd_workspace_bytes(B, Hq, Hkv, N, d, torch.bfloat16)
