@@ -124,14 +124,20 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D, bool BF16>
+// R8: at most 8 query rows per KV head (every decode step with groups of up to 8 heads, two tokens of
+// groups of four).  The products then use only rows 0..7 of the 16-row tiles, so P V runs
+// transposed, O^T = V^T P^T (M = 16 columns of d, N = the 8 rows, K = 16 keys), with P taken
+// straight from the score fragments as the B operand; each lane keeps one softmax row.
+template <int D, bool BF16, bool R8>
 __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   using C = DecCfg<D>;
   constexpr int NT = D / 8;    // 8-column output tiles of P V
+  constexpr int MT = D / 16;   // R8: 16-column tiles of O^T
   constexpr int KS = D / 16;   // k-steps of Q K^T
+  constexpr int NH = R8 ? 1 : 2;  // fragment row halves in use: rows g8 (h = 0) and g8 + 8 (h = 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle: 1024-byte aligned boxes
@@ -243,11 +249,13 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
     *reinterpret_cast<uint32_t*>(sQh + row * C::QSTRIDE + e) = w;
   }
   __syncthreads();
-  // Q as A fragments, one per k-step (16 columns), for the whole key loop
+  // Q as A fragments, one per k-step (16 columns), for the whole key loop (R8: rows 8..15 are zero)
   uint32_t qa[KS][4];
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks)
+  for (int ks = 0; ks < KS; ++ks) {
     ldsm_x4(ptx::smem_u32(sQh + (lane % 16) * C::QSTRIDE + 16 * ks + 8 * (lane / 16)), qa[ks]);
+    if constexpr (R8) qa[ks][1] = qa[ks][3] = 0u;
+  }
 
   // Per lane: rows g8 and g8 + 8 of the fragments; last visible key of each (-1: a padding row).
   int lim[2];
@@ -256,10 +264,14 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
     const int row = g8 + 8 * h;
     lim[h] = row < rows ? min(key_end - 1, p.q_off + row % p.N) : -1;
   }
+  // Chunks whose keys are all at or before this one are visible to every row (padding rows have no
+  // output, so what they compute does not matter): they skip the mask.
+  const int lim_all = min(key_end - 1, p.q_off);
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float o[NT][4];
+  constexpr int NACC = R8 ? MT : NT;
+  float o[NACC][4];  // R8: O^T tiles (columns 16 mt + g8 (+8) of rows 2 t4, 2 t4 + 1); else O tiles
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  for (int nt = 0; nt < NACC; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
   // Key rotation items of this lane: rotation group fg, rows rsub + RS pass of each chunk.
   const int fg = lane % C::GPR, rsub = lane / C::GPR;
@@ -317,9 +329,12 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
       }
     }
     // ---- online softmax on the fragments: rows g8 (h = 0) and g8 + 8 (h = 1) ----------------------
-    uint32_t pa[kKSteps][4];  // P as the A fragments of the 16-key steps of P V
+    const bool masked = j0 + kChunk - 1 > lim_all;  // warp-uniform
+    uint32_t pa[kKSteps][4];  // P as the A fragments of the 16-key steps of P V (R8: [0], [2] used)
+    bool moved = false;       // some row's running max changed (its O needs the rescale)
+    float alpha[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       float sv[2 * kTiles];
       float mx = -INFINITY;
 #pragma unroll
@@ -327,15 +342,16 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int j = j0 + 8 * nt + 2 * t4 + e;
-          const float v = j <= lim[h] ? sc[nt][2 * h + e] * p.scale_log2 : -INFINITY;
+          const float v = (!masked || j <= lim[h]) ? sc[nt][2 * h + e] * p.scale_log2 : -INFINITY;
           sv[2 * nt + e] = v;
           mx = fmaxf(mx, v);
         }
       mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
       const float m_new = fmaxf(m_run[h], mx);
+      moved |= m_new != m_run[h];
       // a row that has seen no visible key keeps m = -inf, P = 0, O = 0
-      const float alpha = m_run[h] == -INFINITY ? 0.f : ptx::ex2_approx(m_run[h] - m_new);
+      alpha[h] = m_run[h] == -INFINITY ? 0.f : ptx::ex2_approx(m_run[h] - m_new);
       float pv[2 * kTiles], sum = 0.f;
 #pragma unroll
       for (int e = 0; e < 2 * kTiles; ++e) {
@@ -344,31 +360,65 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
       }
       sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
       sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-      l_run[h] = l_run[h] * alpha + sum;
+      l_run[h] = l_run[h] * alpha[h] + sum;
       m_run[h] = m_new;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        o[nt][2 * h] *= alpha;
-        o[nt][2 * h + 1] *= alpha;
-      }
       // Score tiles 2 kk and 2 kk + 1 (keys 16 kk .. 16 kk + 15) form the A fragment of key step kk:
-      // a0 / a1 = tile 2 kk, rows g8 / g8 + 8; a2 / a3 = tile 2 kk + 1, rows g8 / g8 + 8.
+      // a0 / a1 = tile 2 kk, rows g8 / g8 + 8; a2 / a3 = tile 2 kk + 1, rows g8 / g8 + 8.  (R8: a0 and
+      // a2 are also the B fragment of O^T += V^T P^T for row g8.)
 #pragma unroll
       for (int kk = 0; kk < kKSteps; ++kk) {
         pa[kk][h] = Pack<BF16>::pack(pv[4 * kk], pv[4 * kk + 1]);
         pa[kk][2 + h] = Pack<BF16>::pack(pv[4 * kk + 2], pv[4 * kk + 3]);
       }
     }
-    // ---- O += P V: 16 keys per step, 16 columns per ldmatrix ------------------------------------
+    // rescale O where a running max moved (most chunks after the first few move none)
+    if (__any_sync(0xFFFFFFFFu, moved)) {
+      if constexpr (R8) {
+        // this lane's O^T columns are rows 2 t4 and 2 t4 + 1, whose alpha lanes 8 t4 and 8 t4 + 4 hold
+        const float a0 = __shfl_sync(0xFFFFFFFFu, alpha[0], 8 * t4);
+        const float a1 = __shfl_sync(0xFFFFFFFFu, alpha[0], 8 * t4 + 4);
 #pragma unroll
-    for (int kk = 0; kk < kKSteps; ++kk) {
-      const int vrow = 16 * kk + (lane % 8) + 8 * ((lane / 8) % 2);
+        for (int mt = 0; mt < MT; ++mt) {
+          o[mt][0] *= a0;
+          o[mt][1] *= a1;
+          o[mt][2] *= a0;
+          o[mt][3] *= a1;
+        }
+      } else {
 #pragma unroll
-      for (int n2 = 0; n2 < NT / 2; ++n2) {
-        uint32_t bv[4];  // keys 16 kk .. +15, columns 16 n2 .. +7 (bv[0..1]) and +8 .. +15 (bv[2..3])
-        ldsm_x4_trans(vst + sw_off(vrow, 2 * n2 + lane / 16), bv);
-        mma_16816<BF16>(o[2 * n2], pa[kk], bv[0], bv[1]);
-        mma_16816<BF16>(o[2 * n2 + 1], pa[kk], bv[2], bv[3]);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            o[nt][2 * h] *= alpha[h];
+            o[nt][2 * h + 1] *= alpha[h];
+          }
+      }
+    }
+    if constexpr (R8) {
+      // ---- O^T += V^T P^T: per 16 columns of d one ldmatrix (transposed) of V and one MMA ---------
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        // matrices: keys 16 kk + 0..7 / + 8..15 (lane / 16) x columns 16 mt + 0..7 / + 8..15 ((lane / 8) % 2)
+        const int vrow = 16 * kk + (lane % 8) + 8 * (lane / 16);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t av[4];
+          ldsm_x4_trans(vst + sw_off(vrow, 2 * mt + (lane / 8) % 2), av);
+          mma_16816<BF16>(o[mt], av, pa[kk][0], pa[kk][2]);
+        }
+      }
+    } else {
+      // ---- O += P V: 16 keys per step, 16 columns per ldmatrix ----------------------------------
+#pragma unroll
+      for (int kk = 0; kk < kKSteps; ++kk) {
+        const int vrow = 16 * kk + (lane % 8) + 8 * ((lane / 8) % 2);
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          uint32_t bv[4];  // keys 16 kk .. +15, columns 16 n2 .. +7 (bv[0..1]) and +8 .. +15 (bv[2..3])
+          ldsm_x4_trans(vst + sw_off(vrow, 2 * n2 + lane / 16), bv);
+          mma_16816<BF16>(o[2 * n2], pa[kk], bv[0], bv[1]);
+          mma_16816<BF16>(o[2 * n2 + 1], pa[kk], bv[2], bv[3]);
+        }
       }
     }
     __syncwarp();
@@ -396,16 +446,27 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
   float* mO = reinterpret_cast<float*>(sgen + C::OFF_RING);     // [warps][16][D]
   float* mM = mO + kWarps * kDecodeMaxRows * D;                 // [warps][16]
   float* mL = mM + kWarps * kDecodeMaxRows;                     // [warps][16]
+  if constexpr (R8) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int row = g8 + 8 * h, col = 8 * nt + 2 * t4;
-      *reinterpret_cast<float2*>(mO + (warp * kDecodeMaxRows + row) * D + col) = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
-    }
+      for (int e = 0; e < 4; ++e) {
+        const int row = 2 * t4 + (e & 1), col = 16 * mt + g8 + 8 * (e >> 1);
+        mO[(warp * kDecodeMaxRows + row) * D + col] = o[mt][e];
+      }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = g8 + 8 * h, col = 8 * nt + 2 * t4;
+        *reinterpret_cast<float2*>(mO + (warp * kDecodeMaxRows + row) * D + col) =
+            make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+      }
+  }
   if (t4 == 0)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       mM[warp * kDecodeMaxRows + g8 + 8 * h] = m_run[h];
       mL[warp * kDecodeMaxRows + g8 + 8 * h] = l_run[h];
     }
@@ -523,21 +584,28 @@ __global__ void __launch_bounds__(kCombineThreads) attn_decode_combine_kernel(co
   }
 }
 
-template <int D, bool BF16>
-cudaError_t launch_decode_impl(const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+template <int D, bool BF16, bool R8>
+cudaError_t launch_decode_kernel(const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
   static DeviceOnce once;  // shared-memory attribute set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int unused = 0;
   e = once.get(dev, [](int*) -> cudaError_t {
-    return cudaFuncSetAttribute(attn_decode_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(attn_decode_kernel<D, BF16, R8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)DecCfg<D>::SMEM);
   }, &unused);
   if (e != cudaSuccess) return e;
-  attn_decode_kernel<D, BF16><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(kThreads),
-                                DecCfg<D>::SMEM, stream>>>(maps.k, maps.v, p);
-  e = cudaGetLastError();
+  attn_decode_kernel<D, BF16, R8><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(kThreads),
+                                    DecCfg<D>::SMEM, stream>>>(maps.k, maps.v, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_decode_impl(const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+  const int rows = (p.Hq / p.Hkv) * p.N;
+  cudaError_t e = rows <= 8 ? launch_decode_kernel<D, BF16, true>(maps, p, stream)
+                            : launch_decode_kernel<D, BF16, false>(maps, p, stream);
   if (e != cudaSuccess) return e;
   if (p.n_splits > kMaxSplits) return cudaErrorInvalidConfiguration;
   // Programmatic dependent launch: the combine grid's launch overlaps the decode grid's tail.

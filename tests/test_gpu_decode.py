@@ -21,10 +21,10 @@ CASES = [
     # B, N, Nk, Hq, Hkv, d, dtype, rotary_dim, interleaved, positions
     (1, 1, 4096, 32, 8, 128, "bf16", None, False, False),   # one decode step, Llama-3-8B heads
     (4, 1, 1000, 32, 8, 128, "fp16", None, False, False),   # ragged split tail, 32 KV heads
-    (16, 1, 300, 8, 4, 128, "bf16", None, False, False),    # 64 KV heads, one 64-key chunk per slice
-    (32, 1, 1024, 16, 4, 128, "bf16", None, False, False),  # 128 KV heads, two slices of 8 chunks
-    (304, 1, 2048, 1, 1, 64, "bf16", None, False, False),   # one slice of 32 chunks: the key cos/sin
-                                                            # walk is recomputed exactly at chunk 16
+    (16, 1, 300, 8, 4, 128, "bf16", None, False, False),    # 64 KV heads, two slices, ragged last chunk
+    (32, 1, 1024, 16, 4, 128, "bf16", None, False, False),  # 128 KV heads, one slice each
+    (304, 1, 2304, 1, 1, 64, "bf16", None, False, False),   # one slice of 144 chunks, 18 per warp: the
+                                                            # key cos/sin walk is exact again at chunk 16
     (2, 4, 777, 8, 2, 64, "bf16", None, False, False),      # speculative decode, 16 rows (the maximum)
     (1, 16, 2048, 16, 4, 128, "bf16", None, False, False),  # 64 rows per KV head: the tile kernels
     (1, 8, 300, 8, 8, 64, "fp16", None, False, False),      # MHA
@@ -33,6 +33,9 @@ CASES = [
                                                             # see none of its keys (empty partials)
     (2, 3, 500, 8, 2, 128, "bf16", 64, True, False),        # RoPE variant
     (2, 2, 640, 4, 2, 64, "fp16", None, False, True),       # explicit positions
+    (2, 2, 500, 8, 4, 128, "bf16", 64, True, False),        # 4 rows, two queries (per-row masks), variant
+    (1, 2, 1000, 16, 4, 128, "fp16", None, False, False),   # 8 rows: the most the 8-row form takes
+    (3, 1, 2100, 8, 1, 128, "bf16", None, False, True),     # 8 heads per KV head, explicit positions
 ]
 
 
