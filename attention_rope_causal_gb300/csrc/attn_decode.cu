@@ -9,19 +9,19 @@
 // ("AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraphs 1-2: RoPE on Q
 // and K before the product, causal mask, softmax).
 //
-// attn_decode_kernel: one CTA per (KV head, slice of keys_per_split keys, batch), eight warps that
-// never wait on one another inside the key loop.  The slice is cut into 16-key chunks; warp w takes
-// chunks w, w + 8, w + 16, ... and owns a ring of three shared-memory stages, each holding one chunk's
-// K and V rows, filled by TMA (cp.async.bulk.tensor, 128-byte swizzle) on the warp's own mbarriers,
-// so up to three chunks per warp are in flight while it computes.  Per chunk the warp rotates the
-// chunk's K rows in place (cos/sin carried along the warp's rows and chunks by angle addition,
-// exact again every 16 chunks; exact per key with explicit positions; rounded to the input type
-// like the other paths), computes S = Q K^T for the <= 16 query rows as m16n8k16 tensor-core tiles
-// (Q fragments kept in registers), runs the online softmax on the fragments in registers (exp2,
-// fp32 max and sum), and adds P V with P passed straight from the score fragments to the operand
-// fragments (P rounded to the input type).  At the end the four warps' partial (O, max, sum) are
-// merged in shared memory and the CTA writes the slice's partial.  Eight warps of one CTA per SM at
-// d = 128 (two CTAs at d = 64) keep 16 chunks per SM in flight while eight warps compute.
+// attn_decode_kernel: one CTA per (KV head, slice of keys_per_split keys, batch), W warps (eight, or
+// twelve in one form, decode_warps) that never wait on one another inside the key loop.  The slice
+// is cut into 16-key chunks; warp w takes chunks w, w + W, w + 2 W, ... and owns a ring of
+// shared-memory stages (three, or two with twelve warps), each holding one chunk's K and V rows,
+// filled by TMA (cp.async.bulk.tensor, 128-byte swizzle) on the warp's own mbarriers, so the warp's
+// next chunks are in flight while it computes.  Per chunk the warp rotates the chunk's K rows in
+// place (cos/sin carried along the warp's rows and chunks by angle addition, exact again every 16
+// chunks; exact per key with explicit positions; rounded to the input type like the other paths),
+// computes S = Q K^T for the <= 16 query rows as m16n8k16 tensor-core tiles (Q fragments kept in
+// registers), runs the online softmax on the fragments in registers (exp2, fp32 max and sum), and
+// adds P V with P passed straight from the score fragments to the operand fragments (P rounded to
+// the input type).  At the end the warps' partial (O, max, sum) are merged in shared memory and the
+// CTA writes the slice's partial.  One CTA per SM at d = 128 (192 KB of rings), two at d = 64.
 // attn_decode_combine_kernel: one CTA per (row, KV head, batch) merges the slices (rescaling each by
 // 2^(m_s - m)) into out and lse; launched as a programmatic dependent of the first kernel, it waits
 // (griddepcontrol.wait) for that grid to complete before reading the partials.
@@ -42,16 +42,13 @@ __device__ unsigned int g_decode_status = 0;
 
 namespace {
 
-constexpr int kWarps = kDecodeWarps;
-constexpr int kThreads = 32 * kWarps;
 constexpr int kChunk = kDecodeChunk;  // keys per chunk (one TMA box of rows)
 constexpr int kTiles = kChunk / 8;    // 8-key score tiles per chunk
 constexpr int kKSteps = kChunk / 16;  // 16-key steps of P V per chunk
-constexpr int kStagesPerWarp = 3;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
-template <int D>
+template <int D, int kWarps, int kStagesPerWarp>
 struct DecCfg {
   static constexpr uint32_t BOX = kChunk * 128;                 // kChunk rows x 64 16-bit columns, swizzled
   static constexpr uint32_t KBYTES = (D / 64) * BOX;            // one chunk of K (or V)
@@ -128,12 +125,13 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity) {
 // groups of four).  The products then use only rows 0..7 of the 16-row tiles, so P V runs
 // transposed, O^T = V^T P^T (M = 16 columns of d, N = the 8 rows, K = 16 keys), with P taken
 // straight from the score fragments as the B operand; each lane keeps one softmax row.
-template <int D, bool BF16, bool R8>
-__global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
+template <int D, bool BF16, bool R8, int W>
+__global__ void __launch_bounds__(32 * W, decode_ctas_per_sm(D))
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  using C = DecCfg<D>;
+  constexpr int kWarps = W, kThreads = 32 * kWarps, kStagesPerWarp = decode_stages(W);
+  using C = DecCfg<D, kWarps, kStagesPerWarp>;
   constexpr int NT = D / 8;    // 8-column output tiles of P V
   constexpr int MT = D / 16;   // R8: 16-column tiles of O^T
   constexpr int KS = D / 16;   // k-steps of Q K^T
@@ -499,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, decode_ctas_per_sm(D))
 // sums the O rows of every 4th split (lane = 4 or 2 consecutive columns) with loads that do not
 // depend on one another; a shared-memory pass adds the 4 warps' sums.  Two rounds of loads in all,
 // whatever the number of splits.
-// 128 threads: with the decode kernel's 226 registers x 256 threads on an SM, a combine CTA still
-// fits beside it (registers and shared memory), so the programmatic dependent's CTAs are resident
-// and waiting when the decode grid finishes.
+// 128 threads: beside an eight-warp decode CTA (at most 228 registers x 256 threads) a combine CTA
+// still fits (registers and shared memory), so the programmatic dependent's CTAs are resident and
+// waiting when the decode grid finishes; beside the twelve-warp form they take the SMs it leaves.
 constexpr int kCombineThreads = 128;
 constexpr int kMaxSplits = 1024;  // decode_plan never makes more
 
@@ -584,28 +582,36 @@ __global__ void __launch_bounds__(kCombineThreads) attn_decode_combine_kernel(co
   }
 }
 
-template <int D, bool BF16, bool R8>
+template <int D, bool BF16, bool R8, int W>
 cudaError_t launch_decode_kernel(const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
+  using Cfg = DecCfg<D, W, decode_stages(W)>;
   static DeviceOnce once;  // shared-memory attribute set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int unused = 0;
   e = once.get(dev, [](int*) -> cudaError_t {
-    return cudaFuncSetAttribute(attn_decode_kernel<D, BF16, R8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)DecCfg<D>::SMEM);
+    return cudaFuncSetAttribute(attn_decode_kernel<D, BF16, R8, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg::SMEM);
   }, &unused);
   if (e != cudaSuccess) return e;
-  attn_decode_kernel<D, BF16, R8><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(kThreads),
-                                    DecCfg<D>::SMEM, stream>>>(maps.k, maps.v, p);
+  attn_decode_kernel<D, BF16, R8, W><<<dim3((unsigned)p.Hkv, (unsigned)p.n_splits, (unsigned)p.B), dim3(32 * W),
+                                       Cfg::SMEM, stream>>>(maps.k, maps.v, p);
   return cudaGetLastError();
 }
 
 template <int D, bool BF16>
 cudaError_t launch_decode_impl(const DecodeMaps& maps, const DecodeParams& p, cudaStream_t stream) {
   const int rows = (p.Hq / p.Hkv) * p.N;
-  cudaError_t e = rows <= 8 ? launch_decode_kernel<D, BF16, true>(maps, p, stream)
-                            : launch_decode_kernel<D, BF16, false>(maps, p, stream);
+  cudaError_t e;
+  if (rows > 8) {
+    e = launch_decode_kernel<D, BF16, false, 8>(maps, p, stream);
+  } else if constexpr (D == 128) {
+    e = p.warps == 12 ? launch_decode_kernel<D, BF16, true, 12>(maps, p, stream)
+                      : launch_decode_kernel<D, BF16, true, 8>(maps, p, stream);
+  } else {
+    e = launch_decode_kernel<D, BF16, true, 8>(maps, p, stream);
+  }
   if (e != cudaSuccess) return e;
   if (p.n_splits > kMaxSplits) return cudaErrorInvalidConfiguration;
   // Programmatic dependent launch: the combine grid's launch overlaps the decode grid's tail.

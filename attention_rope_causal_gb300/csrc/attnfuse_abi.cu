@@ -194,12 +194,13 @@ bool decode_eligible(int B, int Hq, int Hkv, int N, attnfuse_mode_t mode) {
   return rows <= kDecodeMaxRows && B <= 65535 && Hkv <= 65535;  // grid limits
 }
 
-// Splits of the keys, in 32-key chunks: the number of slices that minimises (waves of CTAs) x
+// Splits of the keys, in 16-key chunks: the number of slices that minimises (waves of CTAs) x
 // (chunks per warp of a slice + a CTA's fixed work, about three chunks' time) with
-// decode_ctas_per_sm(d) CTAs resident per SM on 152 SMs and kDecodeWarps warps per CTA, fewest
-// slices among equals (each slice adds a partial to merge).  A slice count rounded up past a whole
-// wave would double the time.
-void decode_plan(int B, int Hkv, int Nk, int d, int* keys_per_split, int* n_splits) {
+// decode_ctas_per_sm(d) CTAs resident per SM on 152 SMs and decode_warps(B, Hkv, d, rows) warps per
+// CTA, fewest slices among equals (each slice adds a partial to merge).  A slice count rounded up
+// past a whole wave would double the time.
+void decode_plan(int B, int Hkv, int Nk, int d, int rows, int* keys_per_split, int* n_splits) {
+  const int warps = decode_warps(B, Hkv, d, rows);
   const long long kSlots = 152LL * decode_ctas_per_sm(d);
   constexpr long long kFixedChunks = 3;
   const int chunks = (Nk + kDecodeChunk - 1) / kDecodeChunk;
@@ -211,7 +212,7 @@ void decode_plan(int B, int Hkv, int Nk, int d, int* keys_per_split, int* n_spli
     const int per = (chunks + s - 1) / s;
     const long long n = (chunks + per - 1) / per;  // slices actually needed
     const long long waves = (heads * n + kSlots - 1) / kSlots;
-    const long long cost = waves * ((per + kDecodeWarps - 1) / kDecodeWarps + kFixedChunks);
+    const long long cost = waves * ((per + warps - 1) / warps + kFixedChunks);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_per = per;
@@ -221,9 +222,9 @@ void decode_plan(int B, int Hkv, int Nk, int d, int* keys_per_split, int* n_spli
   *n_splits = (Nk + *keys_per_split - 1) / *keys_per_split;
 }
 
-size_t decode_workspace_bytes(int B, int Hkv, int Nk, int d) {
+size_t decode_workspace_bytes(int B, int Hkv, int Nk, int d, int rows) {
   int kps = 0, ns = 0;
-  decode_plan(B, Hkv, Nk, d, &kps, &ns);
+  decode_plan(B, Hkv, Nk, d, rows, &kps, &ns);
   const size_t slots = (size_t)B * Hkv * ns * kDecodeMaxRows;
   return round_up(slots * d * sizeof(float), 256) + round_up(slots * 2 * sizeof(float), 256);
 }
@@ -342,7 +343,7 @@ size_t attnfuse_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, attnfus
   const int Nk = (opts && opts->kv_len) ? opts->kv_len : N;
   if (Nk < N) return 0;
   if (Hq % Hkv != 0) return 0;
-  if (decode_eligible(B, Hq, Hkv, N, mode)) return decode_workspace_bytes(B, Hkv, Nk, d);
+  if (decode_eligible(B, Hq, Hkv, N, mode)) return decode_workspace_bytes(B, Hkv, Nk, d, (Hq / Hkv) * N);
   if (mode == ATTNFUSE_AUTO) mode = attnfuse_select_mode(B, Hq, Hkv, Nk, d, dtype);
   if (mode == ATTNFUSE_SPLIT) return round_up(tensor_bytes(B, Nk, Hkv, d), 256);
   if (mode != ATTNFUSE_PREROTATE) return 0;  // FUSED, NONE
@@ -444,7 +445,8 @@ attnfuse_status_t attnfuse_rope_causal_fwd_ex(const void* q, const void* k, cons
     dp.kpos = o.kpos;
     dp.rot_chunks = o.rdim / 16;
     dp.interleaved = o.interleaved;
-    decode_plan(B, Hkv, Nk, d, &dp.keys_per_split, &dp.n_splits);
+    decode_plan(B, Hkv, Nk, d, (Hq / Hkv) * N, &dp.keys_per_split, &dp.n_splits);
+    dp.warps = decode_warps(B, Hkv, d, (Hq / Hkv) * N);
     dp.scale_log2 = (float)(1.4426950408889634074 / std::sqrt((double)d));
     rope_freqs_host(o.rdim, rope_base, &dp.freqs);
     void* owned = nullptr;

@@ -110,12 +110,19 @@ cudaError_t launch_attn_fwd(const AttnMaps& maps, const AttnParams& p, int d, bo
 
 constexpr int kDecodeMaxRows = 16;  // query rows per KV head: (Hq / Hkv) * N
 
-// Decode CTAs (eight warps, each with a ring of three 16-key stages) resident per SM: the kernel's
-// launch bounds and the key-slice planner both follow it.  The rings take 192 KB of shared memory
-// at d = 128 (one CTA) and 96 KB at d = 64 (two).
+// Decode CTAs resident per SM, warps per CTA and 16-key shared-memory stages per warp: the kernel's
+// launch bounds and the key-slice planner both follow them.  At d = 128 one CTA per SM of eight
+// warps with three stages each, or -- the 8-row form (at most 8 query rows per KV head) with more
+// than 16 (batch, KV head) pairs -- twelve warps with two stages each (its 168 registers a thread
+// let twelve warps share the register file; 192 KB of rings either way); at d = 64 two CTAs of
+// eight warps with three stages (96 KB each).  With at most 16 pairs (one wave of CTAs, long
+// slices) the deeper rings of eight warps measured faster; with more, the extra warps.
 constexpr int decode_ctas_per_sm(int d) { return d == 64 ? 2 : 1; }
+__host__ __device__ constexpr int decode_stages(int warps) { return warps == 12 ? 2 : 3; }
+constexpr int decode_warps(int B, int Hkv, int d, int rows) {
+  return d == 128 && rows <= 8 && (long long)B * Hkv > 16 ? 12 : 8;
+}
 constexpr int kDecodeChunk = 16;  // keys per TMA box and per step of a decode warp
-constexpr int kDecodeWarps = 8;   // warps per decode CTA, each walking every eighth chunk
 
 struct DecodeParams {
   const void* q;          // [B, N, Hq, d]
@@ -130,6 +137,7 @@ struct DecodeParams {
   int interleaved;
   int keys_per_split;     // multiple of kDecodeChunk
   int n_splits;
+  int warps;              // decode_warps(B, Hkv, d, rows): the kernel form the planner assumed
   float scale_log2;       // log2(e) / sqrt(d)
   float* part_o;          // [B, Hkv, n_splits, rows, d] unnormalised partial outputs
   float* part_ml;         // [B, Hkv, n_splits, rows, 2]: running max (log2 units) and sum

@@ -36,6 +36,10 @@ CASES = [
     (2, 2, 500, 8, 4, 128, "bf16", 64, True, False),        # 4 rows, two queries (per-row masks), variant
     (1, 2, 1000, 16, 4, 128, "fp16", None, False, False),   # 8 rows: the most the 8-row form takes
     (3, 1, 2100, 8, 1, 128, "bf16", None, False, True),     # 8 heads per KV head, explicit positions
+    # more than 16 (batch, KV head) pairs at d = 128 with at most 8 rows: the twelve-warp form
+    (6, 2, 700, 16, 4, 128, "bf16", 96, True, True),        # per-row masks, variant, explicit positions
+    (152, 1, 3300, 1, 1, 128, "bf16", None, False, False),  # one slice of 207 chunks, 17 or 18 per warp:
+                                                            # the key cos/sin walk is exact again at 16
 ]
 
 
