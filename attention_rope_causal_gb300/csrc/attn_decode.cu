@@ -492,25 +492,26 @@ __global__ void __launch_bounds__(32 * W, decode_ctas_per_sm(D))
 }
 
 // One CTA of 128 threads per (row, KV head, batch): m = max_s m_s, w_s = 2^(m_s - m),
-// l = sum_s l_s w_s, out = sum_s O_s w_s / l, lse = ln 2 (m + log2 l).  The splits' (m, l) pairs
-// are read in one pass by as many threads, the weights go to shared memory, and each of the 4 warps
-// sums the O rows of every 4th split (lane = 4 or 2 consecutive columns) with loads that do not
-// depend on one another; a shared-memory pass adds the 4 warps' sums.  Two rounds of loads in all,
-// whatever the number of splits.
+// l = sum_s l_s w_s, out = sum_s O_s w_s / l, lse = ln 2 (m + log2 l).  Warp w takes splits w,
+// w + 4, w + 8, ... in batches of kBatch: every load of a batch -- each split's (m, l) pair and the
+// lane's 4 (or 2) columns of its O row -- is issued before any is used, so up to 4 kBatch = 32
+// splits cost one round of loads; the warp merges its batches online (running max, rescaled sums),
+// and a shared-memory pass merges the 4 warps.  A split with no visible key of this row has m =
+// -inf (weight 0).
 // 128 threads: beside an eight-warp decode CTA (at most 228 registers x 256 threads) a combine CTA
 // still fits (registers and shared memory), so the programmatic dependent's CTAs are resident and
 // waiting when the decode grid finishes; beside the twelve-warp form they take the SMs it leaves.
 constexpr int kCombineThreads = 128;
 constexpr int kMaxSplits = 1024;  // decode_plan never makes more
+constexpr int kBatch = 8;         // splits per warp whose loads are in flight together
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kCombineThreads) attn_decode_combine_kernel(const __grid_constant__ DecodeParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr int NW = kCombineThreads / 32;
   constexpr int PER = D / 32;  // columns per lane
-  __shared__ float s_w[kMaxSplits];
-  __shared__ float s_red[NW][D];
-  __shared__ float s_part[2][NW];
+  __shared__ float s_acc[NW][D];
+  __shared__ float s_ml[NW][2];
   const int row = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g = p.Hq / p.Hkv;
@@ -518,64 +519,74 @@ __global__ void __launch_bounds__(kCombineThreads) attn_decode_combine_kernel(co
   const size_t base = ((size_t)b * p.Hkv + hk) * p.n_splits * kDecodeMaxRows + row;
   const int S = p.n_splits;
   ptx::grid_dep_wait();  // the partials of every split are complete and visible
-  // (m, l) of this thread's splits; a split with no visible key of this row has m = -inf (weight 0)
-  float m_loc = -INFINITY;
-  for (int s = tid; s < S; s += kCombineThreads) {
-    const float ms = p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2];
-    s_w[s] = ms;
-    m_loc = fmaxf(m_loc, ms);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m_loc = fmaxf(m_loc, __shfl_xor_sync(0xFFFFFFFFu, m_loc, off));
-  if (lane == 0) s_part[0][warp] = m_loc;
-  __syncthreads();
-  float m = s_part[0][0];
-#pragma unroll
-  for (int k = 1; k < NW; ++k) m = fmaxf(m, s_part[0][k]);
-  float l_loc = 0.f;
-  for (int s = tid; s < S; s += kCombineThreads) {
-    const float ms = s_w[s];
-    const float wgt = ms == -INFINITY ? 0.f : ptx::ex2_approx(ms - m);
-    s_w[s] = wgt;
-    if (wgt != 0.f) l_loc = fmaf(p.part_ml[(base + (size_t)s * kDecodeMaxRows) * 2 + 1], wgt, l_loc);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l_loc += __shfl_xor_sync(0xFFFFFFFFu, l_loc, off);
-  if (lane == 0) s_part[1][warp] = l_loc;
-  __syncthreads();
-  float acc[PER];
+  float m_w = -INFINITY, l_w = 0.f, acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int s = warp; s < S; s += NW) {
-    const float wu = s_w[s];
-    const float* o = p.part_o + (base + (size_t)s * kDecodeMaxRows) * D + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(o);
-      acc[0] = fmaf(v.x, wu, acc[0]);
-      acc[1] = fmaf(v.y, wu, acc[1]);
-      acc[2] = fmaf(v.z, wu, acc[2]);
-      acc[3] = fmaf(v.w, wu, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(o);
-      acc[0] = fmaf(v.x, wu, acc[0]);
-      acc[1] = fmaf(v.y, wu, acc[1]);
+  for (int s0 = warp; s0 < S; s0 += NW * kBatch) {
+    float ms[kBatch], ls[kBatch], os[kBatch][PER];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int sp = s0 + NW * k;
+      ms[k] = -INFINITY;
+      ls[k] = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) os[k][e] = 0.f;
+      if (sp < S) {
+        const size_t slot = base + (size_t)sp * kDecodeMaxRows;
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + slot * 2);
+        ms[k] = ml.x;
+        ls[k] = ml.y;
+        const float* o = p.part_o + slot * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(o);
+          os[k][0] = v.x;
+          os[k][1] = v.y;
+          os[k][2] = v.z;
+          os[k][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(o);
+          os[k][0] = v.x;
+          os[k][1] = v.y;
+        }
+      }
     }
+    float mb = m_w;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, ms[k]);
+    if (mb == -INFINITY) continue;  // nothing visible so far
+    const float r = m_w == -INFINITY ? 0.f : ptx::ex2_approx(m_w - mb);
+    l_w *= r;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] *= r;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const float wk = ms[k] == -INFINITY ? 0.f : ptx::ex2_approx(ms[k] - mb);
+      l_w = fmaf(ls[k], wk, l_w);
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(os[k][e], wk, acc[e]);
+    }
+    m_w = mb;
   }
 #pragma unroll
-  for (int e = 0; e < PER; ++e) s_red[warp][lane * PER + e] = acc[e];
+  for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
+  if (lane == 0) {
+    s_ml[warp][0] = m_w;
+    s_ml[warp][1] = l_w;
+  }
   __syncthreads();
   if (tid < D / 2) {
-    float l = 0.f;
+    float m = s_ml[0][0];
 #pragma unroll
-    for (int k = 0; k < NW; ++k) l += s_part[1][k];
-    const float inv = 1.f / l;
-    float x0 = 0.f, x1 = 0.f;
+    for (int k = 1; k < NW; ++k) m = fmaxf(m, s_ml[k][0]);
+    float l = 0.f, x0 = 0.f, x1 = 0.f;
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
-      x0 += s_red[k][2 * tid];
-      x1 += s_red[k][2 * tid + 1];
+      const float wk = s_ml[k][0] == -INFINITY ? 0.f : ptx::ex2_approx(s_ml[k][0] - m);
+      l = fmaf(s_ml[k][1], wk, l);
+      x0 = fmaf(s_acc[k][2 * tid], wk, x0);
+      x1 = fmaf(s_acc[k][2 * tid + 1], wk, x1);
     }
+    const float inv = 1.f / l;
     T* dst = reinterpret_cast<T*>(p.out) + (((size_t)b * p.N + i) * p.Hq + h) * D + 2 * tid;
     *reinterpret_cast<uint32_t*>(dst) = Pack<BF16>::pack(x0 * inv, x1 * inv);
     if (tid == 0 && p.lse != nullptr) p.lse[((size_t)b * p.Hq + h) * p.N + i] = (m + log2f(l)) * kLn2;
