@@ -273,6 +273,7 @@ class RopeCausalAttention(torch.autograd.Function):
 
 
 def rope_causal_attention(q, k, v, rope_base: float, mode: str = "auto", rotary_dim=None, interleaved: bool = False):
-    """Differentiable causal RoPE attention: returns out [B, N, Hq, d] (lse is kept for the backward)."""
+    """Differentiable causal RoPE attention: returns out [B, N, Hq, d] (lse is kept for the backward).
+    k, v may hold Nk >= N tokens (the queries are the last N); their gradients cover all Nk."""
     out, _ = RopeCausalAttention.apply(q, k, v, rope_base, mode, rotary_dim, interleaved)
     return out

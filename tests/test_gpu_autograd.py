@@ -34,3 +34,23 @@ def test_loss_backward_matches_oracle(mode, B, N, Hq, Hkv, d, dt, r, il):
         x = g.double().cpu().numpy()
         rel = ((x - rr) ** 2).sum() ** 0.5 / ((rr ** 2).sum() ** 0.5)
         assert rel <= BTOL[dt], (mode, name, rel)
+
+
+@pytest.mark.parametrize("mode", ["fused", "auto"])
+def test_loss_backward_with_a_cache_matches_oracle(mode):
+    # k, v hold more tokens than q (a prefill that extends a cache: the queries are the last N of the
+    # Nk tokens); the wrapper passes them through unchanged and the backward returns dk, dv over Nk.
+    B, N, Nk, Hq, Hkv, d = 1, 150, 410, 8, 2, 128
+    q, k, v = inputs.make_kv_inputs(B, N, Nk, Hq, Hkv, d, "bf16", seed=41)
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(42)).to(q.dtype)
+    qc, kc, vc = (t.cuda().requires_grad_(True) for t in (q, k, v))
+    out = binding.rope_causal_attention(qc, kc, vc, 1e4, mode=mode)
+    (out.float() * dout.cuda().float()).sum().backward()
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert kc.grad.shape == k.shape and vc.grad.shape == v.shape
+    ref = oracle.rope_causal_bwd(q, k, v, dout, 1e4)
+    for name, g, rr in zip(("dq", "dk", "dv"), (qc.grad, kc.grad, vc.grad), ref):
+        x = g.double().cpu().numpy()
+        rel = ((x - rr) ** 2).sum() ** 0.5 / ((rr ** 2).sum() ** 0.5)
+        assert rel <= BTOL["bf16"], (mode, name, rel)
