@@ -341,15 +341,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t0 = first_qtile(kt, p), nq = nt - t0;
       for (int s = 0; s < g * nq; ++s) {
         const int h = hk * g + s / nq, t = t0 + s % nq, st = gs & 1;
-        if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
-        // L = lse * log2(e) and D of the tile's 128 query rows (rows past N: L = +inf, so P = 0).
-        float* vL = sVec + st * 2 * BM;
+        // L = lse * log2(e) and D of the tile's 128 query rows (rows past N: L = +inf, so P = 0),
+        // read before the stage is free so that their latency overlaps the wait.
         const size_t rbase = ((size_t)b * p.Hq + h) * p.N;
+        float lv[4], dv4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int c = lane * 4 + k, row = t * BM + c;
-          vL[c] = row < p.N ? p.lse[rbase + row] * kLog2e : INFINITY;
-          vL[BM + c] = row < p.N ? p.Dvec[rbase + row] : 0.f;
+          const int row = t * BM + lane * 4 + k;
+          lv[k] = row < p.N ? p.lse[rbase + row] * kLog2e : INFINITY;
+          dv4[k] = row < p.N ? p.Dvec[rbase + row] : 0.f;
+        }
+        if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
+        float* vL = sVec + st * 2 * BM;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          vL[lane * 4 + k] = lv[k];
+          vL[BM + lane * 4 + k] = dv4[k];
         }
         __syncwarp();
         if (lane == 0) {
