@@ -566,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sgen = smem_raw + (sbase - raw);
   BwdCtrl& ctl = *reinterpret_cast<BwdCtrl*>(sgen + C::OFF_CTL);
   const uint32_t sQ = sbase + C::OFF_RES, sO = sQ + C::TILE, sRing = sbase + C::OFF_RING;
+  float* sVec = reinterpret_cast<float*>(sgen + C::OFF_VEC);  // this unit's L[128], D[128] (fp32)
   const int warp = __shfl_sync(0xFFFFFFFFu, (int)(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
 
@@ -586,11 +587,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int gs = 0, uc = 0;
     bool ok = true;
+    // Each unit is taken from the counter one unit ahead, and its rows' L = lse * log2(e) and D are
+    // read before the resident buffers are free: neither round trip sits between the previous
+    // unit's last product and this unit's copies.  The vectors go to shared memory with the unit.
+    int u_next = 0;
+    if (lane == 0) u_next = atomicAdd(p.unit_ctr, 1);
+    u_next = __shfl_sync(0xFFFFFFFFu, u_next, 0);
     for (;;) {
+      const int u = u_next;
+      float lv[4], dv4[4];
+      if (u < total) {
+        if (lane == 0) u_next = atomicAdd(p.unit_ctr, 1);
+        u_next = __shfl_sync(0xFFFFFFFFu, u_next, 0);
+        const int t_ = nt - 1 - u / bh_count, bh_ = u % bh_count, b_ = bh_ / p.Hq, h_ = bh_ - b_ * p.Hq;
+        const size_t rbase = ((size_t)b_ * p.Hq + h_) * p.N;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int row = t_ * BM + lane * 4 + k;
+          lv[k] = row < p.N ? p.lse[rbase + row] * kLog2e : INFINITY;  // rows past N: P = 0
+          dv4[k] = row < p.N ? p.Dvec[rbase + row] : 0.f;
+        }
+      }
       if (!(ok = wait_warp(bar_addr(ctl.res_empty), (uc & 1) ^ 1, ctl, tmo))) break;
-      int u = 0;
-      if (lane == 0) u = atomicAdd(p.unit_ctr, 1);
-      u = __shfl_sync(0xFFFFFFFFu, u, 0);
       if (u >= total) {
         if (lane == 0) {
           ctl.unit_slot[uc & 7] = total;
@@ -599,6 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sVec[lane * 4 + k] = lv[k];
+        sVec[BM + lane * 4 + k] = dv4[k];
+      }
+      __syncwarp();
       if (lane == 0) {
         ctl.unit_slot[uc & 7] = u;
         ptx::mbar_arrive_expect_tx(bar_addr(ctl.res_full), 2 * C::TILE);
@@ -684,9 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= total) break;
       const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
       const int i = t * BM + r;
-      const size_t srow = ((size_t)b * p.Hq + h) * p.N + i;
-      const float L = i < p.N ? p.lse[srow] * kLog2e : INFINITY;  // rows past N: P = 0
-      const float Dr = i < p.N ? p.Dvec[srow] : 0.f;
+      const float L = sVec[r], Dr = sVec[BM + r];  // staged by the producer with the unit
       const int nkj = qtile_keytiles(t, p);
       for (int j = 0; j < nkj; ++j) {
         if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
