@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int row = t * BM + lane * 4 + k;
-          lv[k] = row < p.N ? p.lse[rbase + row] * kLog2e : INFINITY;
+          lv[k] = row < p.N ? -(p.lse[rbase + row] * kLog2e) : -INFINITY;  // -L
           dv4[k] = row < p.N ? p.Dvec[rbase + row] : 0.f;
         }
         if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;      // key row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + COL_S, tP = tmem + lane_off + COL_DP, tA = tmem + lane_off + COL_ACC;
-    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     int gs = 0, uc = 0;
     bool ok = true;
     for (int rnd = 0; rnd * (int)gridDim.x < total && ok; ++rnd) {
@@ -453,17 +453,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld32(tP + q0, dv);
           ptx::tmem_wait_ld();
           uint32_t pp[16], dsp[16];
+          // Column pairs in fp32x2 arithmetic (the same IEEE operations): P = 2^(S sl2 - L),
+          // dS = P (dP - D); the vectors hold -L and D.
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int q = q0 + 2 * e;
-            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -vL[q]));
-            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -vL[q + 1]));
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2,
+                                       *reinterpret_cast<const uint64_t*>(vL + q)),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
             if (diag) {
               if (q < r - delta) p0 = 0.f;
               if (q + 1 < r - delta) p1 = 0.f;
             }
-            const float d0 = p0 * (__uint_as_float(dv[2 * e]) - vL[BM + q]);
-            const float d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - vL[BM + q + 1]);
+            const uint64_t dd = ptx::f2_sub(ptx::f2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])),
+                                            *reinterpret_cast<const uint64_t*>(vL + BM + q));
+            float d0, d1;
+            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), dd), d0, d1);
             pp[e] = pack2<BF16>(p0, p1);
             dsp[e] = pack2<BF16>(d0, d1);
           }
@@ -699,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;      // query row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + COL_S, tP = tmem + lane_off + COL_DP, tA = tmem + lane_off + COL_ACC;
-    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     int gs = 0, uc = 0;
     bool ok = true;
     for (;;) {
@@ -709,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = nt - 1 - u / bh_count, bh = u % bh_count, b = bh / p.Hq, h = bh - b * p.Hq;
       const int i = t * BM + r;
       const float L = sVec[r], Dr = sVec[BM + r];  // staged by the producer with the unit
+      const uint64_t nl2 = ptx::f2_pack(-L, -L), dr2 = ptx::f2_pack(Dr, Dr);
       const int nkj = qtile_keytiles(t, p);
       for (int j = 0; j < nkj; ++j) {
         if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
@@ -724,16 +732,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld32(tP + k0, dv);
           ptx::tmem_wait_ld();
           uint32_t dsp[16];
+          // Column pairs in fp32x2 arithmetic (the same IEEE operations): P = 2^(S sl2 - L), dS = P (dP - D).
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int k = k0 + 2 * e;
-            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -L));
-            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -L));
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2, nl2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
             if (diag) {
               if (k > r + delta) p0 = 0.f;
               if (k + 1 > r + delta) p1 = 0.f;
             }
-            dsp[e] = pack2<BF16>(p0 * (__uint_as_float(dv[2 * e]) - Dr), p1 * (__uint_as_float(dv[2 * e + 1]) - Dr));
+            const uint64_t dd = ptx::f2_sub(ptx::f2_pack(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), dr2);
+            float d0, d1;
+            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), dd), d0, d1);
+            dsp[e] = pack2<BF16>(d0, d1);
           }
           ptx::tmem_st16(tS + 64 * wg + 16 * c, dsp);
         }
