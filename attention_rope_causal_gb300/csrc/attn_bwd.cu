@@ -68,7 +68,8 @@ struct BwdCfg {
 
 struct __align__(8) BwdCtrl {
   uint64_t res_full, res_empty;          // resident pair landed / free again
-  uint64_t ring_full[2], ring_empty[2];  // ring stage landed / free again
+  uint64_t ring_full[4], ring_empty[2];  // ring stage st, rows 64 h .. 64 h + 63 landed (st * 2 + h) /
+                                         // stage free again
   uint64_t s_full[2];                    // S and dP of half h of this step are in tensor memory
   uint64_t p_ready[2];                   // warpgroup h wrote its P / dS (128 arrivals)
   uint64_t acc_full;                     // the unit's accumulators are complete
@@ -219,6 +220,16 @@ __device__ __forceinline__ void issue_acc(uint32_t dst, uint32_t a, uint32_t b, 
 
 constexpr uint32_t kHalfRows = 64 * 128;  // byte offset of row 64 inside a 128-row box
 
+// Rows 64 h .. 64 h + 63 of a 128-row tile through a tensor map whose box is 64 rows: they land at
+// their place in the tile's swizzled boxes (the 128-byte swizzle repeats every 8 rows).
+template <int D>
+__device__ __forceinline__ void tma_half(uint32_t tile, const CUtensorMap* map64, uint32_t bar, int head, int row0,
+                                         int h, int b) {
+#pragma unroll
+  for (int bx = 0; bx < D / 64; ++bx)
+    ptx::tma_load_4d(tile + bx * kBoxBytes + h * kHalfRows, map64, bar, bx * 64, head, row0 + 64 * h, b);
+}
+
 // Common prologue of both kernels: barriers, tensor memory, skip flag.  The dK/dV kernel waits for
 // the D kernel and only then lets the dQ kernel launch, so D, q' and k' are complete when the dQ
 // kernel starts; the dQ kernel reads nothing the dK/dV kernel writes and runs beside it (its CTAs
@@ -229,7 +240,8 @@ __device__ __forceinline__ void bwd_setup(BwdCtrl& ctl, int warp) {
     ptx::mbar_init(bar_addr(ctl.res_full), 1);
     ptx::mbar_init(bar_addr(ctl.res_empty), 1);
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar_addr(ctl.ring_full[s]), 1);
+      ptx::mbar_init(bar_addr(ctl.ring_full[2 * s]), 1);
+      ptx::mbar_init(bar_addr(ctl.ring_full[2 * s + 1]), 1);
       ptx::mbar_init(bar_addr(ctl.ring_empty[s]), 1);
     }
     for (int h = 0; h < 2; ++h) {
@@ -276,7 +288,8 @@ __device__ __forceinline__ void drain_copies(BwdCtrl& ctl, int res_loads, int ri
   const unsigned long long drain = 100000000ull;
   if (res_loads > 0) drain_bar(bar_addr(ctl.res_full), (res_loads - 1) & 1, drain);
   for (int s = 0; s < 2; ++s)
-    if (ring_loads > s) drain_bar(bar_addr(ctl.ring_full[s]), ((ring_loads - 1 - s) / 2) & 1, drain);
+    if (ring_loads > s)
+      for (int h = 0; h < 2; ++h) drain_bar(bar_addr(ctl.ring_full[2 * s + h]), ((ring_loads - 1 - s) / 2) & 1, drain);
 }
 
 template <int D>
@@ -360,10 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
+          // each half of the query rows on its own barrier: the half-steps start as their rows land
           const uint32_t sQ = sRing + st * 2 * C::TILE;
-          ptx::mbar_arrive_expect_tx(bar_addr(ctl.ring_full[st]), 2 * C::TILE);
-          tma_tile<D>(sQ, &tmQ, bar_addr(ctl.ring_full[st]), h, t * BM, b);
-          tma_tile<D>(sQ + C::TILE, &tmO, bar_addr(ctl.ring_full[st]), h, t * BM, b);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t bar = bar_addr(ctl.ring_full[2 * st + hh]);
+            ptx::mbar_arrive_expect_tx(bar, C::TILE);
+            tma_half<D>(sQ, &tmQ, bar, h, t * BM, hh, b);
+            tma_half<D>(sQ + C::TILE, &tmO, bar, h, t * BM, hh, b);
+          }
         }
         ++gs;
       }
@@ -388,10 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= total) break;
       const int kt = u / bh_count, nsteps = g * (nt - first_qtile(kt, p));
       if (!(ok = wait_warp(bar_addr(ctl.res_full), uc & 1, ctl, tmo))) break;
-      if (!(ok = wait_warp(bar_addr(ctl.ring_full[gs & 1]), (gs >> 1) & 1, ctl, tmo))) break;
-      ptx::tc_fence_after();
-      issue_s(gs, 0);
-      issue_s(gs, 1);
+      for (int half = 0; half < 2 && ok; ++half) {
+        if (!(ok = wait_warp(bar_addr(ctl.ring_full[2 * (gs & 1) + half]), (gs >> 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        issue_s(gs, half);
+      }
+      if (!ok) break;
       for (int s = 0; s < nsteps; ++s) {
         const int st = gs & 1;
         const uint32_t sQ = sRing + st * 2 * C::TILE, sO = sQ + C::TILE;
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_acc<D>(tmem + COL_ACC + D, tmem + COL_DP, sQ, IDESC_ACC, half, first);  // dK' += dS^T Q'
           if (half == 1) ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
           if (more) {
-            if (half == 0 && !(ok = wait_warp(bar_addr(ctl.ring_full[(gs + 1) & 1]), ((gs + 1) >> 1) & 1, ctl, tmo)))
+            if (!(ok = wait_warp(bar_addr(ctl.ring_full[2 * ((gs + 1) & 1) + half]), ((gs + 1) >> 1) & 1, ctl, tmo)))
               break;
             ptx::tc_fence_after();
             issue_s(gs + 1, half);
@@ -439,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < g * nq; ++s) {
         const int t = t0 + s % nq, st = gs & 1;
         if (!(ok = wait_warp(bar_addr(ctl.s_full[wg]), gs & 1, ctl, tmo))) break;
-        if (!(ok = wait_warp(bar_addr(ctl.ring_full[st]), (gs >> 1) & 1, ctl, tmo))) break;
+        if (!(ok = wait_warp(bar_addr(ctl.ring_full[2 * st + wg]), (gs >> 1) & 1, ctl, tmo))) break;
         ptx::tc_fence_after();
         const float* vL = sVec + st * 2 * BM;
         // query c of the tile sees key r iff c >= r - delta; only tiles with delta < 127 mask anything
@@ -641,10 +661,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = gs & 1;
         if (!(ok = wait_warp(bar_addr(ctl.ring_empty[st]), ((gs >> 1) & 1) ^ 1, ctl, tmo))) break;
         if (lane == 0) {
+          // each half of the key rows on its own barrier
           const uint32_t sK = sRing + st * 2 * C::TILE;
-          ptx::mbar_arrive_expect_tx(bar_addr(ctl.ring_full[st]), 2 * C::TILE);
-          tma_tile<D>(sK, &tmK, bar_addr(ctl.ring_full[st]), h / g, j * BM, b);
-          tma_tile<D>(sK + C::TILE, &tmV, bar_addr(ctl.ring_full[st]), h / g, j * BM, b);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t bar = bar_addr(ctl.ring_full[2 * st + hh]);
+            ptx::mbar_arrive_expect_tx(bar, C::TILE);
+            tma_half<D>(sK, &tmK, bar, h / g, j * BM, hh, b);
+            tma_half<D>(sK + C::TILE, &tmV, bar, h / g, j * BM, hh, b);
+          }
         }
         ++gs;
       }
@@ -667,10 +692,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = *reinterpret_cast<volatile int*>(&ctl.unit_slot[uc & 7]);
       if (u >= total) break;
       const int t = nt - 1 - u / bh_count;
-      if (!(ok = wait_warp(bar_addr(ctl.ring_full[gs & 1]), (gs >> 1) & 1, ctl, tmo))) break;
-      ptx::tc_fence_after();
-      issue_s(gs, 0);
-      issue_s(gs, 1);
+      for (int half = 0; half < 2 && ok; ++half) {
+        if (!(ok = wait_warp(bar_addr(ctl.ring_full[2 * (gs & 1) + half]), (gs >> 1) & 1, ctl, tmo))) break;
+        ptx::tc_fence_after();
+        issue_s(gs, half);
+      }
+      if (!ok) break;
       const int nkj = qtile_keytiles(t, p);
       for (int j = 0; j < nkj; ++j) {
         const int st = gs & 1;
@@ -684,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_acc<D>(tmem + COL_ACC, tmem + COL_S, sK, IDESC_ACC, half, j == 0 && half == 0);  // dQ' += dS K'
           if (half == 1) ptx::mma_commit_w(bar_addr(ctl.ring_empty[st]));
           if (more) {
-            if (half == 0 && !(ok = wait_warp(bar_addr(ctl.ring_full[(gs + 1) & 1]), ((gs + 1) >> 1) & 1, ctl, tmo)))
+            if (!(ok = wait_warp(bar_addr(ctl.ring_full[2 * ((gs + 1) & 1) + half]), ((gs + 1) >> 1) & 1, ctl, tmo)))
               break;
             ptx::tc_fence_after();
             issue_s(gs + 1, half);
@@ -827,7 +854,8 @@ cudaError_t launch_dependent(K kernel, dim3 grid, dim3 block, uint32_t smem, cud
 // One CTA per SM (shared memory admits one), each walking its share of the units.  TAG separates
 // the per-device set-up caches of kernels that share a signature.
 template <int TAG, typename K>
-cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const AttnBwdMaps& m, const AttnBwdParams& p,
+cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const CUtensorMap& mq, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const CUtensorMap& mo, const AttnBwdParams& p,
                               cudaStream_t stream) {
   static DeviceOnce once;  // attributes set and SM count kept per device
   int dev = 0;
@@ -841,7 +869,7 @@ cudaError_t launch_persistent(K kernel, uint32_t smem, int units, const AttnBwdM
   }, &sms);
   if (e != cudaSuccess) return e;
   const int grid = units < sms ? units : sms;
-  return launch_dependent(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, m.q, m.k, m.v, m.dout, p);
+  return launch_dependent(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, mq, mk, mv, mo, p);
 }
 
 template <int D, bool BF16>
@@ -851,11 +879,12 @@ cudaError_t launch_bwd_impl(const AttnBwdMaps& m, const AttnBwdParams& p, cudaSt
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = launch_dependent(bwd_prep_kernel<D, BF16>, dim3((unsigned)blocks), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
-  e = launch_persistent<2 * D + BF16 * 1>(bwd_dkdv_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hkv * p.n_ktiles, m, p,
-                                          stream);
+  // the dK/dV kernel streams q', dout in 64-row halves; the dQ kernel streams k', v in 64-row halves
+  e = launch_persistent<2 * D + BF16 * 1>(bwd_dkdv_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hkv * p.n_ktiles, m.q64,
+                                          m.k, m.v, m.dout64, p, stream);
   if (e != cudaSuccess) return e;
   return launch_persistent<2 * D + BF16 * 1 + 1000>(bwd_dq_kernel<D, BF16>, BwdCfg<D>::SMEM, p.B * p.Hq * p.n_tiles,
-                                                   m, p, stream);
+                                                   m.q, m.k64, m.v64, m.dout, p, stream);
 }
 
 }  // namespace

@@ -139,7 +139,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 attnfuse_status_t encode_bnhd_uncached(CUtensorMap* map, const void* ptr, int B, int N, int H, int d,
                                        attnfuse_dtype_t dtype, int box_rows, const char* name);
 
-// box_rows: tokens per box (128 for the attention tiles, 32 for the decode kernel's key chunks).
+// box_rows: tokens per box (128 for the attention tiles, 64 for the half tiles the backward streams, 16
+// for the decode kernel's key chunks).
 attnfuse_status_t encode_bnhd(CUtensorMap* map, const void* ptr, int B, int N, int H, int d, attnfuse_dtype_t dtype,
                               const char* name, int box_rows = 128) {
   struct Entry {
@@ -738,7 +739,11 @@ attnfuse_status_t attnfuse_rope_causal_bwd_ex(const void* q, const void* k, cons
   if (st == ATTNFUSE_OK && (st = encode_bnhd(&maps.q, qr, B, N, Hq, d, dtype, "q'")) == ATTNFUSE_OK &&
       (st = encode_bnhd(&maps.k, kr, B, Nk, Hkv, d, dtype, "k'")) == ATTNFUSE_OK &&
       (st = encode_bnhd(&maps.v, v, B, Nk, Hkv, d, dtype, "v")) == ATTNFUSE_OK &&
-      (st = encode_bnhd(&maps.dout, dout, B, N, Hq, d, dtype, "dout")) == ATTNFUSE_OK) {
+      (st = encode_bnhd(&maps.dout, dout, B, N, Hq, d, dtype, "dout")) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.q64, qr, B, N, Hq, d, dtype, "q'", 64)) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.k64, kr, B, Nk, Hkv, d, dtype, "k'", 64)) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.v64, v, B, Nk, Hkv, d, dtype, "v", 64)) == ATTNFUSE_OK &&
+      (st = encode_bnhd(&maps.dout64, dout, B, N, Hq, d, dtype, "dout", 64)) == ATTNFUSE_OK) {
     e = launch_attn_bwd(maps, p, d, dtype == ATTNFUSE_BF16, s);
     if (e != cudaSuccess) st = cuda_fail(e, "backward launch");
     if (st == ATTNFUSE_OK && !plain_form && (e = rotate(dq, dq, dk, dk, 1)) != cudaSuccess)

@@ -179,7 +179,8 @@ struct AttnBwdParams {
 };
 
 struct AttnBwdMaps {
-  CUtensorMap q, k, v, dout;  // q, k: the rotated copies
+  CUtensorMap q, k, v, dout;          // q, k: the rotated copies; boxes of 128 rows
+  CUtensorMap q64, k64, v64, dout64;  // the same tensors in boxes of 64 rows (the streamed tiles)
 };
 
 // Launches D = rowsum(dout * out), then the dK/dV and dQ kernels (rotated q, k already in place).
