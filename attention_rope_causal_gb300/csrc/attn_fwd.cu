@@ -801,12 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
               ptx::fence_proxy_async_smem();
               ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
-              if (i == 0) {
-                if (!(ok = rotate_q(U))) break;
-                // The key walk restarts exactly at tile 1, so it is not live (with the query walk)
-                // across the query rotation.
-                rope_cs8_exact((uint32_t)(BN + r0), sfreq, sfreq + 64, ck * 8, kcs);
-              }
+              if (i == 0 && !(ok = rotate_q(U))) break;
             }
             if (!ok) break;
           }
