@@ -193,7 +193,8 @@ struct Cfg {
 };
 
 struct __align__(8) Ctrl {
-  uint64_t q_full, q_ready, q_empty;
+  uint64_t q_full, q_empty;
+  uint64_t q_ready[2];  // query tile i rotated (by softmax warpgroup i)
   uint64_t k_full[KST], k_ready[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[2], p_full[2], o_full[2];
@@ -398,6 +399,13 @@ __device__ __forceinline__ int unit_of_round(int round, int c, int G) {
   return round * G + ((round & 1) ? (G - 1 - c) : c);
 }
 
+// The k-th unit of this CTA (the sequence FOR_EACH_UNIT walks), or -1 after its last.
+__device__ __forceinline__ int unit_at(int k, const AttnParams& p) {
+  if (k * (int)gridDim.x >= p.total_units) return -1;
+  const int u = unit_of_round(k, blockIdx.x, gridDim.x);
+  return u < p.total_units ? u : -1;
+}
+
 // Key tiles a query tile starting at row r needs: its last row r' = min(r + 127, N - 1) sees keys
 // up to q_off + r'.  With q_off = 0 (GENERAL = false) that is t + 1 for the tile starting at 128 t.
 template <bool GENERAL>
@@ -468,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar_addr(ctl.q_full), 1);
-    ptx::mbar_init(bar_addr(ctl.q_ready), 128);
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(bar_addr(ctl.q_ready[i]), 128);
     ptx::mbar_init(bar_addr(ctl.q_empty), 1);
     for (int s = 0; s < KST; ++s) {
       ptx::mbar_init(bar_addr(ctl.k_full[s]), 1);
@@ -603,7 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       FOR_EACH_UNIT(U) {
-        if (!(ok = I::wait(bar_addr(ROTATE ? ctl.q_ready : ctl.q_full), uc & 1, ctl, tmo))) break;
+        // With rotation each query tile has its own ready barrier (S0 may start before q1 is rotated).
+        if (!(ok = I::wait(bar_addr(ROTATE ? ctl.q_ready[0] : ctl.q_full), uc & 1, ctl, tmo))) break;
+        const uint32_t q1_parity = uc & 1;
         ++uc;
         ptx::tc_fence_after();
         for (int i = 0; i < U.n_kt && ok; ++i) {
@@ -617,6 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             I::commit(bar_addr(ctl.s_full[0]));
           }
           if (pend && !(ok = flush_pv1())) break;
+          if (ROTATE && i == 0) {
+            if (!(ok = I::wait(bar_addr(ctl.q_ready[1]), q1_parity, ctl, tmo))) break;
+            ptx::tc_fence_after();
+          }
           if (i < U.n1) {
             issue_S(1, kbase);
             I::commit(bar_addr(ctl.s_full[1]));
@@ -660,11 +674,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tS = tmem + lane_off + wi * BN;
       const uint32_t tO = tmem + lane_off + C::COL_O + wi * D;
       const float sl2 = p.scale_log2;
-      int gs = 0, uo = 0;
+      int gs = 0, uo = 0, uq = 0;
       bool ok = true;
-      FOR_EACH_UNIT(U) {
-        const int n_steps = wi == 0 ? U.n0 : U.n1;
-        if (n_steps == 0) continue;
+      // Fused: this warpgroup rotates its own query tile of every unit once the tile has landed --
+      // a CTA's first unit's at once, each next unit's right after this unit's last softmax step
+      // (before the epilogue: the next unit's first O += P V waits for that anyway) -- while the
+      // rotation warps turn K tiles; each query tile has its own ready barrier.  cos/sin walk along
+      // the thread's rows from the exact value at its first row.
+      auto rotate_own_q = [&](int u) -> bool {
+        if (!wait_bar_warp(bar_addr(ctl.q_full), uq & 1, ctl, tmo)) return false;
+        ++uq;
+        const Unit V = decode_unit<VARIANT>(u, p);
+        if (wi == 0 || V.active1) {
+          int ck, r0;
+          rot_mapping<D>((warp & 3) * 32 + lane, ck, r0);
+          RopeCS8 step, qcs;
+          rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
+          // Query row i sits at position q_off + i.  Calls with q_off != 0 run the VARIANT kernel.
+          int qpos0 = V.row(wi) + r0;
+          if constexpr (VARIANT) qpos0 += *reinterpret_cast<volatile int*>(&ctl.q_off);
+          rope_cs8_exact((uint32_t)qpos0, sfreq, sfreq + 64, ck * 8, qcs);
+          if constexpr (VARIANT)
+            rotate_tile_variant<D, BF16>(sQ + wi * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0,
+                                         p.qpos ? p.qpos + (size_t)V.b * p.N + V.row(wi) : nullptr,
+                                         p.N - V.row(wi), sfreq);
+          else
+            rotate_tile<D, BF16>(sQ + wi * C::TILE, r0, ck, qcs, step);
+          ptx::fence_proxy_async_smem();
+        }
+        ptx::mbar_arrive(bar_addr(ctl.q_ready[wi]));
+        return true;
+      };
+      if constexpr (ROTATE && ROT_K) {
+        const int u0 = unit_at(0, p);
+        if (u0 >= 0) ok = rotate_own_q(u0);
+      }
+      for (int k = 0, u; ok && (u = unit_at(k, p)) >= 0; ++k) {
+        const Unit U = decode_unit<VARIANT>(u, p);
+        const int n_steps = wi == 0 ? U.n0 : U.n1;  // 0: an inactive q1 (its key loop and epilogue skipped)
         const int qt = U.row(wi) / BM;
         // Key column c of tile j is visible to row r iff c <= q_off + qt*128 + r - j*128; tiles
         // j >= j_mask have that limit below 127 for some row and take the per-element mask (the
@@ -711,6 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive(bar_addr(ctl.p_full[wi]));
         }
         if (!ok) break;
+        if constexpr (ROTATE && ROT_K) {
+          const int un = unit_at(k + 1, p);
+          if (un >= 0 && !(ok = rotate_own_q(un))) break;
+        }
+        if (n_steps == 0) continue;
         if (!(ok = wait_bar_warp(bar_addr(ctl.o_full[wi]), uo & 1, ctl, tmo))) break;
         ++uo;
         ptx::tc_fence_after();
@@ -743,47 +795,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::setmaxnreg_dec<Regs<D, ROTATE>::kRotate>();
     if constexpr (ROTATE) {
       if (!skip) {
-        // ============================== Q and K tile rotation ===================================
+        // ================================ K tile rotation =======================================
         // cos/sin are carried along the thread's rows by angle addition with the exact rotation of
-        // RS rows: exact at the first row of a query tile, and for the keys exact at the first
-        // row of every 16th key tile (one fp32 rounding per step, at most 128 steps between exact
-        // values: relative drift < 1e-5).  Per unit: K_0, then the query tiles (they land after
-        // the previous unit's last QK^T), then K_1, K_2, ...
-        constexpr int kReseed = 16;
-        int ck, r0;
-        rot_mapping<D>(threadIdx.x - 384, ck, r0);
-        RopeCS8 step;
-        rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
-        int gk = 0, uc = 0;
-        bool ok = true;
-        // The unit's query tiles, once they have landed.
-        auto rotate_q = [&](const Unit& U) -> bool {
-          if (!wait_bar_warp(bar_addr(ctl.q_full), uc & 1, ctl, tmo)) return false;
-          ++uc;
-          for (int tq = 0; tq < (U.active1 ? 2 : 1); ++tq) {
-            RopeCS8 qcs;
-            // Query row i sits at position q_off + i.  Calls with q_off != 0 run the VARIANT
-            // kernel: the term alone made the default kernel 1.4% slower on GB300.
-            int qpos0 = U.row(tq) + r0;
-            if constexpr (VARIANT) qpos0 += *reinterpret_cast<volatile int*>(&ctl.q_off);
-            rope_cs8_exact((uint32_t)qpos0, sfreq, sfreq + 64, ck * 8, qcs);
-            if constexpr (VARIANT)
-              rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks, p.interleaved != 0,
-                                           p.qpos ? p.qpos + (size_t)U.b * p.N + U.row(tq) : nullptr,
-                                           p.N - U.row(tq), sfreq);
-            else
-              rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
-          }
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(bar_addr(ctl.q_ready));
-          return true;
-        };
+        // RS rows, exact at the first row of every 16th key tile (one fp32 rounding per step, at most
+        // 128 steps between exact values: relative drift < 1e-5).  Fused: the query tiles are
+        // rotated by the softmax warpgroups.  Split: K arrives rotated (the pre-rotation pass) and
+        // these warps rotate the query tiles instead, each arriving on its own ready barrier.
         if constexpr (!ROT_K) {
-          // Split mode: K arrives rotated (the pre-rotation pass); only the query tiles turn here.
+          int ck, r0;
+          rot_mapping<D>(threadIdx.x - 384, ck, r0);
+          RopeCS8 step;
+          rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
+          int uc = 0;
           FOR_EACH_UNIT(U) {
-            if (!(ok = rotate_q(U))) break;
+            if (!wait_bar_warp(bar_addr(ctl.q_full), uc & 1, ctl, tmo)) break;
+            ++uc;
+            for (int tq = 0; tq < 2; ++tq) {
+              if (tq == 0 || U.active1) {
+                RopeCS8 qcs;
+                int qpos0 = U.row(tq) + r0;
+                if constexpr (VARIANT) qpos0 += *reinterpret_cast<volatile int*>(&ctl.q_off);
+                rope_cs8_exact((uint32_t)qpos0, sfreq, sfreq + 64, ck * 8, qcs);
+                if constexpr (VARIANT)
+                  rotate_tile_variant<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step, p.rot_chunks,
+                                               p.interleaved != 0,
+                                               p.qpos ? p.qpos + (size_t)U.b * p.N + U.row(tq) : nullptr,
+                                               p.N - U.row(tq), sfreq);
+                else
+                  rotate_tile<D, BF16>(sQ + tq * C::TILE, r0, ck, qcs, step);
+                ptx::fence_proxy_async_smem();
+              }
+              ptx::mbar_arrive(bar_addr(ctl.q_ready[tq]));
+            }
           }
-        } else {
+        }
+        if constexpr (ROT_K) {
+          constexpr int kReseed = 16;
+          int ck, r0;
+          rot_mapping<D>(threadIdx.x - 384, ck, r0);
+          RopeCS8 step;
+          rope_cs8_exact((uint32_t)RotGeom<D>::RS, sfreq, sfreq + 64, ck * 8, step);
+          int gk = 0;
+          bool ok = true;
           FOR_EACH_UNIT(U) {
             RopeCS8 kcs;
             for (int i = 0; i < U.n_kt && ok; ++i) {
@@ -801,7 +854,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rotate_tile<D, BF16>(sK + ks * C::TILE, r0, ck, kcs, step);
               ptx::fence_proxy_async_smem();
               ptx::mbar_arrive(bar_addr(ctl.k_ready[ks]));
-              if (i == 0 && !(ok = rotate_q(U))) break;
             }
             if (!ok) break;
           }
