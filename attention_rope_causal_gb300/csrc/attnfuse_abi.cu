@@ -325,12 +325,13 @@ attnfuse_mode_t attnfuse_select_mode(int B, int Hq, int Hkv, int N, int d, attnf
   (void)dtype;
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0) return ATTNFUSE_FUSED;
   // Measured on GB300 (bench.py --sweep, N from 1024 to 16384 at 16384 tokens, bf16 and fp16): with
-  // 4:1 GQA, rotating K in a pass and Q on chip (split) is fastest at 12 of the 14 points (pre-rotation
-  // at N = 16384, within 0.4%) and fused is slowest everywhere; with MHA d = 64, fused is fastest at
-  // N = 1024 and 1536 and pre-rotation from N = 2048 (interpolated crossover N* = 1862 in bf16, 1865
-  // in fp16), split within 1% of pre-rotation.
+  // 4:1 GQA, rotating K in a pass and Q on chip (split) is fastest at all 14 points (fused beats
+  // pre-rotation only below N* = 1244 in bf16, 1347 in fp16); with MHA d = 64, fused is fastest at
+  // N = 1024 and 1536, pre-rotation at 2048 (interpolated fused-vs-pre-rotate N* = 1892 in both
+  // dtypes), pre-rotation and split tie at 4096 and split leads (by 0.9-1.7%) from 5500 on.
   if (Hq / Hkv >= 2) return N >= 1024 ? ATTNFUSE_SPLIT : ATTNFUSE_FUSED;
-  return N >= 1864 ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
+  if (N >= 4096) return ATTNFUSE_SPLIT;
+  return N >= 1892 ? ATTNFUSE_PREROTATE : ATTNFUSE_FUSED;
 }
 
 size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_mode_t mode, attnfuse_dtype_t dtype) {

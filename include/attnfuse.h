@@ -103,10 +103,10 @@ size_t attnfuse_workspace_bytes(int B, int Hq, int Hkv, int N, int d, attnfuse_m
 /*
  * The fastest mode for a shape on GB300, from the measured sweep of all three ("Rotation Calculus" in
  * "AttnFuse Makes RoPE a First-Class Attention Compilation Operation", paragraph 2, made a runtime
- * choice): grouped-query attention (Hq / Hkv >= 2) with N >= 1024 -> SPLIT (fastest at 12 of 14
- * measured points from 1024 to 16384, pre-rotation at the other two, within 0.4%); multi-head
- * attention (Hq == Hkv) with N >= 1864 -> PREROTATE (measured N* = 1862 to 1865 against FUSED);
- * else -> FUSED.
+ * choice): grouped-query attention (Hq / Hkv >= 2) with N >= 1024 -> SPLIT (fastest at all 14
+ * measured points from 1024 to 16384); multi-head attention (Hq == Hkv) with N >= 4096 -> SPLIT
+ * (tied with pre-rotation at 4096, ahead from 5500), with 1892 <= N < 4096 -> PREROTATE (measured
+ * N* = 1892 against FUSED); else -> FUSED.
  * Host-only and pure: no device access; arguments it cannot classify (non-positive sizes, Hq not a
  * multiple of Hkv) give FUSED.
  */

@@ -91,7 +91,8 @@ def test_workspace_bytes(lib):
 @pytest.mark.parametrize("B,Hq,Hkv,N,mode", [
     (1, 32, 8, 4096, 3), (4, 32, 8, 2048, 3), (1, 32, 8, 16384, 3), (16, 32, 8, 1024, 3),  # GQA 4:1
     (8, 32, 8, 1023, 0), (1, 8, 4, 3000, 3), (1, 64, 8, 1023, 0),                          # other groups
-    (2, 16, 16, 1536, 0), (1, 16, 16, 1863, 0), (1, 16, 16, 1864, 1), (1, 16, 16, 32768, 1),  # MHA
+    (2, 16, 16, 1536, 0), (1, 16, 16, 1891, 0), (1, 16, 16, 1892, 1), (1, 16, 16, 4095, 1),  # MHA
+    (1, 16, 16, 4096, 3), (1, 16, 16, 32768, 3),
     (0, 16, 16, 4096, 0), (1, 6, 4, 4096, 0),                                          # not classified
 ])
 def test_select_mode_follows_the_measured_crossover(lib, B, Hq, Hkv, N, mode):
@@ -113,6 +114,8 @@ def test_auto_mode_workspace_is_that_of_the_selected_mode(lib):
         assert lib.attnfuse_workspace_bytes(*shape, 2, 0) == lib.attnfuse_workspace_bytes(*shape, sel, 0)
     assert binding.select_mode(1, 32, 8, 4096, 128) == "split"
     assert binding.select_mode(2, 16, 16, 1536, 64) == "fused"
+    assert binding.select_mode(1, 16, 16, 2048, 64) == "prerotate"
+    assert binding.select_mode(1, 16, 16, 8192, 64) == "split"
 
 
 @pytest.mark.parametrize("r,il,status", [(8, 0, 1), (24, 0, 1), (80, 1, 1), (-16, 0, 1), (64, 2, 1), (64, -1, 1)])
