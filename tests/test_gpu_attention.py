@@ -155,10 +155,12 @@ def test_running_max_jumps(mode, dt, Hq):
     assert_close(out.double().numpy(), lse.double().numpy(), o_ref, l_ref, dt, f"max jumps {mode} {dt}")
 
 
-@pytest.mark.parametrize("shape", [(1, 2048, 4, 2, 64, "bf16"), (1, 300, 4, 4, 64, "fp16")])
+@pytest.mark.parametrize("shape", [(1, 2048, 4, 2, 64, "bf16"), (1, 300, 4, 4, 64, "fp16"),
+                                   (1, 2048, 2, 2, 64, "fp16"), (1, 4096, 2, 2, 64, "bf16")])
 def test_auto_mode_runs_the_selected_mode(shape):
-    # mode "auto" resolves on the host to fused or pre-rotate (attnfuse_select_mode) and then runs
-    # exactly that path: bitwise the same result, and within the oracle tolerance.
+    # mode "auto" resolves on the host to one of fused, pre-rotate and split (attnfuse_select_mode:
+    # here split for GQA, then fused, pre-rotate and split for MHA as N grows) and then runs exactly
+    # that path: bitwise the same result, and within the oracle tolerance.
     B, N, Hq, Hkv, d, dt = shape
     q, k, v = draw(B, N, Hq, Hkv, d, dt, seed=31)
     sel = binding.select_mode(B, Hq, Hkv, N, d, q.dtype)
